@@ -1,0 +1,566 @@
+"""Benchmark of the folded-Hadamard ternary Packed layer on GB300.
+
+Default workload (one "step" = one decode token, M = 1): the embedding lookup of
+one token id plus the 401 packed linears of a synthetic 64-layer Bonsai-2 27B text
+stack (48 linear-attention layers: in_proj_qkv, in_proj_z, out_proj; 16 full-
+attention layers: q, k, v, o; 64 MLPs: gate, up, down; lm_head), every linear
+the fused sign*FWHT + W2-g128 GEMV.  25.1e9 weights = 7.06 GB of packed codes,
+scales and biases stream from HBM per token; the step is replayed as one CUDA
+graph.  Weights are far larger than L2, so no flush is needed between steps.
+
+Prints ONE JSON line (rank 0).  ``--config`` picks other workloads for profiling
+(layers, prefill, batched, embed, all); they print one JSON line each.
+``--impl reference`` times the float64 CPU oracle on a bounded sample instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import tb_inputs as ti  # noqa: E402
+
+METRIC = "decode tok/s at 27B shapes (M=1) + fused W2 GEMV HBM GB/s as % of GB300 peak"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return (float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", 0)),
+                "measured")
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+# ---------------------------------------------------------------------------- distributed
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+class Dist:
+    def __init__(self, backend):
+        import torch
+        import torch.distributed as td
+
+        self.world, self.rank, self.local = dist_env()
+        self.td = td if self.world > 1 else None
+        if self.td is not None:
+            os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+            td.init_process_group(backend)
+        self.torch = torch
+
+    def barrier(self):
+        if self.td is not None:
+            self.td.barrier()
+
+    def max(self, v: float) -> float:
+        if self.td is None:
+            return v
+        t = self.torch.tensor([v], dtype=self.torch.float64,
+                              device="cuda" if self.td.get_backend() == "nccl" else "cpu")
+        self.td.all_reduce(t, op=self.td.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.td is not None:
+            self.td.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------- clocks
+class Clocks:
+    """nvidia-smi sampling during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, mx, reasons = [], None, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx = float(f[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------- GPU workloads
+class Packed:
+    """One packed W2-g128 linear on the device (codes drawn by the device generator)."""
+
+    def __init__(self, tb, tdev, torch, seed, N, K, tmp):
+        dev = torch.device("cuda")
+        self.N, self.K, self.G = N, K, K // 128
+        self.w = torch.empty((N, K // 16), dtype=torch.int32, device=dev)
+        self.s = torch.empty((N, self.G), dtype=torch.float16, device=dev)
+        self.b = torch.empty((N, self.G), dtype=torch.float16, device=dev)
+        step = tmp.numel() // K
+        for r0 in range(0, N, step):
+            n = min(step, N - r0)
+            c = tmp[: n * K].view(n, K)
+            tdev.fill_codes(c, seed, r0, K)
+            tdev.fill_scales(self.s[r0:r0 + n], seed, r0, self.G)
+            tb.tb_pack_w2(c, self.s[r0:r0 + n], self.w[r0:r0 + n], self.b[r0:r0 + n])
+
+    @property
+    def algo_bytes(self):
+        return ti.packed_bytes(self.K, self.N)
+
+
+def build_sweep(tb, tdev, torch):
+    dev = torch.device("cuda")
+    tmp = torch.empty(1 << 30, dtype=torch.int8, device=dev)
+    layers = []
+    for i, (name, K, N) in enumerate(ti.sweep_layers()):
+        layers.append((name, Packed(tb, tdev, torch, ti.config_seed(3, i), N, K, tmp)))
+    emb = Packed(tb, tdev, torch, ti.config_seed(3, 999), ti.VOCAB, ti.HIDDEN, tmp)
+    del tmp
+    torch.cuda.synchronize()
+    xs = {K: torch.from_numpy(ti.activations(ti.config_seed(3, 1000 + K), 1, K)).to(dev)
+          for K in (ti.HIDDEN, 6144, ti.MLP)}
+    signs = {K: torch.from_numpy(ti.rademacher_signs(ti.config_seed(3, 2000 + K), K)).to(dev)
+             for K in (ti.HIDDEN, 6144, ti.MLP)}
+    ymax = max(p.N for _, p in layers)
+    y = torch.empty((1, ymax), dtype=torch.float16, device=dev)
+    return layers, emb, xs, signs, y
+
+
+def sweep_step(tb, layers, emb, xs, signs, y, ids, e_out, status):
+    """One decode token: embedding lookup + 401 fused FWHT/GEMV linears."""
+    tb.tb_embed_lookup(ids, emb.w, emb.s, emb.b, signs[ti.HIDDEN], 1024, e_out, status)
+    for _, p in layers:
+        tb.tb_packed_linear(xs[p.K], signs[p.K], 1024, p.w, p.s, p.b, y[:, : p.N], None, status)
+
+
+def linears_only(tb, layers, xs, signs, y, status):
+    for _, p in layers:
+        tb.tb_packed_linear(xs[p.K], signs[p.K], 1024, p.w, p.s, p.b, y[:, : p.N], None, status)
+
+
+def time_graph(torch, graph, steps, dist):
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    dist.barrier()
+    torch.cuda.synchronize()
+    start.record()
+    for _ in range(steps):
+        graph.replay()
+    end.record()
+    torch.cuda.synchronize()
+    dist.barrier()
+    return start.elapsed_time(end) / 1e3
+
+
+def capture(torch, fn):
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn()  # attributes set, lazy loads done before capture
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    torch.cuda.synchronize()
+    return g
+
+
+def cpu_baseline_sample(budget_s: float = 12.0):
+    """The float64 oracle on sampled rows of every distinct sweep shape, M = 1.
+
+    Returns (tok/s extrapolated to the full 401-linear step + embedding, description).
+    """
+    import oracle
+
+    shapes = {}
+    for _, K, N in ti.sweep_layers():
+        shapes[(K, N)] = shapes.get((K, N), 0) + 1
+    per_shape = budget_s / len(shapes)
+    sec_per_token = 0.0
+    desc = []
+    for (K, N), count in sorted(shapes.items()):
+        x = ti.activations(7, 1, K)
+        sg = ti.rademacher_signs(7, K)
+        rows = 64
+        while True:
+            codes = ti.ternary_codes(11, 0, rows, K)
+            sc = ti.group_scales(11, 0, rows, K // 128)
+            w = oracle.pack_w2(codes)
+            b = oracle.biases_for(sc)
+            t0 = time.perf_counter()
+            oracle.packed_linear(x, sg, 1024, w, sc, b)
+            dt = time.perf_counter() - t0
+            if dt > per_shape / 3 or rows >= N:
+                break
+            rows = min(N, rows * 4)
+        sec_per_token += count * dt * (N / rows)
+        desc.append(f"{K}->{N}x{count}: {rows} rows")
+    # embedding of one id: dequantise one 5120 row + inverse transform
+    codes = ti.ternary_codes(12, 0, 16, ti.HIDDEN)
+    sc = ti.group_scales(12, 0, 16, ti.HIDDEN // 128)
+    w = oracle.pack_w2(codes)
+    t0 = time.perf_counter()
+    oracle.embed_lookup(np.arange(16), w, sc, oracle.biases_for(sc), ti.rademacher_signs(1, ti.HIDDEN), 1024)
+    sec_per_token += (time.perf_counter() - t0) / 16
+    return 1.0 / sec_per_token, "; ".join(desc)
+
+
+def run_sweep(args, dist, tb, tdev, torch):
+    hbm, _, _, peak_kind = peaks()
+    layers, emb, xs, signs, y = build_sweep(tb, tdev, torch)
+    dev = torch.device("cuda")
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    ids = torch.tensor([int(ti.token_ids(ti.config_seed(3, 3000), 1, ti.VOCAB)[0])], dtype=torch.int32,
+                       device=dev)
+    e_out = torch.empty((1, ti.HIDDEN), dtype=torch.float16, device=dev)
+
+    step_graph = capture(torch, lambda: sweep_step(tb, layers, emb, xs, signs, y, ids, e_out, status))
+    gemv_graph = capture(torch, lambda: linears_only(tb, layers, xs, signs, y, status))
+    launches_per_step = 1 + len(layers)
+
+    for _ in range(args.warmup):
+        step_graph.replay()
+    torch.cuda.synchronize()
+    clocks = Clocks(dist.local)
+    clocks.start()
+    secs = dist.max(time_graph(torch, step_graph, args.steps, dist))
+    clk = clocks.stop()
+    # the dominant kernel alone: the 401 fused FWHT + GEMV launches
+    for _ in range(2):
+        gemv_graph.replay()
+    gsecs = dist.max(time_graph(torch, gemv_graph, args.steps, dist))
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+
+    gemv_bytes = sum(p.algo_bytes for _, p in layers)
+    gemv_launch_s = gsecs / (args.steps * len(layers))
+    achieved = gemv_bytes / len(layers) / gemv_launch_s / 1e9
+
+    # end to end through the public C ABI with host buffers: H2D of the token id,
+    # the 402 calls, D2H of the logits, every step
+    h_id = torch.empty(1, dtype=torch.int32).pin_memory()
+    h_id[0] = int(ids[0])
+    h_logits = torch.empty((1, ti.VOCAB), dtype=torch.float16).pin_memory()
+    for _ in range(2):
+        ids.copy_(h_id, non_blocking=True)
+        sweep_step(tb, layers, emb, xs, signs, y, ids, e_out, status)
+        h_logits.copy_(y[:, : ti.VOCAB], non_blocking=True)
+    torch.cuda.synchronize()
+    dist.barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        ids.copy_(h_id, non_blocking=True)
+        sweep_step(tb, layers, emb, xs, signs, y, ids, e_out, status)
+        h_logits.copy_(y[:, : ti.VOCAB], non_blocking=True)
+    torch.cuda.synchronize()
+    e2e_s = dist.max(time.perf_counter() - t0)
+    dist.barrier()
+
+    n = dist.world
+    line = {
+        "metric": METRIC,
+        "value": round(n * args.steps / secs, 3),
+        "unit": "tok/s",
+        "n_gpus": n,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(secs / args.steps * 1e3, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f16",
+        "data": "synthetic",
+        "config": {
+            "workload": "decode step, M=1: embedding of 1 id + 401 fused sign*FWHT-1024 + W2-g128 "
+                        "GEMV linears of a 64-layer 27B stack (hidden 5120, MLP 17408, vocab 248320)",
+            "weights_gb_per_step": round((gemv_bytes + ti.HIDDEN // 4 + ti.HIDDEN // 32) / 1e9, 4),
+            "l2": "no flush: 7.06 GB of weights per step, far larger than the 129 MB L2",
+            "graph": "one CUDA graph per step",
+            "parallelism": f"replicas x{n}",
+        },
+        "roofline": {
+            "bound": "hbm",
+            "achieved": round(achieved, 1),
+            "peak": hbm,
+            "unit": "GB/s",
+            "frac": round(achieved / hbm, 4),
+            "traffic": None,
+            "kernel": "w2_gemv_kernel<1> (fused FWHT prologue + W2-g128 GEMV), 401 launches averaged",
+            "peak_kind": f"{peak_kind} hbm_gbs",
+        },
+        "e2e": {
+            "value": round(n * args.steps / e2e_s, 3),
+            "unit": "tok/s",
+            "h2d_bytes_per_step": 4,
+            "d2h_bytes_per_step": ti.VOCAB * 2,
+            "note": "402 C-ABI calls per step on the host, no graph",
+        },
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+    }
+    if dist.rank == 0 and n == 1 and not args.no_cpu_baseline:
+        v, desc = cpu_baseline_sample()
+        line["cpu_baseline"] = {"value": round(v, 6), "unit": "tok/s",
+                                "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+                                "sample": "float64 NumPy oracle, M=1, sampled rows of every distinct "
+                                          "sweep shape, extrapolated to the 401 linears + embedding: " + desc}
+    return line
+
+
+def run_layers(args, dist, tb, tdev, torch):
+    """Per-shape decode GEMV at the 27B layer shapes (M = 1)."""
+    hbm, _, _, peak_kind = peaks()
+    dev = torch.device("cuda")
+    tmp = torch.empty(1 << 30, dtype=torch.int8, device=dev)
+    rows = []
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    for name, K, N in ti.LAYER_SHAPES + [("qkv", 5120, 10240), ("lm_head", 5120, ti.VOCAB)]:
+        # enough distinct copies that one pass exceeds L2
+        copies = max(1, -(-(512 << 20) // ti.packed_bytes(K, N)))
+        ps = [Packed(tb, tdev, torch, ti.config_seed(2, j), N, K, tmp) for j in range(copies)]
+        x = torch.from_numpy(ti.activations(5, 1, K)).to(dev)
+        sg = torch.from_numpy(ti.rademacher_signs(5, K)).to(dev)
+        y = torch.empty((1, N), dtype=torch.float16, device=dev)
+
+        def fn():
+            for p in ps:
+                tb.tb_packed_linear(x, sg, 1024, p.w, p.s, p.b, y, None, status)
+
+        g = capture(torch, fn)
+        for _ in range(3):
+            g.replay()
+        reps = max(3, args.steps)
+        secs = time_graph(torch, g, reps, dist)
+        per = secs / (reps * copies)
+        gbs = ti.packed_bytes(K, N) / per / 1e9
+        rows.append({"shape": f"{name} {K}->{N}", "us": round(per * 1e6, 2), "GB/s": round(gbs, 1),
+                     "frac": round(gbs / hbm, 4), "copies": copies})
+        del ps
+    del tmp
+    return {"metric": "decode GEMV per layer shape (M=1)", "unit": "GB/s", "peak": hbm,
+            "peak_kind": peak_kind, "layers": rows}
+
+
+def run_prefill(args, dist, tb, tdev, torch):
+    _, tf, tfs, peak_kind = peaks()
+    dev = torch.device("cuda")
+    tmp = torch.empty(1 << 30, dtype=torch.int8, device=dev)
+    rows = []
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    for M in (512, 4096):
+        for K, N in ((5120, 17408), (17408, 5120)):
+            p = Packed(tb, tdev, torch, ti.config_seed(4, K), N, K, tmp)
+            x = torch.from_numpy(ti.activations(4, M, K)).to(dev)
+            sg = torch.from_numpy(ti.rademacher_signs(4, K)).to(dev)
+            y = torch.empty((M, N), dtype=torch.float16, device=dev)
+            ws = torch.empty(tb.tb_packed_linear_workspace_size(M, K, N), dtype=torch.uint8, device=dev)
+            flush = torch.empty(256 << 20, dtype=torch.int8, device=dev)
+
+            def fn():
+                tb.tb_packed_linear(x, sg, 1024, p.w, p.s, p.b, y, ws, status)
+
+            for _ in range(3):
+                fn()
+            torch.cuda.synchronize()
+            reps = max(3, args.steps)
+            tot = 0.0
+            for _ in range(reps):
+                flush.zero_()  # L2 flush between timed iterations
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                fn()
+                b.record()
+                torch.cuda.synchronize()
+                tot += a.elapsed_time(b) / 1e3
+            per = tot / reps
+            tflops = 2.0 * M * N * K / per / 1e12
+            rows.append({"shape": f"M={M} {K}->{N}", "ms": round(per * 1e3, 4), "TFLOP/s": round(tflops, 1),
+                         "frac": round(tflops / tf, 4)})
+            del p, x, y, ws, flush
+    del tmp
+    return {"metric": "prefill GEMM (FWHT prologue + tcgen05 GEMM)", "unit": "TFLOP/s", "peak": tf,
+            "peak_kind": f"{peak_kind} bf16 burst (fp16 dense rate equal)", "rows": rows}
+
+
+def run_batched(args, dist, tb, tdev, torch):
+    hbm, _, _, peak_kind = peaks()
+    dev = torch.device("cuda")
+    tmp = torch.empty(1 << 30, dtype=torch.int8, device=dev)
+    K, N = 5120, 17408
+    copies = 8
+    ps = [Packed(tb, tdev, torch, ti.config_seed(5, j), N, K, tmp) for j in range(copies)]
+    del tmp
+    sg = torch.from_numpy(ti.rademacher_signs(5, K)).to(dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    rows = []
+    for M in (1, 2, 4, 8, 16, 32, 64):
+        x = torch.from_numpy(ti.activations(5, M, K)).to(dev)
+        y = torch.empty((M, N), dtype=torch.float16, device=dev)
+        nws = tb.tb_packed_linear_workspace_size(M, K, N)
+        ws = torch.empty(max(nws, 16), dtype=torch.uint8, device=dev) if nws else None
+
+        def fn():
+            for p in ps:
+                tb.tb_packed_linear(x, sg, 1024, p.w, p.s, p.b, y, ws, status)
+
+        g = capture(torch, fn)
+        for _ in range(3):
+            g.replay()
+        reps = max(3, args.steps)
+        per = time_graph(torch, g, reps, dist) / (reps * copies)
+        gbs = ti.packed_bytes(K, N) / per / 1e9
+        rows.append({"M": M, "us": round(per * 1e6, 2), "GB/s": round(gbs, 1), "frac": round(gbs / hbm, 4),
+                     "TFLOP/s": round(2 * M * N * K / per / 1e12, 2)})
+    return {"metric": "batched decode 5120->17408", "unit": "GB/s", "peak": hbm, "peak_kind": peak_kind,
+            "rows": rows}
+
+
+def run_embed(args, dist, tb, tdev, torch):
+    hbm, _, _, peak_kind = peaks()
+    dev = torch.device("cuda")
+    tmp = torch.empty(1 << 30, dtype=torch.int8, device=dev)
+    V, D, T = ti.VOCAB, ti.HIDDEN, 256
+    p = Packed(tb, tdev, torch, ti.config_seed(5, 99), V, D, tmp)
+    del tmp
+    sg = torch.from_numpy(ti.rademacher_signs(5, D)).to(dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    rows = []
+    for r in range(max(3, args.steps)):
+        ids = torch.from_numpy(ti.token_ids(100 + r, T, V)).to(dev)
+        out = torch.empty((T, D), dtype=torch.float16, device=dev)
+        flush = torch.empty(256 << 20, dtype=torch.int8, device=dev)
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        tb.tb_embed_lookup(ids, p.w, p.s, p.b, sg, 1024, out, status)
+        b.record()
+        torch.cuda.synchronize()
+        rows.append(a.elapsed_time(b) / 1e3)
+    per = float(np.median(rows[1:]))
+    byts = T * (D // 4 + D // 64) + T * D * 2
+    return {"metric": "embedding lookup 256 ids, 248320x5120 packed table", "us": round(per * 1e6, 2),
+            "GB/s": round(byts / per / 1e9, 1), "peak": hbm, "peak_kind": peak_kind}
+
+
+# ---------------------------------------------------------------------------- reference arm
+def run_reference(args):
+    """The float64 CPU oracle as the reference arm: bounded sample per step."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return None
+    import oracle
+
+    shapes = {}
+    for _, K, N in ti.sweep_layers():
+        shapes[(K, N)] = shapes.get((K, N), 0) + 1
+    rows = 32
+
+    def one_step():
+        sec = 0.0
+        for (K, N), count in sorted(shapes.items()):
+            x = ti.activations(7, 1, K)
+            sg = ti.rademacher_signs(7, K)
+            codes = ti.ternary_codes(11, 0, rows, K)
+            sc = ti.group_scales(11, 0, rows, K // 128)
+            w = oracle.pack_w2(codes)
+            t0 = time.perf_counter()
+            oracle.packed_linear(x, sg, 1024, w, sc, oracle.biases_for(sc))
+            sec += count * (time.perf_counter() - t0) * N / rows
+        return sec
+
+    for _ in range(args.warmup):
+        one_step()
+    t = [one_step() for _ in range(args.steps)]
+    sec = float(np.mean(t))
+    v = 1.0 / sec
+    return {"impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": "tok/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sec * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": "decode step, M=1: 401 W2-g128 linears of the 64-layer 27B stack "
+                                   "(float64 CPU oracle, extrapolated from sampled rows)"},
+            "cpu_baseline": {"value": round(v, 6), "unit": "tok/s", "cores": len(os.sched_getaffinity(0)),
+                             "kind": "oracle",
+                             "sample": f"{rows} rows of each distinct shape per step, extrapolated"},
+            "e2e": {"value": round(v, 6), "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="sweep", choices=["sweep", "layers", "prefill", "batched", "embed", "all"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    if args.impl == "reference":
+        line = run_reference(args)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+
+    import torch
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dist = Dist("nccl")
+    import ternary_hadamard_rotated_gb300 as tb
+    from tb_inputs import device as tdev
+
+    tb.load()
+    configs = ["sweep", "layers", "prefill", "batched", "embed"] if args.config == "all" else [args.config]
+    for c in configs:
+        fn = {"sweep": run_sweep, "layers": run_layers, "prefill": run_prefill, "batched": run_batched,
+              "embed": run_embed}[c]
+        line = fn(args, dist, tb, tdev, torch)
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+        torch.cuda.empty_cache()
+    dist.close()
+
+
+if __name__ == "__main__":
+    main()

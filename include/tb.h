@@ -1,0 +1,167 @@
+/*
+ * tb.h — C ABI of the folded-Hadamard ternary "Packed" layer on one GB300 (sm_103a).
+ *
+ * The layer (restated from two pages about the Ternary-Bonsai-2-27B-mlx-2bit pack):
+ *   [ARCH] "3.9GB 里藏了什么Bonsai 的混合注意力 推测解码 262K 上下文端侧架构逐层拆"
+ *          (kwkr.cn/news/564617), sections "Hadamard 旋转把量化误差抹平的免费午餐" and
+ *          "打包格式的工程MLX 2.25 bits 与 GGUF 的两种装箱";
+ *   [PACK] PACK-RUNTIME.md walkthrough (lpnh.cn/news/2438023), sections
+ *          "文本模型加载artifact.load_model 与 Packed 模块" and
+ *          "仿射 2-bit 格式与 Prism contract v1".
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - All array arguments are DEVICE pointers owned by the caller; the library
+ *    allocates no device memory and keeps no state between calls.
+ *  - fp16 arrays are passed as uint16_t* holding IEEE binary16 bit patterns.
+ *  - Every array is row-major and contiguous.  Device pointers must be 16-byte
+ *    aligned (TB_ERR_ALIGN otherwise).
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Every call is
+ *    asynchronous on that stream; the return value reports argument validation
+ *    and launch errors only.  Errors that depend on data (a bad code, an id out
+ *    of range, a bounded wait that ran out) are OR-ed into the optional device
+ *    word `dev_status` (TB_DEV_* bits), which the caller reads after a sync.
+ *    Kernels never trap.
+ *  - The layer refuses rather than guesses: a shape, block or group size it
+ *    does not implement is an error, never a silent fallback.
+ *  - Codes: ternary t in {-1,0,1} is stored as q = t + 1 in {0,1,2}; a uint32
+ *    word holds 16 codes, code i of the word at bits 2i..2i+1 (least
+ *    significant first); word j of a row holds the row's codes 16j..16j+15.
+ *  - Group size 128 and 2 bits per code are fixed.  Per group: one fp16 scale s
+ *    and one fp16 bias b (= -s in the pack); a code decodes to s*q + b.
+ *  - Hadamard block: 1024 (the pack's block_size) or 0 (= module not folded,
+ *    no transform).  The transform is the normalised Sylvester-Walsh-Hadamard
+ *    matrix in natural order, H[i][j] = (-1)^popcount(i&j), scaled by
+ *    1/sqrt(1024) = 1/32, applied to consecutive 1024-element blocks of the
+ *    last axis; the sign vector is indexed by the absolute position on that axis.
+ */
+#ifndef TB_H
+#define TB_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* return codes */
+enum {
+  TB_OK = 0,
+  TB_ERR_NULL = -1,        /* a required pointer is NULL */
+  TB_ERR_SHAPE = -2,       /* M, N, K, T, V or D out of range or not a multiple it must be */
+  TB_ERR_UNSUPPORTED = -3, /* block other than 0 or 1024, or an algorithm not built */
+  TB_ERR_VALUE = -4,       /* a host-checked value is invalid */
+  TB_ERR_CUDA = -5,        /* a CUDA launch or query failed (see tb_last_cuda_error) */
+  TB_ERR_ALIGN = -6,       /* a device pointer is not 16-byte aligned */
+  TB_ERR_WORKSPACE = -7    /* workspace NULL or smaller than the size query returned */
+};
+
+/* bits OR-ed into *dev_status by kernels */
+#define TB_DEV_BAD_CODE 1  /* tb_pack_w2: a code outside {-1,0,1} */
+#define TB_DEV_BAD_ID 2    /* tb_embed_lookup: an id outside [0, V) (its row is written as zeros) */
+#define TB_DEV_TIMEOUT 4   /* a bounded wait inside a kernel gave up; outputs are not valid */
+
+/* algorithm choice for tb_packed_linear_algo */
+#define TB_ALGO_AUTO 0     /* GEMV for M <= 8, tensor-core GEMM above */
+#define TB_ALGO_GEMV 1     /* fused sign*FWHT prologue + streaming W2 GEMV; any M (passes of 8 tokens) */
+#define TB_ALGO_TC 2       /* FWHT kernel into the workspace + tcgen05/TMEM GEMM; any M */
+
+/* Human-readable text of a return code; never NULL. */
+const char* tb_status_string(int status);
+
+/* Text of the last CUDA error seen by this thread's calls (or ""). */
+const char* tb_last_cuda_error(void);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int tb_version(void);
+
+/*
+ * tb_pack_w2 — weight packer of the W2-g128 affine container.
+ * [ARCH] "打包格式的工程": codes {0,1,2} rearranged into uint32 words; bias = -scale.
+ *   codes   int8 [N, K], values in {-1,0,1}
+ *   scales  fp16 [N, K/128]
+ *   w       uint32 [N, K/16]   (out) packed codes, layout as above
+ *   biases  fp16 [N, K/128]    (out) -scales (sign bit flipped; exact)
+ *   dev_status optional int32: TB_DEV_BAD_CODE if a code is not -1, 0 or 1
+ *              (that field is still written, as (t+1) & 3).
+ * K must be a positive multiple of 128, N >= 1.
+ */
+int tb_pack_w2(const int8_t* codes, const uint16_t* scales, int64_t N, int64_t K,
+               uint32_t* w, uint16_t* biases, int32_t* dev_status, void* stream);
+
+/*
+ * tb_unpack_w2 — inverse of the packer (verification support).
+ * [ARCH] "打包格式的工程": the codec ships an independent unpack() to check the packing.
+ *   w      uint32 [N, K/16];  codes int8 [N, K] (out) = q - 1 (a field q = 3 gives 2).
+ * K must be a positive multiple of 16, N >= 1.
+ */
+int tb_unpack_w2(const uint32_t* w, int64_t N, int64_t K, int8_t* codes, void* stream);
+
+/*
+ * tb_fwht — sign * normalised Walsh-Hadamard transform over blocks of 1024.
+ * [ARCH] "Hadamard 旋转": fwht uses hadamard_transform with scale 1/sqrt(block);
+ * forward multiplies by the signs first, the inverse multiplies by them again at the end.
+ *   x  fp16 [M, K];  y fp16 [M, K] (out; y may equal x);
+ *   signs int8 [K] of +-1, or NULL for all +1 (not checked on the device);
+ *   forward (inverse = 0): y = (H/32) (signs * x) per block;
+ *   inverse (inverse = 1): y = signs * ((H/32) x) per block.
+ * Computed in fp32, rounded to fp16 (round to nearest even).  block must be 1024,
+ * K a positive multiple of 1024, M >= 1.
+ */
+int tb_fwht(const uint16_t* x, uint16_t* y, const int8_t* signs, int64_t M, int64_t K,
+            int block, int inverse, void* stream);
+
+/*
+ * Bytes of workspace tb_packed_linear needs for these sizes (0 when the GEMV
+ * path is taken and needs none).  The workspace holds the rotated activations
+ * x' (fp16 [M, K]) for the tensor-core path.
+ */
+size_t tb_packed_linear_workspace_size(int64_t M, int64_t K, int64_t N, int block);
+size_t tb_packed_linear_algo_workspace_size(int64_t M, int64_t K, int64_t N, int block, int algo);
+
+/*
+ * tb_packed_linear — Packed.__call__ on the non-embedding path.
+ * [ARCH] "Hadamard 旋转" (if block: x = fwht(x, block, signs); then
+ * quantized_matmul(x, weight, scales, biases, transpose=True, group_size=128, bits=2))
+ * and [PACK] "文本模型加载" (packed weights consumed directly, never expanded).
+ *   y[m, n] = sum_k x'[m, k] * (s[n, k/128] * q[n, k] + b[n, k/128]),
+ *   x' = fwht(x, block, signs) rounded to fp16 (x' = x when block = 0);
+ *   x fp16 [M, K]; signs int8 [K] (+-1) or NULL (all +1; ignored when block = 0);
+ *   w uint32 [N, K/16]; scales, biases fp16 [N, K/128]; y fp16 [M, N] (out).
+ * fp32 accumulation, fp16 output (round to nearest even).
+ * K: positive multiple of 1024 when block = 1024, of 128 when block = 0.  M, N >= 1.
+ * workspace: device memory of at least tb_packed_linear_workspace_size(...) bytes
+ * (may be NULL when that size is 0); its contents are scratch.
+ * dev_status optional (TB_DEV_TIMEOUT).
+ */
+int tb_packed_linear(const uint16_t* x, int64_t M, int64_t K, const int8_t* signs, int block,
+                     const uint32_t* w, const uint16_t* scales, const uint16_t* biases, int64_t N,
+                     uint16_t* y, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                     void* stream);
+
+/* Same as tb_packed_linear with an explicit algorithm (TB_ALGO_*). */
+int tb_packed_linear_algo(const uint16_t* x, int64_t M, int64_t K, const int8_t* signs, int block,
+                          const uint32_t* w, const uint16_t* scales, const uint16_t* biases,
+                          int64_t N, uint16_t* y, void* workspace, size_t workspace_bytes,
+                          int32_t* dev_status, int algo, void* stream);
+
+/*
+ * tb_embed_lookup — Packed.__call__ on the embedding path.
+ * [ARCH] "Hadamard 旋转" (return fwht(out, block, signs, inverse=True)) and
+ * [PACK] "文本模型加载" (mx.dequantize of the looked-up rows, then the inverse transform).
+ *   out[t, :] = signs * ((H/32) e) per block,  e = s*q + b of row ids[t] of the table.
+ *   ids int32 [T]; w uint32 [V, D/16]; scales, biases fp16 [V, D/128];
+ *   signs int8 [D] (+-1) or NULL (all +1); out fp16 [T, D] (out).
+ * An id outside [0, V) writes a row of zeros and sets TB_DEV_BAD_ID in dev_status.
+ * block 1024 (D a multiple of 1024) or 0 (D a multiple of 128); T >= 0 (T = 0 is a no-op).
+ */
+int tb_embed_lookup(const int32_t* ids, int64_t T, const uint32_t* w, const uint16_t* scales,
+                    const uint16_t* biases, int64_t V, int64_t D, const int8_t* signs, int block,
+                    uint16_t* out, int32_t* dev_status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TB_H */

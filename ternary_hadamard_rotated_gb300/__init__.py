@@ -1,0 +1,149 @@
+"""Python binding of the GB300 folded-Hadamard ternary ``Packed`` layer library.
+
+Argument marshalling only: every step of the layer runs in the sm_103a kernels of
+``libtb.so`` (C ABI declared in ``include/tb.h``).  Tensors are torch CUDA
+tensors (torch provides device memory and streams); the calls are asynchronous
+on the current torch stream unless a stream is given.  There is no CPU path:
+if the library is not built, importing the calls raises.
+
+Names follow the C ABI: ``tb_pack_w2``, ``tb_unpack_w2``, ``tb_fwht``,
+``tb_packed_linear``, ``tb_embed_lookup``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libtb.so")
+
+TB_OK = 0
+TB_ERR_NULL = -1
+TB_ERR_SHAPE = -2
+TB_ERR_UNSUPPORTED = -3
+TB_ERR_VALUE = -4
+TB_ERR_CUDA = -5
+TB_ERR_ALIGN = -6
+TB_ERR_WORKSPACE = -7
+
+TB_DEV_BAD_CODE = 1
+TB_DEV_BAD_ID = 2
+TB_DEV_TIMEOUT = 4
+
+TB_ALGO_AUTO = 0
+TB_ALGO_GEMV = 1
+TB_ALGO_TC = 2
+
+_lib = None
+
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_INT = ctypes.c_int
+_SZ = ctypes.c_size_t
+
+_SIGNATURES = {
+    "tb_status_string": (ctypes.c_char_p, [_INT]),
+    "tb_last_cuda_error": (ctypes.c_char_p, []),
+    "tb_version": (_INT, []),
+    "tb_pack_w2": (_INT, [_P, _P, _I64, _I64, _P, _P, _P, _P]),
+    "tb_unpack_w2": (_INT, [_P, _I64, _I64, _P, _P]),
+    "tb_fwht": (_INT, [_P, _P, _P, _I64, _I64, _INT, _INT, _P]),
+    "tb_packed_linear_workspace_size": (_SZ, [_I64, _I64, _I64, _INT]),
+    "tb_packed_linear_algo_workspace_size": (_SZ, [_I64, _I64, _I64, _INT, _INT]),
+    "tb_packed_linear": (_INT, [_P, _I64, _I64, _P, _INT, _P, _P, _P, _I64, _P, _P, _SZ, _P, _P]),
+    "tb_packed_linear_algo": (_INT, [_P, _I64, _I64, _P, _INT, _P, _P, _P, _I64, _P, _P, _SZ, _P,
+                                     _INT, _P]),
+    "tb_embed_lookup": (_INT, [_P, _I64, _P, _P, _P, _I64, _I64, _P, _INT, _P, _P, _P]),
+}
+
+EXPORTED = tuple(_SIGNATURES)
+
+
+class TBError(RuntimeError):
+    def __init__(self, fn, status):
+        lib = load()
+        msg = lib.tb_status_string(status).decode()
+        if status == TB_ERR_CUDA:
+            msg += ": " + lib.tb_last_cuda_error().decode()
+        super().__init__(f"{fn} failed ({status}): {msg}")
+        self.status = status
+
+
+def load(path: str = LIB_PATH):
+    """Load libtb.so (built by build.py); raises if it is missing."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(path):
+            raise ImportError(f"libtb.so not built at {path}; run ternary_hadamard_rotated_gb300.build")
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(fn, rc):
+    if rc != TB_OK:
+        raise TBError(fn, rc)
+
+
+def tb_pack_w2(codes, scales, w, biases, dev_status=None, stream=None):
+    """codes int8 [N,K], scales fp16 [N,K/128] -> w uint32 [N,K/16] (as int32), biases fp16."""
+    N, K = codes.shape
+    _check("tb_pack_w2", load().tb_pack_w2(_ptr(codes), _ptr(scales), N, K, _ptr(w), _ptr(biases),
+                                           _ptr(dev_status), _stream(stream)))
+
+
+def tb_unpack_w2(w, codes, stream=None):
+    N, K = codes.shape
+    _check("tb_unpack_w2", load().tb_unpack_w2(_ptr(w), N, K, _ptr(codes), _stream(stream)))
+
+
+def tb_fwht(x, y, signs=None, block=1024, inverse=False, stream=None):
+    M, K = x.shape
+    _check("tb_fwht", load().tb_fwht(_ptr(x), _ptr(y), _ptr(signs), M, K, block, int(bool(inverse)),
+                                     _stream(stream)))
+
+
+def tb_packed_linear_workspace_size(M, K, N, block=1024, algo=TB_ALGO_AUTO):
+    return load().tb_packed_linear_algo_workspace_size(M, K, N, block, algo)
+
+
+def tb_packed_linear(x, signs, block, w, scales, biases, y, workspace=None, dev_status=None,
+                     algo=TB_ALGO_AUTO, stream=None):
+    """y[M,N] = fwht(x)[M,K] . dequant(w)^T with the packed W2-g128 weights."""
+    M, K = x.shape
+    N = y.shape[-1]
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("tb_packed_linear",
+           load().tb_packed_linear_algo(_ptr(x), M, K, _ptr(signs), block, _ptr(w), _ptr(scales),
+                                        _ptr(biases), N, _ptr(y), _ptr(workspace), ws_bytes,
+                                        _ptr(dev_status), algo, _stream(stream)))
+
+
+def tb_embed_lookup(ids, w, scales, biases, signs, block, out, dev_status=None, stream=None):
+    T = ids.shape[0]
+    V = w.shape[0]
+    D = out.shape[-1]
+    _check("tb_embed_lookup",
+           load().tb_embed_lookup(_ptr(ids), T, _ptr(w), _ptr(scales), _ptr(biases), V, D,
+                                  _ptr(signs), block, _ptr(out), _ptr(dev_status), _stream(stream)))

@@ -1,0 +1,193 @@
+// Device helpers shared by the kernels of the W2-g128 folded-Hadamard layer.
+// sm_103a only: mbarrier / bulk-copy / tcgen05 PTX is written inline.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/tb.h"
+
+#define TB_DEVI __device__ __forceinline__
+
+// Upper bound of every spin on an mbarrier, in nanoseconds of %globaltimer.
+// A wait that runs out records TB_DEV_TIMEOUT and the kernel winds down.
+#ifndef TB_WAIT_NS
+#define TB_WAIT_NS 2000000000ull
+#endif
+
+namespace tb {
+
+constexpr int kGroup = 128;        // weights per scale/bias group
+constexpr int kCodesPerWord = 16;  // 2-bit codes per uint32
+constexpr int kBlock = 1024;       // Hadamard block
+constexpr float kInvSqrtBlock = 1.0f / 32.0f;
+
+// ---------------------------------------------------------------- addresses
+TB_DEVI uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+TB_DEVI uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+TB_DEVI void set_status(int32_t* st, int bits) {
+  if (st) atomicOr(st, bits);
+}
+
+// ---------------------------------------------------------------- mbarrier
+TB_DEVI void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+
+// make barrier initialisation visible to the async proxy (bulk copies, tcgen05)
+TB_DEVI void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+TB_DEVI void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+TB_DEVI void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+TB_DEVI void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(
+                   smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+TB_DEVI bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait for the phase with the given parity to complete.  Returns false
+// when TB_WAIT_NS elapsed first.
+TB_DEVI bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (globaltimer_ns() - t0 > TB_WAIT_NS) return false;
+  }
+}
+
+// ---------------------------------------------------------------- bulk copies
+// 1-D bulk copy global -> shared, completion counted in bytes on `bar`.
+// dst, src 16-byte aligned; bytes a multiple of 16.
+TB_DEVI void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Same with an L2 evict-first policy: for data read exactly once (weights).
+TB_DEVI uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+TB_DEVI void bulk_g2s_hint(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                           uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+// ---------------------------------------------------------------- small ALU helpers
+TB_DEVI uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;  // (a & b) | c
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+TB_DEVI uint32_t pack_half2(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+TB_DEVI float half_bits_to_float(uint16_t b) { return __half2float(__ushort_as_half(b)); }
+
+// ---------------------------------------------------------------- warp FWHT
+// 32 values per lane; two layouts of a 1024-block:
+//   layout A: v[r] is element lane*32 + r
+//   layout B: v[j] is element j*32 + lane
+// The transform's 10 butterfly stages commute, so the stages over the
+// in-register index bits run in whichever layout is current.
+
+// the five butterfly stages over the register index (bits 0..4 of it)
+TB_DEVI void butterfly32(float (&v)[32]) {
+#pragma unroll
+  for (int h = 1; h < 32; h <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      if ((i & h) == 0) {
+        const float a = v[i], b = v[i + h];
+        v[i] = a + b;
+        v[i + h] = a - b;
+      }
+    }
+  }
+}
+
+// layout B -> layout A through a padded 32x33 float scratch owned by the warp
+TB_DEVI void transpose_b_to_a(float (&v)[32], float* scratch, int lane) {
+#pragma unroll
+  for (int j = 0; j < 32; ++j) scratch[j * 33 + lane] = v[j];
+  __syncwarp();
+#pragma unroll
+  for (int r = 0; r < 32; ++r) v[r] = scratch[lane * 33 + r];
+  __syncwarp();
+}
+
+// layout A -> layout B
+TB_DEVI void transpose_a_to_b(float (&v)[32], float* scratch, int lane) {
+#pragma unroll
+  for (int r = 0; r < 32; ++r) scratch[lane * 33 + r] = v[r];
+  __syncwarp();
+#pragma unroll
+  for (int j = 0; j < 32; ++j) v[j] = scratch[j * 33 + lane];
+  __syncwarp();
+}
+
+// unnormalised Walsh-Hadamard transform of one 1024-block held by a warp:
+// in: layout B, out: layout A
+TB_DEVI void wht1024_b_to_a(float (&v)[32], float* scratch, int lane) {
+  butterfly32(v);  // element bits 5..9
+  transpose_b_to_a(v, scratch, lane);
+  butterfly32(v);  // element bits 0..4
+}
+
+// in: layout A, out: layout B
+TB_DEVI void wht1024_a_to_b(float (&v)[32], float* scratch, int lane) {
+  butterfly32(v);  // element bits 0..4
+  transpose_a_to_b(v, scratch, lane);
+  butterfly32(v);  // element bits 5..9
+}
+
+constexpr int kWarpScratchFloats = 32 * 33;
+
+}  // namespace tb

@@ -1,0 +1,328 @@
+// Prefill path of the Packed layer: tcgen05 / TMEM tensor-core GEMM on packed W2-g128 weights.
+//
+// [ARCH] kwkr.cn/news/564617, section "Hadamard 旋转把量化误差抹平的免费午餐": the same
+// Packed.__call__ (fwht on the activations, then quantized_matmul with group 128,
+// 2 bits, transpose) at M = prompt length.  Ternary codes times an fp16 scale plus
+// the fp16 bias -s give {-s, 0, s}, exact in fp16, so fp16 tensor-core operands lose
+// nothing on the weight side.
+//
+// y[M, N] = x'[M, K] . W[N, K]^T with
+//   A = x' (fp16, written by the rotate kernel into the workspace, TMA-loaded with the
+//       128-byte swizzle), tile 128 tokens x 64 k;
+//   B = W decoded in shared memory by 8 decoder warps straight from the packed words
+//       (never materialised in global memory), tile 256 rows x 64 k, written in the
+//       same K-major 128-byte-swizzled layout the UMMA descriptor reads;
+//   D = fp32 accumulator, 128 x 256, in tensor memory (256 columns).
+// Warp roles: warp 0 issues the TMA loads, warp 1 owns TMEM and issues tcgen05.mma
+// (one thread), warps 2..9 decode B and afterwards drain TMEM to fp16 y.
+// A 4-stage mbarrier ring couples the three roles; every wait is bounded.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include "tb_common.cuh"
+#include "tb_host.h"
+
+namespace tb {
+
+constexpr int kTcBM = 128, kTcBN = 256, kTcBK = 64, kTcStages = 4;
+constexpr int kTcThreads = 320;
+constexpr int kTcABytes = kTcBM * kTcBK * 2;  // 16 KB
+constexpr int kTcBBytes = kTcBN * kTcBK * 2;  // 32 KB
+constexpr int kTcStageBytes = kTcABytes + kTcBBytes;
+constexpr int kTcSmemBytes = kTcStages * kTcStageBytes + 1024 /*barriers*/ + 1024 /*align*/;
+constexpr int kTcTmemCols = 256;
+
+struct TcArgs {
+  const uint32_t* w;     // [N, K/16]
+  const __half* scales;  // [N, G]
+  const __half* biases;  // [N, G]
+  __half* y;             // [M, N]
+  int M, N, K, G;
+  int32_t* status;
+};
+
+// K-major operand in the 128-byte swizzle: 8-row core groups 1024 bytes apart.
+TB_DEVI uint64_t umma_desc_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);  // start address
+  d |= (uint64_t)1u << 16;                  // leading byte offset (unused for this layout)
+  d |= (uint64_t)(1024u >> 4) << 32;        // stride byte offset: next 8-row group
+  d |= (uint64_t)1u << 46;                  // descriptor version (tcgen05)
+  d |= (uint64_t)2u << 61;                  // 128-byte swizzle
+  return d;
+}
+
+// kind::f16 instruction descriptor: fp16 A and B, fp32 D, both K-major, M = 128, N = 256
+constexpr uint32_t kTcIdesc = (1u << 4) | ((uint32_t)(kTcBN >> 3) << 17) | ((uint32_t)(kTcBM >> 4) << 24);
+
+TB_DEVI void tma_load_2d(void* dst, const CUtensorMap* tm, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+TB_DEVI void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+TB_DEVI void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+TB_DEVI void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+TB_DEVI void tc_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   smem_u32(bar))
+               : "memory");
+}
+
+TB_DEVI void tc_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+TB_DEVI void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+               : "memory");
+}
+
+// one packed word (codes k..k+15) -> 8 half2 (s*q_p + b, s*q_{p+8} + b), p = 0..7
+TB_DEVI void decode_word_affine(uint32_t w, __half2 s2, __half2 b2, uint32_t (&o)[8]) {
+  const __half2 k1024 = __half2half2(__ushort_as_half(0x6400u));
+#pragma unroll
+  for (int p = 0; p < 8; ++p) {
+    const uint32_t v = lop3_and_or(w >> (2 * p), 0x00030003u, 0x64006400u);
+    const __half2 q = __hsub2(*reinterpret_cast<const __half2*>(&v), k1024);  // exact {0,1,2,3}
+    const __half2 r = __hfma2(q, s2, b2);
+    o[p] = *reinterpret_cast<const uint32_t*>(&r);
+  }
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+    w2_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const TcArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kTcStages * kTcStageBytes);
+  uint64_t* fullA = bars;
+  uint64_t* fullB = bars + kTcStages;
+  uint64_t* empty = bars + 2 * kTcStages;
+  uint64_t* accum = bars + 3 * kTcStages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * kTcStages + 1);
+  __shared__ volatile int aborted;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n0 = blockIdx.x * kTcBN, m0 = blockIdx.y * kTcBM;
+  const int nkb = a.K / kTcBK;
+
+  if (threadIdx.x == 0) {
+    aborted = 0;
+    for (int s = 0; s < kTcStages; ++s) {
+      mbar_init(fullA + s, 1);
+      mbar_init(fullB + s, 256);
+      mbar_init(empty + s, 1);
+    }
+    mbar_init(accum, 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(kTcTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_d = *tmem_slot;
+
+  auto wait = [&](uint64_t* bar, uint32_t parity) {
+    if (aborted) return;
+    if (!mbar_wait(bar, parity)) {
+      aborted = 1;
+      set_status(a.status, TB_DEV_TIMEOUT);
+    }
+  };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
+      for (int kb = 0; kb < nkb; ++kb) {
+        const int s = kb % kTcStages, it = kb / kTcStages;
+        if (it > 0) wait(empty + s, (it - 1) & 1);
+        mbar_arrive_expect_tx(fullA + s, kTcABytes);
+        tma_load_2d(smem + s * kTcStageBytes, &tmA, kb * kTcBK, m0, fullA + s);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      for (int kb = 0; kb < nkb; ++kb) {
+        const int s = kb % kTcStages, it = kb / kTcStages;
+        wait(fullA + s, it & 1);
+        wait(fullB + s, it & 1);
+        tc_fence_after();
+        const uint32_t sa = smem_u32(smem + s * kTcStageBytes);
+        const uint64_t ad = umma_desc_sw128(sa), bd = umma_desc_sw128(sa + kTcABytes);
+#pragma unroll
+        for (int k = 0; k < kTcBK / 16; ++k)
+          tc_mma(tmem_d, ad + 2 * k, bd + 2 * k, kTcIdesc, (kb | k) != 0);
+        tc_commit(empty + s);
+      }
+      tc_commit(accum);
+    }
+    __syncwarp();
+  } else {
+    // ---- decoders: thread d owns row n0 + d of the B tile ----
+    const int d = threadIdx.x - 64;
+    const int row = n0 + d;
+    const bool valid = row < a.N;
+    const uint4* wrow = reinterpret_cast<const uint4*>(a.w + (int64_t)(valid ? row : 0) * (a.K / 16));
+    const __half* srow = a.scales + (int64_t)(valid ? row : 0) * a.G;
+    const __half* brow = a.biases + (int64_t)(valid ? row : 0) * a.G;
+    uint4 cur = valid ? __ldg(wrow) : make_uint4(0, 0, 0, 0);
+    for (int kb = 0; kb < nkb; ++kb) {
+      const int s = kb % kTcStages, it = kb / kTcStages;
+      uint4 nxt = make_uint4(0, 0, 0, 0);
+      if (valid && kb + 1 < nkb) nxt = __ldg(wrow + kb + 1);
+      const __half sv = srow[kb >> 1], bv = brow[kb >> 1];
+      if (it > 0) wait(empty + s, (it - 1) & 1);
+      const uint32_t bt = smem_u32(smem + s * kTcStageBytes + kTcABytes) + d * 128;
+      const uint32_t sw = d & 7;
+      const uint32_t words[4] = {cur.x, cur.y, cur.z, cur.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint32_t o[8];
+        if (valid) {
+          decode_word_affine(words[j], __half2half2(sv), __half2half2(bv), o);
+        } else {
+#pragma unroll
+          for (int p = 0; p < 8; ++p) o[p] = 0;
+        }
+        sts128(bt + (((2 * j) ^ sw) << 4), o[0], o[1], o[2], o[3]);
+        sts128(bt + (((2 * j + 1) ^ sw) << 4), o[4], o[5], o[6], o[7]);
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(fullB + s);
+      cur = nxt;
+    }
+    // ---- epilogue: TMEM -> fp16 y ----
+    wait(accum, 0);
+    tc_fence_after();
+    const int q = warp & 3;                // TMEM lane quarter this warp may read
+    const int colbase = ((warp - 2) >> 2) * (kTcBN / 2);
+    const int tok = m0 + q * 32 + lane;
+    const bool vec = (a.N % 8) == 0;
+#pragma unroll 1
+    for (int c = 0; c < kTcBN / 2; c += 32) {
+      uint32_t r[32];
+      tc_ld32(tmem_d + ((uint32_t)(q * 32) << 16) + (uint32_t)(colbase + c), r);
+      const int n = n0 + colbase + c;
+      if (tok < a.M && n < a.N) {
+        __half* dst = a.y + (int64_t)tok * a.N + n;
+        if (vec && n + 32 <= a.N) {
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            uint32_t h[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              h[e] = pack_half2(__uint_as_float(r[8 * v + 2 * e]), __uint_as_float(r[8 * v + 2 * e + 1]));
+            *reinterpret_cast<uint4*>(dst + 8 * v) = make_uint4(h[0], h[1], h[2], h[3]);
+          }
+        } else {
+          for (int e = 0; e < 32 && n + e < a.N; ++e) dst[e] = __float2half_rn(__uint_as_float(r[e]));
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_d),
+                 "r"(kTcTmemCols)
+                 : "memory");
+  }
+}
+
+int launch_rotate_pairorder(const __half* x, __half* out, const int8_t* signs, int64_t M,
+                            int64_t K, int rotate, cudaStream_t s);
+
+// cuTensorMapEncodeTiled from the driver, resolved once through the runtime (the library
+// does not link libcuda directly, so it loads on machines without a driver too)
+static PFN_cuTensorMapEncodeTiled_v12000 encode_tiled_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+size_t gemm_tc_workspace(int64_t M, int64_t K) { return (size_t)M * (size_t)K * 2; }
+
+int launch_gemm_tc(const __half* x, int64_t M, int64_t K, const int8_t* signs, int block,
+                   const uint32_t* w, const __half* scales, const __half* biases, int64_t N,
+                   __half* y, void* workspace, int32_t* status, cudaStream_t s) {
+  if (M > 0x7fffffffLL || N > 0x7fffffffLL || K > (1 << 24)) return TB_ERR_SHAPE;
+  __half* xp = static_cast<__half*>(workspace);
+  int rc = launch_rotate_pairorder(x, xp, signs, M, K, block != 0, s);
+  if (rc != TB_OK) return rc;
+
+  CUtensorMap tm;
+  const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
+  const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)kTcBK, (cuuint32_t)kTcBM};
+  const cuuint32_t estr[2] = {1, 1};
+  PFN_cuTensorMapEncodeTiled_v12000 encode = encode_tiled_fn();
+  if (!encode) return TB_ERR_CUDA;
+  CUresult cr = encode(&tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, xp, dims, strides,
+                                       box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                       CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (cr != CUDA_SUCCESS) return TB_ERR_CUDA;
+
+  cudaError_t e = cudaFuncSetAttribute(w2_gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kTcSmemBytes);
+  if (e != cudaSuccess) {
+    record_cuda_error(e);
+    return TB_ERR_CUDA;
+  }
+  TcArgs a;
+  a.w = w;
+  a.scales = scales;
+  a.biases = biases;
+  a.y = y;
+  a.M = (int)M;
+  a.N = (int)N;
+  a.K = (int)K;
+  a.G = (int)(K / kGroup);
+  a.status = status;
+  dim3 grid((unsigned)((N + kTcBN - 1) / kTcBN), (unsigned)((M + kTcBM - 1) / kTcBM));
+  w2_gemm_tc_kernel<<<grid, kTcThreads, kTcSmemBytes, s>>>(tm, a);
+  return check_launch();
+}
+
+}  // namespace tb

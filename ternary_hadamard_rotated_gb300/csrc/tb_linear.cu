@@ -1,0 +1,85 @@
+// Entry points of the non-embedding path: argument checks and the choice between the
+// streaming GEMV (decode, M <= 8 tokens) and the tensor-core GEMM (prefill).
+//
+// [ARCH] kwkr.cn/news/564617, section "Hadamard 旋转把量化误差抹平的免费午餐":
+//   Packed.__call__: if self.block: x = fwht(x, self.block, self.signs), then
+//   mx.quantized_matmul(x, self.weight, self.scales, self.biases, transpose=True,
+//   group_size=128, bits=2).
+#include <cuda_runtime.h>
+
+#include "tb_common.cuh"
+#include "tb_host.h"
+
+namespace tb {
+
+int launch_gemv(const __half* x, int64_t M, int64_t K, const int8_t* signs, int block,
+                const uint32_t* w, const __half* scales, const __half* biases, int64_t N,
+                __half* y, int32_t* status, cudaStream_t s);
+int launch_gemm_tc(const __half* x, int64_t M, int64_t K, const int8_t* signs, int block,
+                   const uint32_t* w, const __half* scales, const __half* biases, int64_t N,
+                   __half* y, void* workspace, int32_t* status, cudaStream_t s);
+size_t gemm_tc_workspace(int64_t M, int64_t K);
+
+// decode (GEMV) up to this many tokens; the tensor-core GEMM above
+constexpr int64_t kGemvMaxTokens = 8;
+
+static int resolve_algo(int64_t M, int algo) {
+  if (algo == TB_ALGO_AUTO) return M <= kGemvMaxTokens ? TB_ALGO_GEMV : TB_ALGO_TC;
+  return algo;
+}
+
+static int check_linear_shape(int64_t M, int64_t K, int block, int64_t N) {
+  if (block != 0 && block != kBlock) return TB_ERR_UNSUPPORTED;
+  if (M < 1 || N < 1 || K < kGroup || K % kGroup) return TB_ERR_SHAPE;
+  if (block == kBlock && K % kBlock) return TB_ERR_SHAPE;
+  return TB_OK;
+}
+
+}  // namespace tb
+
+extern "C" size_t tb_packed_linear_algo_workspace_size(int64_t M, int64_t K, int64_t N, int block,
+                                                       int algo) {
+  using namespace tb;
+  if (check_linear_shape(M, K, block, N) != TB_OK) return 0;
+  return resolve_algo(M, algo) == TB_ALGO_TC ? gemm_tc_workspace(M, K) : 0;
+}
+
+extern "C" size_t tb_packed_linear_workspace_size(int64_t M, int64_t K, int64_t N, int block) {
+  return tb_packed_linear_algo_workspace_size(M, K, N, block, TB_ALGO_AUTO);
+}
+
+extern "C" int tb_packed_linear_algo(const uint16_t* x, int64_t M, int64_t K, const int8_t* signs,
+                                     int block, const uint32_t* w, const uint16_t* scales,
+                                     const uint16_t* biases, int64_t N, uint16_t* y,
+                                     void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                     int algo, void* stream) {
+  using namespace tb;
+  if (!x || !w || !scales || !biases || !y) return TB_ERR_NULL;
+  int rc = check_linear_shape(M, K, block, N);
+  if (rc != TB_OK) return rc;
+  if (algo != TB_ALGO_AUTO && algo != TB_ALGO_GEMV && algo != TB_ALGO_TC) return TB_ERR_UNSUPPORTED;
+  if (!aligned16(x) || !aligned16(w) || !aligned16(scales) || !aligned16(biases) || !aligned16(y) ||
+      (signs && !aligned16(signs)) || (workspace && !aligned16(workspace)))
+    return TB_ERR_ALIGN;
+  const int use = resolve_algo(M, algo);
+  const int8_t* sg = block ? signs : nullptr;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const __half* xh = reinterpret_cast<const __half*>(x);
+  const __half* sh = reinterpret_cast<const __half*>(scales);
+  const __half* bh = reinterpret_cast<const __half*>(biases);
+  __half* yh = reinterpret_cast<__half*>(y);
+  if (use == TB_ALGO_TC) {
+    const size_t need = gemm_tc_workspace(M, K);
+    if (!workspace || workspace_bytes < need) return TB_ERR_WORKSPACE;
+    return launch_gemm_tc(xh, M, K, sg, block, w, sh, bh, N, yh, workspace, dev_status, s);
+  }
+  return launch_gemv(xh, M, K, sg, block, w, sh, bh, N, yh, dev_status, s);
+}
+
+extern "C" int tb_packed_linear(const uint16_t* x, int64_t M, int64_t K, const int8_t* signs,
+                                int block, const uint32_t* w, const uint16_t* scales,
+                                const uint16_t* biases, int64_t N, uint16_t* y, void* workspace,
+                                size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  return tb_packed_linear_algo(x, M, K, signs, block, w, scales, biases, N, y, workspace,
+                               workspace_bytes, dev_status, TB_ALGO_AUTO, stream);
+}

@@ -1,0 +1,103 @@
+"""Shared helpers of the GPU parity tests: seeded layers on both sides, tolerances.
+
+The CUDA side gets its weights from ``tb_pack_w2`` (codes drawn on the host, or
+on the device by ``tb_inputs.device`` for the large tables); the oracle side
+packs the same codes itself with ``oracle.pack_w2``.  Nothing the oracle uses
+comes from the CUDA path.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+import oracle
+import tb_inputs as ti
+
+# tolerance of the linear and GEMM outputs:
+#   |y_gpu - y_ref| <= 2e-3 * sum_k |x'_k w_k| + 1e-5   (per element)
+LIN_REL = 2e-3
+LIN_ABS = 1e-5
+# tolerance of transform outputs (FWHT, embedding): 1e-3 relative, with an absolute
+# floor of 1e-6 * ||block||_2 for elements near zero (relative error is undefined there)
+FWHT_REL = 1e-3
+
+
+class HostLayer:
+    """Codes/scales drawn on the host; oracle-side packing."""
+
+    def __init__(self, seed: int, N: int, K: int, rows=None):
+        self.N, self.K, self.G = N, K, K // 128
+        r0, r1 = (0, N) if rows is None else rows
+        self.codes = ti.ternary_codes(seed, r0, r1, K)
+        self.scales = ti.group_scales(seed, r0, r1, self.G)
+        self.biases = oracle.biases_for(self.scales)
+        self.words = oracle.pack_w2(self.codes)
+
+
+def device_layer(seed: int, N: int, K: int, from_host: HostLayer | None = None, chunk_rows=None):
+    """Packed layer on the GPU: w (int32 view of uint32) [N, K/16], scales, biases fp16.
+
+    Codes come from the host layer when given, else from the device generator in
+    row chunks (bounded temporary memory).  Packing is tb_pack_w2 on the device.
+    """
+    import torch
+
+    import ternary_hadamard_rotated_gb300 as tb
+    from tb_inputs import device as tdev
+
+    dev = torch.device("cuda")
+    G = K // 128
+    w = torch.empty((N, K // 16), dtype=torch.int32, device=dev)
+    scales = torch.empty((N, G), dtype=torch.float16, device=dev)
+    biases = torch.empty((N, G), dtype=torch.float16, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    if from_host is not None:
+        codes = torch.from_numpy(from_host.codes).to(dev)
+        scales.copy_(torch.from_numpy(from_host.scales))
+        tb.tb_pack_w2(codes, scales, w, biases, status)
+    else:
+        step = chunk_rows or max(1, (1 << 28) // K)
+        tmp = torch.empty((min(step, N), K), dtype=torch.int8, device=dev)
+        for r0 in range(0, N, step):
+            n = min(step, N - r0)
+            tdev.fill_codes(tmp[:n], seed, r0, K)
+            tdev.fill_scales(scales[r0:r0 + n], seed, r0, G)
+            tb.tb_pack_w2(tmp[:n], scales[r0:r0 + n], w[r0:r0 + n], biases[r0:r0 + n], status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    return w, scales, biases
+
+
+def linear_reference(x16, signs, block, layer: HostLayer):
+    """(y_ref, bound) in float64 for the rows held by the host layer."""
+    x = x16.astype(np.float64)
+    y = oracle.packed_linear(x, signs, block, layer.words, layer.scales, layer.biases)
+    bound = LIN_REL * oracle.abs_product_sum(x, signs, block, layer.words, layer.scales,
+                                             layer.biases) + LIN_ABS
+    return y, bound
+
+
+def assert_linear_close(y_gpu, y_ref, bound, what=""):
+    y_gpu = np.asarray(y_gpu, dtype=np.float64)
+    err = np.abs(y_gpu - y_ref)
+    bad = ~(err <= bound)
+    if bad.any():
+        idx = np.argwhere(bad)[:5]
+        raise AssertionError(f"{what}: {bad.sum()} of {bad.size} outside tolerance; first {idx.tolist()} "
+                             f"gpu={y_gpu[tuple(idx[0])]} ref={y_ref[tuple(idx[0])]} "
+                             f"bound={bound[tuple(idx[0])]}")
+    rms = np.sqrt(np.mean(y_ref ** 2)) or 1.0
+    return float(err.max() / rms), float(np.sqrt(np.mean(err ** 2)) / rms)
+
+
+def assert_transform_close(out_gpu, ref, block=1024, what=""):
+    out_gpu = np.asarray(out_gpu, dtype=np.float64)
+    lead = ref.shape[:-1]
+    K = ref.shape[-1]
+    nb = max(1, K // block)
+    norms = np.linalg.norm(ref.reshape(lead + (nb, -1)), axis=-1)
+    floor = np.repeat(norms, K // nb, axis=-1).reshape(ref.shape) * 1e-6
+    err = np.abs(out_gpu - ref)
+    bad = ~(err <= FWHT_REL * np.abs(ref) + floor)
+    if bad.any():
+        idx = np.argwhere(bad)[:5]
+        raise AssertionError(f"{what}: {bad.sum()} of {bad.size} outside tolerance; first {idx.tolist()}")

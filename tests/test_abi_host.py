@@ -1,0 +1,107 @@
+"""Host-side checks of the C ABI (no GPU needed).
+
+The library loads, exports every entry point include/tb.h declares, and refuses
+bad arguments before touching the device.  Argument validation returns before
+any CUDA call, so these run on a machine without a GPU.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import ternary_hadamard_rotated_gb300 as tb
+    from ternary_hadamard_rotated_gb300 import build as tbbuild
+
+    if not os.path.exists(tb.LIB_PATH):
+        tbbuild.build()
+    return tb.load()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "tb.h"), encoding="utf-8").read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(tb_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_declares_the_layer_entry_points():
+    names = declared_functions()
+    for required in ("tb_pack_w2", "tb_unpack_w2", "tb_fwht", "tb_packed_linear",
+                     "tb_embed_lookup", "tb_status_string"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    import ternary_hadamard_rotated_gb300 as tb
+
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert name in tb.EXPORTED, f"binding lacks {name}"
+
+
+def test_status_strings(lib):
+    for code in range(0, -8, -1):
+        s = lib.tb_status_string(code).decode()
+        assert s and s != "unknown status"
+    assert lib.tb_status_string(42).decode() == "unknown status"
+    assert lib.tb_version() >= 100
+
+
+P = 0x1000  # a 16-byte aligned non-null placeholder; never dereferenced by these calls
+
+
+def test_packed_linear_refuses_bad_arguments(lib):
+    f = lib.tb_packed_linear
+    ok = dict(x=P, M=1, K=1024, signs=P, block=1024, w=P, s=P, b=P, N=16, y=P)
+
+    def call(**kw):
+        a = {**ok, **kw}
+        return f(a["x"], a["M"], a["K"], a["signs"], a["block"], a["w"], a["s"], a["b"], a["N"],
+                 a["y"], None, 0, None, None)
+
+    assert call(x=None) == -1
+    assert call(w=None) == -1
+    assert call(y=None) == -1
+    assert call(block=512) == -3          # only 1024 (and 0 = not folded) are built
+    assert call(block=2048) == -3
+    assert call(K=1000) == -2             # not a multiple of 128
+    assert call(K=1152) == -2             # a multiple of 128 but not of the 1024 block
+    assert call(M=0) == -2
+    assert call(N=0) == -2
+    assert call(x=P + 2) == -6            # misaligned
+    # algorithm choice
+    g = lib.tb_packed_linear_algo
+    assert g(P, 1, 1024, P, 1024, P, P, P, 16, P, None, 0, None, 7, None) == -3
+    # the tensor-core path needs its workspace
+    assert g(P, 300, 1024, P, 1024, P, P, P, 16, P, None, 0, None, 2, None) == -7
+    assert g(P, 300, 1024, P, 1024, P, P, P, 16, P, P, 100, None, 2, None) == -7
+
+
+def test_workspace_size_query(lib):
+    ws = lib.tb_packed_linear_workspace_size
+    assert ws(1, 5120, 17408, 1024) == 0            # decode path: none
+    assert ws(8, 5120, 17408, 1024) == 0
+    assert ws(512, 5120, 17408, 1024) == 512 * 5120 * 2
+    assert ws(512, 1000, 17408, 1024) == 0          # invalid shape -> 0
+    assert lib.tb_packed_linear_algo_workspace_size(4, 2048, 64, 1024, 2) == 4 * 2048 * 2
+
+
+def test_other_entry_points_refuse_bad_arguments(lib):
+    assert lib.tb_pack_w2(None, P, 4, 128, P, P, None, None) == -1
+    assert lib.tb_pack_w2(P, P, 4, 100, P, P, None, None) == -2
+    assert lib.tb_pack_w2(P, P, 0, 128, P, P, None, None) == -2
+    assert lib.tb_unpack_w2(P, 4, 20, P, None) == -2
+    assert lib.tb_fwht(P, P, None, 2, 1024, 512, 0, None) == -3
+    assert lib.tb_fwht(P, P, None, 2, 1536, 1024, 0, None) == -2
+    assert lib.tb_fwht(P + 8, P, None, 2, 1024, 1024, 0, None) == -6
+    e = lib.tb_embed_lookup
+    assert e(P, 4, P, P, P, 100, 1000, None, 1024, P, None, None) == -2
+    assert e(P, 4, P, P, P, 100, 1024, None, 4096, P, None, None) == -3
+    assert e(P, 4, P, P, P, 0, 1024, None, 1024, P, None, None) == -2
+    assert e(P, 0, P, P, P, 100, 1024, None, 1024, P, None, None) == 0   # T = 0: no-op
+    assert e(None, 4, P, P, P, 100, 1024, None, 1024, P, None, None) == -1
