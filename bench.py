@@ -164,16 +164,16 @@ def build_sweep(tb, tdev, torch):
     return layers, emb, xs, signs, y
 
 
-def sweep_step(tb, layers, emb, xs, signs, y, ids, e_out, status):
+def sweep_step(tb, layers, emb, xs, signs, y, ids, e_out, ws, status):
     """One decode token: embedding lookup + 401 fused FWHT/GEMV linears."""
     tb.tb_embed_lookup(ids, emb.w, emb.s, emb.b, signs[ti.HIDDEN], 1024, e_out, status)
     for _, p in layers:
-        tb.tb_packed_linear(xs[p.K], signs[p.K], 1024, p.w, p.s, p.b, y[:, : p.N], None, status)
+        tb.tb_packed_linear(xs[p.K], signs[p.K], 1024, p.w, p.s, p.b, y[:, : p.N], ws, status)
 
 
-def linears_only(tb, layers, xs, signs, y, status):
+def linears_only(tb, layers, xs, signs, y, ws, status):
     for _, p in layers:
-        tb.tb_packed_linear(xs[p.K], signs[p.K], 1024, p.w, p.s, p.b, y[:, : p.N], None, status)
+        tb.tb_packed_linear(xs[p.K], signs[p.K], 1024, p.w, p.s, p.b, y[:, : p.N], ws, status)
 
 
 def time_graph(torch, graph, steps, dist):
@@ -252,9 +252,10 @@ def run_sweep(args, dist, tb, tdev, torch):
     ids = torch.tensor([int(ti.token_ids(ti.config_seed(3, 3000), 1, ti.VOCAB)[0])], dtype=torch.int32,
                        device=dev)
     e_out = torch.empty((1, ti.HIDDEN), dtype=torch.float16, device=dev)
+    ws = torch.zeros(tb.tb_packed_linear_workspace_size(1, ti.MLP, ti.HIDDEN), dtype=torch.uint8, device=dev)
 
-    step_graph = capture(torch, lambda: sweep_step(tb, layers, emb, xs, signs, y, ids, e_out, status))
-    gemv_graph = capture(torch, lambda: linears_only(tb, layers, xs, signs, y, status))
+    step_graph = capture(torch, lambda: sweep_step(tb, layers, emb, xs, signs, y, ids, e_out, ws, status))
+    gemv_graph = capture(torch, lambda: linears_only(tb, layers, xs, signs, y, ws, status))
     launches_per_step = 1 + len(layers)
 
     for _ in range(args.warmup):
@@ -282,14 +283,14 @@ def run_sweep(args, dist, tb, tdev, torch):
     h_logits = torch.empty((1, ti.VOCAB), dtype=torch.float16).pin_memory()
     for _ in range(2):
         ids.copy_(h_id, non_blocking=True)
-        sweep_step(tb, layers, emb, xs, signs, y, ids, e_out, status)
+        sweep_step(tb, layers, emb, xs, signs, y, ids, e_out, ws, status)
         h_logits.copy_(y[:, : ti.VOCAB], non_blocking=True)
     torch.cuda.synchronize()
     dist.barrier()
     t0 = time.perf_counter()
     for _ in range(args.steps):
         ids.copy_(h_id, non_blocking=True)
-        sweep_step(tb, layers, emb, xs, signs, y, ids, e_out, status)
+        sweep_step(tb, layers, emb, xs, signs, y, ids, e_out, ws, status)
         h_logits.copy_(y[:, : ti.VOCAB], non_blocking=True)
     torch.cuda.synchronize()
     e2e_s = dist.max(time.perf_counter() - t0)
@@ -324,7 +325,7 @@ def run_sweep(args, dist, tb, tdev, torch):
             "unit": "GB/s",
             "frac": round(achieved / hbm, 4),
             "traffic": None,
-            "kernel": "w2_gemv_kernel<1> (fused FWHT prologue + W2-g128 GEMV), 401 launches averaged",
+            "kernel": "w2_gemv_tma_kernel<1> (fused FWHT prologue + W2-g128 GEMV), 401 launches averaged",
             "peak_kind": f"{peak_kind} hbm_gbs",
         },
         "e2e": {
@@ -360,10 +361,11 @@ def run_layers(args, dist, tb, tdev, torch):
         x = torch.from_numpy(ti.activations(5, 1, K)).to(dev)
         sg = torch.from_numpy(ti.rademacher_signs(5, K)).to(dev)
         y = torch.empty((1, N), dtype=torch.float16, device=dev)
+        ws = torch.zeros(tb.tb_packed_linear_workspace_size(1, K, N), dtype=torch.uint8, device=dev)
 
         def fn():
             for p in ps:
-                tb.tb_packed_linear(x, sg, 1024, p.w, p.s, p.b, y, None, status)
+                tb.tb_packed_linear(x, sg, 1024, p.w, p.s, p.b, y, ws, status)
 
         g = capture(torch, fn)
         for _ in range(3):
@@ -392,7 +394,7 @@ def run_prefill(args, dist, tb, tdev, torch):
             x = torch.from_numpy(ti.activations(4, M, K)).to(dev)
             sg = torch.from_numpy(ti.rademacher_signs(4, K)).to(dev)
             y = torch.empty((M, N), dtype=torch.float16, device=dev)
-            ws = torch.empty(tb.tb_packed_linear_workspace_size(M, K, N), dtype=torch.uint8, device=dev)
+            ws = torch.zeros(tb.tb_packed_linear_workspace_size(M, K, N), dtype=torch.uint8, device=dev)
             flush = torch.empty(256 << 20, dtype=torch.int8, device=dev)
 
             def fn():
@@ -435,8 +437,7 @@ def run_batched(args, dist, tb, tdev, torch):
     for M in (1, 2, 4, 8, 16, 32, 64):
         x = torch.from_numpy(ti.activations(5, M, K)).to(dev)
         y = torch.empty((M, N), dtype=torch.float16, device=dev)
-        nws = tb.tb_packed_linear_workspace_size(M, K, N)
-        ws = torch.empty(max(nws, 16), dtype=torch.uint8, device=dev) if nws else None
+        ws = torch.zeros(tb.tb_packed_linear_workspace_size(M, K, N), dtype=torch.uint8, device=dev)
 
         def fn():
             for p in ps:

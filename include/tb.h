@@ -113,9 +113,13 @@ int tb_fwht(const uint16_t* x, uint16_t* y, const int8_t* signs, int64_t M, int6
             int block, int inverse, void* stream);
 
 /*
- * Bytes of workspace tb_packed_linear needs for these sizes (0 when the GEMV
- * path is taken and needs none).  The workspace holds the rotated activations
- * x' (fp16 [M, K]) for the tensor-core path.
+ * Bytes of workspace tb_packed_linear uses for these sizes.  Layout: a fixup region
+ * (about 1 MB) for the decode GEMV's split schedule (fp32 sums and counters of output
+ * tiles shared by several SMs), then, for the tensor-core path, the rotated activations
+ * x' (fp16 [M, K]).  The fixup region must be zero-filled before the first call
+ * that uses the workspace; every completed call leaves it zero (a call that reported
+ * TB_DEV_TIMEOUT may not: zero it again).  Calls sharing one workspace must be
+ * ordered on one stream.
  */
 size_t tb_packed_linear_workspace_size(int64_t M, int64_t K, int64_t N, int block);
 size_t tb_packed_linear_algo_workspace_size(int64_t M, int64_t K, int64_t N, int block, int algo);
@@ -131,8 +135,10 @@ size_t tb_packed_linear_algo_workspace_size(int64_t M, int64_t K, int64_t N, int
  *   w uint32 [N, K/16]; scales, biases fp16 [N, K/128]; y fp16 [M, N] (out).
  * fp32 accumulation, fp16 output (round to nearest even).
  * K: positive multiple of 1024 when block = 1024, of 128 when block = 0.  M, N >= 1.
- * workspace: device memory of at least tb_packed_linear_workspace_size(...) bytes
- * (may be NULL when that size is 0); its contents are scratch.
+ * workspace: device memory of at least tb_packed_linear_workspace_size(...) bytes,
+ * zero-filled before its first use (see above).  The GEMV path (M <= 8) also runs with
+ * workspace = NULL, then with output tiles never split between SMs (slower on shapes
+ * whose row-tile count is not a multiple of the SM count).
  * dev_status optional (TB_DEV_TIMEOUT).
  */
 int tb_packed_linear(const uint16_t* x, int64_t M, int64_t K, const int8_t* signs, int block,

@@ -117,6 +117,40 @@ TB_DEVI void bulk_g2s_hint(void* dst, const void* src, uint32_t bytes, uint64_t*
       : "memory");
 }
 
+// ---------------------------------------------------------------- explicit shared-memory access
+// (32-bit shared addresses: no generic-address resolution on the hot path)
+TB_DEVI uint4 ld_shared_v4(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+  return v;
+}
+TB_DEVI uint2 ld_shared_v2(uint32_t a) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+  return v;
+}
+TB_DEVI float2 ld_shared_f2(uint32_t a) {
+  float2 v;
+  asm volatile("ld.shared.v2.f32 {%0,%1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(a));
+  return v;
+}
+TB_DEVI float ld_shared_f(uint32_t a) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a));
+  return v;
+}
+TB_DEVI float ld_shared_half(uint32_t a) {
+  unsigned short h;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(h) : "r"(a));
+  return __half2float(__ushort_as_half(h));
+}
+TB_DEVI void st_shared_f(uint32_t a, float v) {
+  asm volatile("st.shared.f32 [%0], %1;" ::"r"(a), "f"(v) : "memory");
+}
+TB_DEVI void red_shared_add(uint32_t a, float v) {
+  asm volatile("red.shared.add.f32 [%0], %1;" ::"r"(a), "f"(v) : "memory");
+}
+
 // ---------------------------------------------------------------- small ALU helpers
 TB_DEVI uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t c) {
   uint32_t d;  // (a & b) | c

@@ -40,7 +40,8 @@ constexpr int kTileRows = 16;
 constexpr int kStageGroups = 4;                                 // K groups per ring stage
 constexpr int kStagePitch = kStageGroups * 32 + 32;             // bytes per row (== 32 mod 128)
 constexpr int kStageBytes = kTileRows * kStagePitch;            // 2560
-constexpr int kScaleSlots = 2;
+constexpr int kMaxScaleSlots = 8;                              // tiles of scales in flight
+constexpr int kScaleSlotBytesPerGroup = 2 * kTileRows * 2;      // scale + bias of 16 rows
 constexpr uint32_t kMagic = 0x64006400u;                        // half2(1024, 1024)
 
 struct GemvArgs {
@@ -54,6 +55,7 @@ struct GemvArgs {
   int K, N, G;
   int rotate;            // 1: x' = fwht(x); 0: x' = x
   int ring;              // stages per warp ring
+  int sslots;            // tiles of scales/biases in flight
   int32_t* status;
 };
 
@@ -64,11 +66,11 @@ struct GemvLayout {
 __host__ __device__ inline int round_up(int v, int a) { return (v + a - 1) / a * a; }
 
 template <int MT>
-__host__ __device__ inline GemvLayout gemv_layout(int G, int ring) {
+__host__ __device__ inline GemvLayout gemv_layout(int G, int ring, int sslots) {
   GemvLayout L;
   int off = 0;
   L.bars = off;
-  off += (kGemvWarps * ring + kScaleSlots) * 8;
+  off += (kGemvWarps * ring + sslots) * 8;
   off = round_up(off, 128);
   L.img = off;
   off += G * 256 * MT;
@@ -76,7 +78,7 @@ __host__ __device__ inline GemvLayout gemv_layout(int G, int ring) {
   off += G * MT * 8;
   off = round_up(off, 128);
   L.scl = off;
-  off += kScaleSlots * 2 * kTileRows * G * 2;
+  off += sslots * 2 * kTileRows * G * 2;
   off = round_up(off, 128);
   L.scratch = off;
   const int fw = kGemvWarps * kWarpScratchFloats * 4;
@@ -91,7 +93,7 @@ __host__ __device__ inline GemvLayout gemv_layout(int G, int ring) {
 
 TB_DEVI void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                       uint32_t b0, uint32_t b1) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
       "{%8,%9}, {%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
@@ -118,18 +120,52 @@ TB_DEVI float inv_sigma(int p) {
        : (p == 3 || p == 6) ? 0.015625f : 0.00390625f;
 }
 
-TB_DEVI uint2 lds64(uint32_t addr) {
-  uint2 v;
-  asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
-  return v;
-}
-
-TB_DEVI uint4 lds128(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(addr));
-  return v;
+// One or two K groups of a 16-row tile: decode, 8 mma each (two independent chains when
+// NG = 2), then the per-group scale epilogue into acc.
+template <int MT, int NG>
+TB_DEVI void gemv_groups(const uint8_t* rowg, int gi0, int grp0, const uint4* imgt, const __half* ss,
+                         const __half* sb, int G, int g, const float2* cs, int t0, int t1,
+                         float (&acc)[4]) {
+  uint2 wa[NG], wb[NG];
+#pragma unroll
+  for (int n = 0; n < NG; ++n) {
+    wa[n] = *reinterpret_cast<const uint2*>(rowg + (gi0 + n) * 32);
+    wb[n] = *reinterpret_cast<const uint2*>(rowg + 8 * kStagePitch + (gi0 + n) * 32);
+  }
+  float d[NG][4];
+#pragma unroll
+  for (int n = 0; n < NG; ++n) d[n][0] = d[n][1] = d[n][2] = d[n][3] = 0.f;
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    uint32_t P[NG][8], Q[NG][8];
+    uint4 i0[NG], i1[NG];
+#pragma unroll
+    for (int n = 0; n < NG; ++n) {
+      decode_word(half ? wa[n].y : wa[n].x, P[n]);
+      decode_word(half ? wb[n].y : wb[n].x, Q[n]);
+      i0[n] = imgt[((grp0 + n) * 4 + 2 * half) * MT * 4];
+      i1[n] = imgt[((grp0 + n) * 4 + 2 * half + 1) * MT * 4];
+    }
+#pragma unroll
+    for (int n = 0; n < NG; ++n) mma16816(d[n], P[n][0], Q[n][0], P[n][1], Q[n][1], i0[n].x, i0[n].y);
+#pragma unroll
+    for (int n = 0; n < NG; ++n) mma16816(d[n], P[n][2], Q[n][2], P[n][3], Q[n][3], i0[n].z, i0[n].w);
+#pragma unroll
+    for (int n = 0; n < NG; ++n) mma16816(d[n], P[n][4], Q[n][4], P[n][5], Q[n][5], i1[n].x, i1[n].y);
+#pragma unroll
+    for (int n = 0; n < NG; ++n) mma16816(d[n], P[n][6], Q[n][6], P[n][7], Q[n][7], i1[n].z, i1[n].w);
+  }
+#pragma unroll
+  for (int n = 0; n < NG; ++n) {
+    const int grp = grp0 + n;
+    const float sA = __half2float(ss[g * G + grp]), bA = __half2float(sb[g * G + grp]);
+    const float sB = __half2float(ss[(g + 8) * G + grp]), bB = __half2float(sb[(g + 8) * G + grp]);
+    const float2 c0 = cs[grp * MT + t0], c1 = cs[grp * MT + t1];
+    acc[0] += sA * (d[n][0] - c0.x) + bA * c0.y;
+    acc[1] += sA * (d[n][1] - c1.x) + bA * c1.y;
+    acc[2] += sB * (d[n][2] - c0.x) + bB * c0.y;
+    acc[3] += sB * (d[n][3] - c1.x) + bB * c1.y;
+  }
 }
 
 template <int MT>
@@ -137,11 +173,15 @@ __global__ void __launch_bounds__(kGemvThreads, 1) w2_gemv_kernel(const GemvArgs
   extern __shared__ __align__(128) uint8_t smem[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, t = lane & 3;
-  const int K = a.K, N = a.N, G = a.G, D = a.ring;
-  const GemvLayout L = gemv_layout<MT>(G, D);
+  const int K = a.K, N = a.N, G = a.G, D = a.ring, R = a.sslots;
+  const GemvLayout L = gemv_layout<MT>(G, D, R);
+
+  // the next kernel on the stream may start now; it waits for this grid before reading
+  // anything this grid writes (programmatic dependent launch)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);  // [warp][D]
-  uint64_t* sfull = full + kGemvWarps * D;                       // [kScaleSlots]
+  uint64_t* sfull = full + kGemvWarps * D;                       // [R]
   __half* img = reinterpret_cast<__half*>(smem + L.img);
   float2* cs = reinterpret_cast<float2*>(smem + L.cs);           // [G][MT] = (C, S)
   __half* scl = reinterpret_cast<__half*>(smem + L.scl);         // [slot][s|b][16][G]
@@ -159,7 +199,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) w2_gemv_kernel(const GemvArgs
   if (threadIdx.x == 0) {
     aborted = 0;
     for (int i = 0; i < kGemvWarps * D; ++i) mbar_init(full + i, 1);
-    for (int i = 0; i < kScaleSlots; ++i) mbar_init(sfull + i, 1);
+    for (int i = 0; i < R; ++i) mbar_init(sfull + i, 1);
     fence_barrier_init();
   }
   __syncthreads();
@@ -179,11 +219,11 @@ __global__ void __launch_bounds__(kGemvThreads, 1) w2_gemv_kernel(const GemvArgs
                     a.w + (int64_t)(r0 + lane) * (K / kCodesPerWord) + ga * 8, (uint32_t)(gn * 32),
                     full + warp * D + slot, pol);
   };
-  // scales and biases of local tile j into slot j % kScaleSlots (warp 0 only)
+  // scales and biases of local tile j into slot j % R (warp 0 only)
   auto issue_scales = [&](int j) {
     const int r0 = (blockIdx.x + j * gridDim.x) * kTileRows;
     const int rows = min(kTileRows, N - r0);
-    const int slot = j % kScaleSlots;
+    const int slot = j % R;
     __half* ds = scl + slot * 2 * kTileRows * G;
     __half* db = ds + kTileRows * G;
     const uint32_t bytes = (uint32_t)(rows * G * 2);
@@ -205,9 +245,12 @@ __global__ void __launch_bounds__(kGemvThreads, 1) w2_gemv_kernel(const GemvArgs
     __syncwarp();
   };
 
+  // weights, scales and biases are never written by a kernel that lets this one start
+  // early, so their prefetch may run ahead of the dependency wait
   for (int i = 0; i < min(D, total); ++i) issue_stage(i);
   if (warp == 0)
-    for (int j = 0; j < min(kScaleSlots, nt); ++j) issue_scales(j);
+    for (int j = 0; j < min(R, nt); ++j) issue_scales(j);
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   // ---- prologue: x' = fwht(signs * x) -> B-fragment image, C and S per group ----
   {
@@ -277,20 +320,20 @@ __global__ void __launch_bounds__(kGemvThreads, 1) w2_gemv_kernel(const GemvArgs
   __syncthreads();
 
   // ---- main loop ------------------------------------------------------------
-  const uint32_t img_u32 = smem_u32(img);
-  const uint32_t ring_u32 = smem_u32(ring);
+  // Lanes whose mma column g is not a live token read token 0's image: their D columns
+  // are never used.
   const int tokc = g < MT ? g : 0;
-  const bool bvalid = g < MT;
+  const uint4* imgt = reinterpret_cast<const uint4*>(img) + tokc * 4 + t;
   const int t0 = min(2 * t, MT - 1), t1 = min(2 * t + 1, MT - 1);
   float* red = scratch;  // [2][warp][16][MT]
   int i = 0;
 
   for (int j = 0; j < nt; ++j) {
     const int r0 = (blockIdx.x + j * gridDim.x) * kTileRows;
-    const int sslot = j % kScaleSlots;
+    const int sslot = j % R;
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     if (spt > 0) {
-      if (!aborted && !mbar_wait(sfull + sslot, (j / kScaleSlots) & 1)) {
+      if (!aborted && !mbar_wait(sfull + sslot, (j / R) & 1)) {
         aborted = 1;
         set_status(a.status, TB_DEV_TIMEOUT);
       }
@@ -304,34 +347,11 @@ __global__ void __launch_bounds__(kGemvThreads, 1) w2_gemv_kernel(const GemvArgs
         }
         const int ga = g0 + c * kStageGroups;
         const int gn = min(kStageGroups, g1 - ga);
-        const uint32_t st = ring_u32 + slot * kStageBytes;
-        for (int gi = 0; gi < gn; ++gi) {
-          const int grp = ga + gi;
-          const uint2 wa = lds64(st + g * kStagePitch + gi * 32 + t * 8);
-          const uint2 wb = lds64(st + (g + 8) * kStagePitch + gi * 32 + t * 8);
-          float d[4] = {0.f, 0.f, 0.f, 0.f};
-          const uint32_t ib = img_u32 + ((grp * 4) * MT + tokc) * 64 + t * 16;
-#pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            uint32_t P[8], Q[8];
-            decode_word(half ? wa.y : wa.x, P);
-            decode_word(half ? wb.y : wb.x, Q);
-            uint4 i0 = lds128(ib + (2 * half) * MT * 64);
-            uint4 i1 = lds128(ib + (2 * half + 1) * MT * 64);
-            if (!bvalid) i0 = i1 = make_uint4(0, 0, 0, 0);
-            mma16816(d, P[0], Q[0], P[1], Q[1], i0.x, i0.y);
-            mma16816(d, P[2], Q[2], P[3], Q[3], i0.z, i0.w);
-            mma16816(d, P[4], Q[4], P[5], Q[5], i1.x, i1.y);
-            mma16816(d, P[6], Q[6], P[7], Q[7], i1.z, i1.w);
-          }
-          const float sA = __half2float(ss[g * G + grp]), bA = __half2float(sb[g * G + grp]);
-          const float sB = __half2float(ss[(g + 8) * G + grp]), bB = __half2float(sb[(g + 8) * G + grp]);
-          const float2 c0 = cs[grp * MT + t0], c1 = cs[grp * MT + t1];
-          acc[0] += sA * (d[0] - c0.x) + bA * c0.y;
-          acc[1] += sA * (d[1] - c1.x) + bA * c1.y;
-          acc[2] += sB * (d[2] - c0.x) + bB * c0.y;
-          acc[3] += sB * (d[3] - c1.x) + bB * c1.y;
-        }
+        const uint8_t* rowg = ring + slot * kStageBytes + g * kStagePitch + t * 8;
+        int gi = 0;
+        for (; gi + 2 <= gn; gi += 2)
+          gemv_groups<MT, 2>(rowg, gi, ga + gi, imgt, ss, sb, G, g, cs, t0, t1, acc);
+        if (gi < gn) gemv_groups<MT, 1>(rowg, gi, ga + gi, imgt, ss, sb, G, g, cs, t0, t1, acc);
         __syncwarp();
         if (i + D < total) {
           fence_proxy_async_smem();  // generic reads of this slot before the async refill
@@ -350,7 +370,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) w2_gemv_kernel(const GemvArgs
       rw[(g + 8) * MT + 2 * t + 1] = acc[3];
     }
     asm volatile("bar.sync 1, %0;" ::"n"(kGemvThreads) : "memory");
-    if (warp == 0 && j + kScaleSlots < nt) issue_scales(j + kScaleSlots);
+    if (warp == 0 && j + R < nt) issue_scales(j + R);
     if (threadIdx.x < kTileRows * MT) {
       const int row = threadIdx.x / MT, tok = threadIdx.x - row * MT;
       float sum = 0.f;
@@ -363,9 +383,16 @@ __global__ void __launch_bounds__(kGemvThreads, 1) w2_gemv_kernel(const GemvArgs
 }
 
 // host side --------------------------------------------------------------------
+// tiles of scales and biases kept in flight: enough to cover the DRAM latency of small
+// tiles, at most 32 KB
+static int gemv_scale_slots(int G) {
+  int r = 32768 / (kScaleSlotBytesPerGroup * G);
+  return r < 2 ? 2 : (r > kMaxScaleSlots ? kMaxScaleSlots : r);
+}
+
 template <int MT>
 static int gemv_ring_for(int G, int smem_optin) {
-  const int fixed = gemv_layout<MT>(G, 0).total + kGemvWarps * 8 * 16;  // bars headroom
+  const int fixed = gemv_layout<MT>(G, 0, gemv_scale_slots(G)).total + kGemvWarps * 8 * 16;  // bars headroom
   const int per = kGemvWarps * kStageBytes;
   const int d = (smem_optin - fixed) / per;
   return d > 16 ? 16 : d;
@@ -378,7 +405,8 @@ static int launch_gemv_mt(const GemvArgs& base, int64_t M, int64_t K, const Devi
   const int ring = gemv_ring_for<MT>(a.G, f.smem_optin);
   if (ring < 2) return TB_ERR_SHAPE;
   a.ring = ring;
-  const int bytes = gemv_layout<MT>(a.G, ring).total;
+  a.sslots = gemv_scale_slots(a.G);
+  const int bytes = gemv_layout<MT>(a.G, ring, a.sslots).total;
   cudaError_t e = cudaFuncSetAttribute(w2_gemv_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        bytes);
   if (e != cudaSuccess) {
@@ -391,9 +419,21 @@ static int launch_gemv_mt(const GemvArgs& base, int64_t M, int64_t K, const Devi
     a.x = base.x + m0 * K;
     a.y = base.y + m0 * a.N;
     a.Mc = (int)((M - m0) < MT ? (M - m0) : MT);
-    w2_gemv_kernel<MT><<<grid, kGemvThreads, bytes, s>>>(a);
-    int rc = check_launch();
-    if (rc != TB_OK) return rc;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kGemvThreads);
+    cfg.dynamicSmemBytes = bytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, w2_gemv_kernel<MT>, a);
+    if (e != cudaSuccess) {
+      record_cuda_error(e);
+      return TB_ERR_CUDA;
+    }
   }
   return TB_OK;
 }
@@ -431,6 +471,7 @@ int launch_gemv(const __half* x, int64_t M, int64_t K, const int8_t* signs, int 
   a.G = (int)(K / kGroup);
   a.rotate = block != 0;
   a.ring = 0;
+  a.sslots = 0;
   a.status = status;
   const int mt = gemv_tokens_per_pass(M, a.G, f.smem_optin);
   switch (mt) {

@@ -1,0 +1,626 @@
+// Decode path of the Packed layer, TMA-streamed: fused sign*FWHT prologue + W2-g128 GEMV.
+//
+// [ARCH] kwkr.cn/news/564617, section "Hadamard 旋转把量化误差抹平的免费午餐":
+//   if self.block: x = fwht(x, block, signs); y = quantized_matmul(x, weight, scales,
+//   biases, transpose=True, group_size=128, bits=2): the packed 2-bit words are consumed
+//   directly and never expanded to fp16.
+// [PACK] lpnh.cn/news/2438023, section "文本模型加载artifact.load_model 与 Packed 模块".
+//
+// Work unit: 128 output rows x 512 k (4 groups of 128) = one 16 KB TMA box of packed codes
+// (128 rows x 128 B, 128-byte swizzle; rows past N are zero-filled).  Each SM can keep only
+// a handful of TMA requests in flight, so requests are made large: 16 KB boxes stream at
+// the HBM rate where 2-4 KB requests stall at a fraction of it.  Scales and biases (8 B
+// per row per unit) are read by the consumer warps themselves, two units ahead, and staged
+// through shared memory.
+//
+// Schedule (stream-K): the units of all 128-row tiles, tile-major, are cut into one
+// contiguous, equal range per CTA (one persistent CTA per SM).  A producer warp keeps a
+// ring of 16 KB slots in flight; 12 consumer warps form 3 unit groups of 4 warps; group u
+// takes the CTA's units u, u + 3, ... and warp i of the group the rows 32i..32i+31 of the
+// unit.  Every warp adds its 32-row partial sums into a per-tile shared accumulator; the
+// warp that completes a tile's count in this CTA writes y, or, when the tile continues in a
+// neighbouring CTA, adds the CTA's partial into the tile's fp32 sum in the workspace, and
+// the last of the tile's CTAs converts that sum to y and returns sum and counter to zero.
+//
+// Arithmetic (per group of 128, per token): LOP3 puts each 2-bit code into the mantissa of
+// an fp16 1024.0 (1024 + sigma*q, exact; sigma = 4^j from the field's bit position j);
+// those half2 are mma.sync A fragments, x'/sigma the B fragment, and the accumulator
+// starts at -1024*sum(x'/sigma) so the tensor core returns D = sum q*x' directly:
+//   y += s * D + b * S,   S = sum x' over the group.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+#include <unordered_map>
+
+#include "tb_common.cuh"
+#include "tb_host.h"
+
+namespace tb {
+
+constexpr int kUnitRows = 128;
+constexpr int kUnitGroups = 4;                       // groups per unit (512 k)
+constexpr int kBoxBytes = kUnitRows * 128;           // 16 KB
+constexpr int kGroupsOfWarps = 3;                    // unit groups
+constexpr int kWarpsPerUnit = 4;                     // 32 rows each
+constexpr int kTmaConsumers = kGroupsOfWarps * kWarpsPerUnit;
+constexpr int kTmaThreads = (kTmaConsumers + 1) * 32;
+constexpr int kTmaFwhtWarps = 8;
+constexpr int kMaxSlotsPerGroup = 4;
+constexpr int kScaleStageBytes = 32 * kUnitGroups * 2 * 2;  // per warp: 32 rows x 4 groups, s and b
+constexpr uint32_t kMagic1024 = 0x64006400u;
+
+struct GemvTmaArgs {
+  const __half* x;        // [Mc, K]
+  const int8_t* signs;    // [K] or null
+  const __half* scales;   // [N, G]
+  const __half* biases;   // [N, G]
+  __half* y;              // [Mc, N]
+  float* ws_partial;      // [kFixupCtas][128][MT] fp32 sums of shared tiles, or null (tile-aligned)
+  int* ws_count;          // [kFixupCtas]
+  int Mc, K, N, G, C;     // C = units per tile = K / 512
+  int rotate, dw, tslots;
+  int n_tiles;            // ceil(N / 128)
+  int split;              // 1: stream-K ranges; 0: ranges on tile boundaries
+  int32_t* status;
+};
+
+struct GemvTmaLayout {
+  int codes, img, cs, scratch, sstage, accs, cnt, bars, total;
+};
+
+__host__ __device__ inline int rup(int v, int a) { return (v + a - 1) / a * a; }
+
+template <int MT>
+__host__ __device__ inline GemvTmaLayout gemv_tma_layout(int G, int dw, int tslots) {
+  GemvTmaLayout L;
+  int off = 0;
+  L.codes = off;  // 1024-aligned boxes (the 128-byte swizzle repeats every 1024 bytes)
+  off += kGroupsOfWarps * dw * kBoxBytes;
+  L.img = off;
+  off += G * 256 * MT;
+  L.cs = off;
+  off += G * MT * 8;
+  off = rup(off, 16);
+  L.scratch = off;
+  off += kTmaFwhtWarps * kWarpScratchFloats * 4;
+  L.sstage = off;
+  off += kTmaConsumers * kScaleStageBytes;
+  L.accs = off;
+  off += tslots * kUnitRows * MT * 4;
+  L.cnt = off;
+  off += tslots * 4;
+  off = rup(off, 8);
+  L.bars = off;
+  off += 2 * kGroupsOfWarps * dw * 8;
+  L.total = off + 1024;  // slack to align the base to 1024
+  return L;
+}
+
+// owner of global unit s when S units are cut into grid ranges [S*i/grid, S*(i+1)/grid)
+__host__ __device__ inline int stage_owner(int64_t s, int64_t S, int grid) {
+  return (int)(((s + 1) * grid - 1) / S);
+}
+
+TB_DEVI void mma16816_acc(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                          uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+TB_DEVI void decode_word_sigma(uint32_t w, uint32_t (&P)[8]) {
+  const uint32_t w6 = w >> 6;
+  P[0] = lop3_and_or(w, 0x00030003u, kMagic1024);   // codes 0, 8   sigma 1
+  P[1] = lop3_and_or(w, 0x000C000Cu, kMagic1024);   // codes 1, 9   sigma 4
+  P[2] = lop3_and_or(w, 0x00300030u, kMagic1024);   // codes 2, 10  sigma 16
+  P[3] = lop3_and_or(w, 0x00C000C0u, kMagic1024);   // codes 3, 11  sigma 64
+  P[4] = lop3_and_or(w, 0x03000300u, kMagic1024);   // codes 4, 12  sigma 256
+  P[5] = lop3_and_or(w6, 0x00300030u, kMagic1024);  // codes 5, 13  sigma 16
+  P[6] = lop3_and_or(w6, 0x00C000C0u, kMagic1024);  // codes 6, 14  sigma 64
+  P[7] = lop3_and_or(w6, 0x03000300u, kMagic1024);  // codes 7, 15  sigma 256
+}
+
+TB_DEVI float inv_sigma_p(int p) {
+  return p == 0 ? 1.0f : p == 1 ? 0.25f : (p == 2 || p == 5) ? 0.0625f
+       : (p == 3 || p == 6) ? 0.015625f : 0.00390625f;
+}
+
+TB_DEVI void tma2d(uint32_t dst, const CUtensorMap* tm, int x, int y, uint64_t* bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(pol)
+      : "memory");
+}
+
+// One group gi (0..3) of a unit for the warp's two 16-row blocks: decode, 2 x 8 mma (two
+// independent accumulator chains sharing one B fragment), scale epilogue.
+//   box:  the unit's code box; R0, R0 + 16: this lane's A rows of block 0 (block 1 = + 16)
+//   imgt: B-fragment image entry of this lane; csa: (C, S) pairs [G][MT]
+//   ss:   this warp's staged scales [32 rows][4] (biases follow after 256 B)
+template <int MT>
+TB_DEVI void unit_group(uint32_t box, int R0, int t, int gi, int grp, uint32_t imgt, uint32_t ss,
+                        int rA, uint32_t csa, int t0, int t1, float (&acc)[2][4]) {
+  const int c = 2 * gi + (t >> 1);  // logical 16-byte chunk of the 128-byte row
+  uint2 w[2][2];
+#pragma unroll
+  for (int j = 0; j < 2; ++j)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int R = R0 + 16 * j + 8 * h;  // (R & 7) == (rA & 7)
+      w[j][h] = ld_shared_v2(box + R * 128 + ((c ^ (rA & 7)) << 4) + (t & 1) * 8);
+    }
+  const float2 cs0 = ld_shared_f2(csa + (grp * MT + t0) * 8);
+  const float2 cs1 = ld_shared_f2(csa + (grp * MT + t1) * 8);
+  float d[2][4];
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    d[j][0] = -cs0.x;
+    d[j][1] = -cs1.x;
+    d[j][2] = -cs0.x;
+    d[j][3] = -cs1.x;
+  }
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    const uint4 i0 = ld_shared_v4(imgt + (grp * 4 + 2 * half) * MT * 64);
+    const uint4 i1 = ld_shared_v4(imgt + (grp * 4 + 2 * half + 1) * MT * 64);
+    uint32_t P[2][8], Q[2][8];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      decode_word_sigma(half ? w[j][0].y : w[j][0].x, P[j]);
+      decode_word_sigma(half ? w[j][1].y : w[j][1].x, Q[j]);
+    }
+#pragma unroll
+    for (int j = 0; j < 2; ++j) mma16816_acc(d[j], P[j][0], Q[j][0], P[j][1], Q[j][1], i0.x, i0.y);
+#pragma unroll
+    for (int j = 0; j < 2; ++j) mma16816_acc(d[j], P[j][2], Q[j][2], P[j][3], Q[j][3], i0.z, i0.w);
+#pragma unroll
+    for (int j = 0; j < 2; ++j) mma16816_acc(d[j], P[j][4], Q[j][4], P[j][5], Q[j][5], i1.x, i1.y);
+#pragma unroll
+    for (int j = 0; j < 2; ++j) mma16816_acc(d[j], P[j][6], Q[j][6], P[j][7], Q[j][7], i1.z, i1.w);
+  }
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const int ra = 16 * j + rA, rb = ra + 8;  // rows within the warp's 32
+    const float sA = ld_shared_half(ss + (ra * kUnitGroups + gi) * 2);
+    const float bA = ld_shared_half(ss + 256 + (ra * kUnitGroups + gi) * 2);
+    const float sB = ld_shared_half(ss + (rb * kUnitGroups + gi) * 2);
+    const float bB = ld_shared_half(ss + 256 + (rb * kUnitGroups + gi) * 2);
+    acc[j][0] = fmaf(sA, d[j][0], fmaf(bA, cs0.y, acc[j][0]));
+    acc[j][1] = fmaf(sA, d[j][1], fmaf(bA, cs1.y, acc[j][1]));
+    acc[j][2] = fmaf(sB, d[j][2], fmaf(bB, cs0.y, acc[j][2]));
+    acc[j][3] = fmaf(sB, d[j][3], fmaf(bB, cs1.y, acc[j][3]));
+  }
+}
+
+template <int MT>
+__global__ void __launch_bounds__(kTmaThreads, 1)
+    w2_gemv_tma_kernel(const __grid_constant__ CUtensorMap tmW, const GemvTmaArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  // unit group u owns slots [u*DW, (u+1)*DW) and takes the CTA's units u, u + 3, ... in
+  // order, so no wait is ever more than one phase ahead of its barrier
+  const int DW = a.dw, TS = a.tslots, C = a.C, G = a.G, K = a.K, N = a.N;
+  const GemvTmaLayout L = gemv_tma_layout<MT>(G, DW, TS);
+  const uint32_t codes_u32 = smem_u32(smem + L.codes);
+  __half* img = reinterpret_cast<__half*>(smem + L.img);
+  float2* cs = reinterpret_cast<float2*>(smem + L.cs);    // [G][MT] = (1024 sum x'/sigma, sum x')
+  float* scratch = reinterpret_cast<float*>(smem + L.scratch);
+  float* accs = reinterpret_cast<float*>(smem + L.accs);  // [TS][128][MT]
+  int* cnt = reinterpret_cast<int*>(smem + L.cnt);         // [TS]
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
+  uint64_t* empty = full + kGroupsOfWarps * DW;
+  __shared__ volatile int aborted;
+
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+  // this CTA's unit range
+  const int64_t S = (int64_t)a.n_tiles * C;
+  int64_t lo, hi;
+  if (a.split) {
+    lo = S * blockIdx.x / gridDim.x;
+    hi = S * (blockIdx.x + 1) / gridDim.x;
+  } else {
+    lo = (int64_t)C * ((int64_t)a.n_tiles * blockIdx.x / gridDim.x);
+    hi = (int64_t)C * ((int64_t)a.n_tiles * (blockIdx.x + 1) / gridDim.x);
+  }
+  const int nst = (int)(hi - lo);
+  const int64_t tile_lo = lo / C;
+
+  if (threadIdx.x == 0) {
+    aborted = 0;
+    for (int i = 0; i < kGroupsOfWarps * DW; ++i) {
+      mbar_init(full + i, 1);
+      mbar_init(empty + i, kWarpsPerUnit);
+    }
+    fence_barrier_init();
+  }
+  for (int i = threadIdx.x; i < TS * kUnitRows * MT; i += blockDim.x) accs[i] = 0.f;
+  for (int i = threadIdx.x; i < TS; i += blockDim.x) cnt[i] = 0;
+  __syncthreads();
+
+  auto wait = [&](uint64_t* bar, uint32_t parity) {
+    if (aborted) return;
+    if (!mbar_wait(bar, parity)) {
+      aborted = 1;
+      set_status(a.status, TB_DEV_TIMEOUT);
+    }
+  };
+
+  if (warp == kTmaConsumers) {
+    // ---- producer: the packed codes never depend on the previous kernel ----
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      for (int q = 0; q < nst; ++q) {
+        const int n = q / kGroupsOfWarps, j = n % DW, k = n / DW;
+        const int slot = (q % kGroupsOfWarps) * DW + j;
+        if (k > 0) wait(empty + slot, (k - 1) & 1);
+        const int64_t s = lo + q;
+        const int tile = (int)(s / C), chunk = (int)(s - (int64_t)tile * C);
+        mbar_arrive_expect_tx(full + slot, kBoxBytes);
+        tma2d(codes_u32 + slot * kBoxBytes, &tmW, chunk * 32, tile * kUnitRows, full + slot, pol);
+      }
+      // leave no copy in flight: the last use of every slot has completed
+      for (int q = nst - 1; q >= 0 && q >= nst - kGroupsOfWarps * DW; --q) {
+        const int n = q / kGroupsOfWarps;
+        wait(full + (q % kGroupsOfWarps) * DW + n % DW, (n / DW) & 1);
+      }
+    }
+    __syncwarp();
+    return;
+  }
+
+  // ---- consumers ----
+  const int g = lane >> 2, t = lane & 3;
+  const int ug = warp / kWarpsPerUnit, wi = warp % kWarpsPerUnit;
+  // scale / bias prefetch for this warp's units (rows 32*wi + lane of the unit)
+  auto load_sb = [&](int q, uint2& sv, uint2& bv) {
+    sv = make_uint2(0, 0);
+    bv = make_uint2(0, 0);
+    if (q >= nst) return;
+    const int64_t s = lo + q;
+    const int tile = (int)(s / C), chunk = (int)(s - (int64_t)tile * C);
+    const int row = tile * kUnitRows + 32 * wi + lane;
+    if (row < N) {
+      const int64_t off = (int64_t)row * G + chunk * kUnitGroups;
+      sv = __ldg(reinterpret_cast<const uint2*>(a.scales + off));
+      bv = __ldg(reinterpret_cast<const uint2*>(a.biases + off));
+    }
+  };
+  uint2 s0, b0, s1, b1;
+  load_sb(ug, s0, b0);
+  load_sb(ug + kGroupsOfWarps, s1, b1);
+
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  {
+    // prologue: x' = fwht(signs * x) -> B-fragment image, (C, S) per group and token
+    const int nchunk = K / kBlock;
+    if (warp < kTmaFwhtWarps) {
+      float* sw = scratch + warp * kWarpScratchFloats;
+      for (int it = warp; it < MT * nchunk; it += kTmaFwhtWarps) {
+        const int tok = it / nchunk, b = it - tok * nchunk;
+        float v[32];
+        if (tok < a.Mc) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            float f = __half2float(a.x[(int64_t)tok * K + b * kBlock + j * 32 + lane]);
+            if (a.signs && a.signs[b * kBlock + j * 32 + lane] < 0) f = -f;
+            v[j] = f;
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = 0.f;
+        }
+        if (a.rotate) {
+          wht1024_b_to_a(v, sw, lane);
+#pragma unroll
+          for (int r = 0; r < 32; ++r) v[r] *= kInvSqrtBlock;
+        } else {
+          transpose_b_to_a(v, sw, lane);
+        }
+        const int grp = b * (kBlock / kGroup) + (lane >> 2);
+        float ssum = 0.f, csum = 0.f;
+#pragma unroll
+        for (int r = 0; r < 32; ++r) {
+          v[r] = __half2float(__float2half_rn(v[r]));  // x' rounded to fp16
+          ssum += v[r];
+        }
+#pragma unroll
+        for (int mp = 0; mp < 4; ++mp) {
+          uint32_t pk[4];
+#pragma unroll
+          for (int e2 = 0; e2 < 4; ++e2) {
+            const int p = 4 * (mp & 1) + e2;
+            const int r = (mp >> 1) * 16 + p;
+            const float is = inv_sigma_p(p);
+            const __half lo_ = __float2half_rn(v[r] * is), hi_ = __float2half_rn(v[r + 8] * is);
+            csum += __half2float(lo_) + __half2float(hi_);
+            pk[e2] = (uint32_t)__half_as_ushort(lo_) | ((uint32_t)__half_as_ushort(hi_) << 16);
+          }
+          *reinterpret_cast<uint4*>(img + ((size_t)(grp * 4 + mp) * MT + tok) * 32 + t * 8) =
+              make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        }
+        ssum += __shfl_xor_sync(0xffffffffu, ssum, 1);
+        ssum += __shfl_xor_sync(0xffffffffu, ssum, 2);
+        csum += __shfl_xor_sync(0xffffffffu, csum, 1);
+        csum += __shfl_xor_sync(0xffffffffu, csum, 2);
+        if (t == 0) cs[grp * MT + tok] = make_float2(1024.f * csum, ssum);
+      }
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(kTmaConsumers * 32) : "memory");
+  }
+
+  // mma row g <-> unit row 32*wi + 16*j + rA (and + 8): conflict-free swizzled reads
+  const int rA = 2 * (g & 3) + (g >> 2);
+  const int tokc = g < MT ? g : 0;
+  const uint32_t imgt = smem_u32(img) + tokc * 64 + t * 16;
+  const uint32_t csa = smem_u32(cs);
+  const uint32_t ss = smem_u32(smem + L.sstage) + warp * kScaleStageBytes;
+  const uint32_t accs_u32 = smem_u32(accs);
+  const int t0 = min(2 * t, MT - 1), t1 = min(2 * t + 1, MT - 1);
+
+  for (int q = ug, n = 0; q < nst; q += kGroupsOfWarps, ++n) {
+    // stage this unit's scales and biases, prefetch the ones two units ahead
+    {
+      const uint32_t r = ss + lane * kUnitGroups * 2;
+      asm volatile("st.shared.v2.u32 [%0], {%1,%2};" ::"r"(r), "r"(s0.x), "r"(s0.y) : "memory");
+      asm volatile("st.shared.v2.u32 [%0], {%1,%2};" ::"r"(r + 256), "r"(b0.x), "r"(b0.y) : "memory");
+      s0 = s1;
+      b0 = b1;
+      load_sb(q + 2 * kGroupsOfWarps, s1, b1);
+      __syncwarp();
+    }
+    const int slot = ug * DW + n % DW;
+    wait(full + slot, (n / DW) & 1);
+    const int64_t s = lo + q;
+    const int tile = (int)(s / C), chunk = (int)(s - (int64_t)tile * C);
+    const uint32_t box = codes_u32 + slot * kBoxBytes;
+    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll 1
+    for (int gi = 0; gi < kUnitGroups; ++gi)
+      unit_group<MT>(box, 32 * wi + rA, t, gi, chunk * kUnitGroups + gi, imgt, ss, rA, csa, t0, t1, acc);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty + slot);
+
+    // add this warp's 32 rows into the tile's shared accumulator
+    const int lt = (int)(tile - tile_lo);
+    const int ts = lt % TS;
+    const uint32_t atu = accs_u32 + ts * kUnitRows * MT * 4;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int ra = 32 * wi + 16 * j + rA, rb = ra + 8;
+      if (2 * t < MT) {
+        red_shared_add(atu + (ra * MT + 2 * t) * 4, acc[j][0]);
+        red_shared_add(atu + (rb * MT + 2 * t) * 4, acc[j][2]);
+      }
+      if (2 * t + 1 < MT) {
+        red_shared_add(atu + (ra * MT + 2 * t + 1) * 4, acc[j][1]);
+        red_shared_add(atu + (rb * MT + 2 * t + 1) * 4, acc[j][3]);
+      }
+    }
+    const int64_t t_beg = (int64_t)tile * C, t_end = t_beg + C;
+    const int64_t c_beg = t_beg > lo ? t_beg : lo, c_end = t_end < hi ? t_end : hi;
+    const int need = (int)(c_end - c_beg) * kWarpsPerUnit;
+    __syncwarp();
+    int last = 0;
+    if (lane == 0) {
+      __threadfence_block();
+      last = atomicAdd(cnt + ts, 1) == need - 1;
+    }
+    last = __shfl_sync(0xffffffffu, last, 0);
+    if (!last) continue;
+
+    // this warp finishes the tile for this CTA
+    __threadfence_block();
+    float* at = accs + ts * kUnitRows * MT;
+    const bool complete = t_beg >= lo && t_end <= hi;
+    // a tile shared with other CTAs is summed in the workspace slot of its first CTA
+    const int first = complete ? 0 : stage_owner(t_beg, S, gridDim.x);
+    float* wsum = a.ws_partial + (int64_t)first * kUnitRows * MT;
+    for (int e = lane; e < kUnitRows * MT; e += 32) {
+      const float u = at[e];
+      at[e] = 0.f;
+      const int r_ = e / MT, k_ = e - r_ * MT;
+      if (complete) {
+        if (tile * kUnitRows + r_ < N && k_ < a.Mc)
+          a.y[(int64_t)k_ * N + tile * kUnitRows + r_] = __float2half_rn(u);
+      } else {
+        atomicAdd(wsum + e, u);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) cnt[ts] = 0;
+    __threadfence_block();
+    if (complete) continue;
+    // the last of the tile's CTAs converts the sum, then returns the slot and counter to zero
+    const int lastc = stage_owner(t_end - 1, S, gridDim.x);
+    int fin = 0;
+    if (lane == 0) {
+      __threadfence();
+      fin = atomicAdd(a.ws_count + first, 1) == lastc - first;
+    }
+    fin = __shfl_sync(0xffffffffu, fin, 0);
+    if (!fin) continue;
+    __threadfence();
+    for (int e = lane; e < kUnitRows * MT; e += 32) {
+      const float v = __ldcg(wsum + e);
+      wsum[e] = 0.f;
+      const int r_ = e / MT, k_ = e - r_ * MT;
+      if (tile * kUnitRows + r_ < N && k_ < a.Mc)
+        a.y[(int64_t)k_ * N + tile * kUnitRows + r_] = __float2half_rn(v);
+    }
+    if (lane == 0) a.ws_count[first] = 0;
+  }
+}
+
+// ------------------------------------------------------------------ host side
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// tensor map of one packed matrix's codes, cached by (pointer, shape)
+static int code_map(const uint32_t* w, int64_t N, int64_t K, CUtensorMap* out) {
+  struct Key {
+    const void* w;
+    int64_t N, K;
+    bool operator==(const Key& o) const { return w == o.w && N == o.N && K == o.K; }
+  };
+  struct Hash {
+    size_t operator()(const Key& k) const {
+      return std::hash<const void*>()(k.w) ^ std::hash<int64_t>()(k.N * 131 + k.K);
+    }
+  };
+  static std::mutex mu;
+  static std::unordered_map<Key, CUtensorMap, Hash> cache;
+  const Key key{w, N, K};
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) {
+      *out = it->second;
+      return TB_OK;
+    }
+  }
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+  if (!enc) return TB_ERR_CUDA;
+  CUtensorMap m;
+  const cuuint64_t dims[2] = {(cuuint64_t)(K / 16), (cuuint64_t)N};
+  const cuuint64_t strides[1] = {(cuuint64_t)(K / 4)};
+  const cuuint32_t box[2] = {32, (cuuint32_t)kUnitRows};
+  const cuuint32_t es[2] = {1, 1};
+  if (enc(&m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, (void*)w, dims, strides, box, es,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return TB_ERR_CUDA;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache.size() > 4096) cache.clear();
+    cache[key] = m;
+  }
+  *out = m;
+  return TB_OK;
+}
+
+// workspace of the split (stream-K) schedule: fp32 sums [kFixupCtas][128][8] of tiles shared
+// by several CTAs (indexed by the tile's first CTA), then counters [kFixupCtas]; both must
+// be zero before a call and are zero after it
+constexpr int kFixupCtas = 256;
+constexpr size_t kFixupPartialBytes = (size_t)kFixupCtas * kUnitRows * 8 * 4;
+size_t gemv_fixup_bytes() { return kFixupPartialBytes + kFixupCtas * 4; }
+
+template <int MT>
+static int launch_tma_mt(GemvTmaArgs a, const CUtensorMap& m, int64_t M, int64_t K, int64_t N,
+                         const DeviceFacts& f, cudaStream_t s) {
+  // slots per unit group from what is left of shared memory
+  int dw = kMaxSlotsPerGroup;
+  auto ts_for = [&](int d) { return kGroupsOfWarps * d / a.C + 3; };
+  while (dw >= 1 && gemv_tma_layout<MT>(a.G, dw, ts_for(dw)).total > f.smem_optin) --dw;
+  if (dw < 1) return TB_ERR_SHAPE;
+  a.dw = dw;
+  a.tslots = ts_for(dw);
+  const int bytes = gemv_tma_layout<MT>(a.G, dw, a.tslots).total;
+  cudaError_t e = cudaFuncSetAttribute(w2_gemv_tma_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) {
+    record_cuda_error(e);
+    return TB_ERR_CUDA;
+  }
+  const int64_t S = (int64_t)a.n_tiles * a.C;
+  int grid = f.sms;
+  if (!a.split && a.n_tiles < grid) grid = a.n_tiles;
+  if (S < grid) grid = (int)S;
+  const __half* x0 = a.x;
+  __half* y0 = a.y;
+  for (int64_t m0 = 0; m0 < M; m0 += MT) {
+    a.x = x0 + m0 * K;
+    a.y = y0 + m0 * N;
+    a.Mc = (int)((M - m0) < MT ? (M - m0) : MT);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kTmaThreads);
+    cfg.dynamicSmemBytes = bytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, w2_gemv_tma_kernel<MT>, m, a);
+    if (e != cudaSuccess) {
+      record_cuda_error(e);
+      return TB_ERR_CUDA;
+    }
+  }
+  return TB_OK;
+}
+
+// tokens per pass: the largest of 8, 4, 2, 1 (not above M rounded up) whose B image leaves
+// room for two slots per unit group
+static int tma_tokens_per_pass(int64_t M, int G, int C, int smem_optin) {
+  int mt = M >= 5 ? 8 : M >= 3 ? 4 : M == 2 ? 2 : 1;
+  auto fits = [&](int total) { return total <= smem_optin; };
+  while (mt > 1) {
+    const int ts = kGroupsOfWarps * 2 / C + 3;
+    const bool ok = mt == 8 ? fits(gemv_tma_layout<8>(G, 2, ts).total)
+                  : mt == 4 ? fits(gemv_tma_layout<4>(G, 2, ts).total)
+                            : fits(gemv_tma_layout<2>(G, 2, ts).total);
+    if (ok) break;
+    mt >>= 1;
+  }
+  return mt;
+}
+
+int launch_gemv_tma(const __half* x, int64_t M, int64_t K, const int8_t* signs, int block,
+                    const uint32_t* w, const __half* scales, const __half* biases, int64_t N,
+                    __half* y, void* workspace, size_t ws_bytes, int32_t* status, cudaStream_t s) {
+  DeviceFacts f;
+  int rc = device_facts(&f);
+  if (rc != TB_OK) return rc;
+  if (N > (1LL << 30) || K > (1 << 22) || K % kBlock) return TB_ERR_SHAPE;
+  CUtensorMap m;
+  rc = code_map(w, N, K, &m);
+  if (rc != TB_OK) return rc;
+  GemvTmaArgs a;
+  a.x = x;
+  a.signs = signs;
+  a.scales = scales;
+  a.biases = biases;
+  a.y = y;
+  const bool split = workspace && ws_bytes >= gemv_fixup_bytes() && f.sms <= kFixupCtas;
+  a.ws_partial = split ? static_cast<float*>(workspace) : nullptr;
+  a.ws_count = split ? reinterpret_cast<int*>(static_cast<char*>(workspace) + kFixupPartialBytes)
+                     : nullptr;
+  a.split = split ? 1 : 0;
+  a.Mc = 0;
+  a.K = (int)K;
+  a.N = (int)N;
+  a.G = (int)(K / kGroup);
+  a.C = (int)(K / (kUnitGroups * kGroup));
+  a.rotate = block != 0;
+  a.dw = a.tslots = 0;
+  a.n_tiles = (int)((N + kUnitRows - 1) / kUnitRows);
+  a.status = status;
+  const int mt = tma_tokens_per_pass(M, a.G, a.C, f.smem_optin);
+  switch (mt) {
+    case 8: return launch_tma_mt<8>(a, m, M, K, N, f, s);
+    case 4: return launch_tma_mt<4>(a, m, M, K, N, f, s);
+    case 2: return launch_tma_mt<2>(a, m, M, K, N, f, s);
+    default: return launch_tma_mt<1>(a, m, M, K, N, f, s);
+  }
+}
+
+}  // namespace tb

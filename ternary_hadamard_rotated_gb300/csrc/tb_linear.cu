@@ -19,6 +19,14 @@ int launch_gemm_tc(const __half* x, int64_t M, int64_t K, const int8_t* signs, i
                    const uint32_t* w, const __half* scales, const __half* biases, int64_t N,
                    __half* y, void* workspace, int32_t* status, cudaStream_t s);
 size_t gemm_tc_workspace(int64_t M, int64_t K);
+int launch_gemv_tma(const __half* x, int64_t M, int64_t K, const int8_t* signs, int block,
+                    const uint32_t* w, const __half* scales, const __half* biases, int64_t N,
+                    __half* y, void* workspace, size_t ws_bytes, int32_t* status, cudaStream_t s);
+size_t gemv_fixup_bytes();
+
+// Workspace layout: [fixup region of the GEMV split schedule (zero before the first call,
+// left zero by every completed call)][x' of the tensor-core path], 1 KB aligned.
+static size_t fixup_region() { return (gemv_fixup_bytes() + 1023) / 1024 * 1024; }
 
 // decode (GEMV) up to this many tokens; the tensor-core GEMM above
 constexpr int64_t kGemvMaxTokens = 8;
@@ -41,7 +49,7 @@ extern "C" size_t tb_packed_linear_algo_workspace_size(int64_t M, int64_t K, int
                                                        int algo) {
   using namespace tb;
   if (check_linear_shape(M, K, block, N) != TB_OK) return 0;
-  return resolve_algo(M, algo) == TB_ALGO_TC ? gemm_tc_workspace(M, K) : 0;
+  return fixup_region() + (resolve_algo(M, algo) == TB_ALGO_TC ? gemm_tc_workspace(M, K) : 0);
 }
 
 extern "C" size_t tb_packed_linear_workspace_size(int64_t M, int64_t K, int64_t N, int block) {
@@ -69,10 +77,14 @@ extern "C" int tb_packed_linear_algo(const uint16_t* x, int64_t M, int64_t K, co
   const __half* bh = reinterpret_cast<const __half*>(biases);
   __half* yh = reinterpret_cast<__half*>(y);
   if (use == TB_ALGO_TC) {
-    const size_t need = gemm_tc_workspace(M, K);
+    const size_t need = fixup_region() + gemm_tc_workspace(M, K);
     if (!workspace || workspace_bytes < need) return TB_ERR_WORKSPACE;
-    return launch_gemm_tc(xh, M, K, sg, block, w, sh, bh, N, yh, workspace, dev_status, s);
+    return launch_gemm_tc(xh, M, K, sg, block, w, sh, bh, N, yh,
+                          static_cast<char*>(workspace) + fixup_region(), dev_status, s);
   }
+  if (K % kBlock == 0)  // TMA-streamed GEMV; without a workspace its ranges stay on tile bounds
+    return launch_gemv_tma(xh, M, K, sg, block, w, sh, bh, N, yh, workspace, workspace_bytes,
+                           dev_status, s);
   return launch_gemv(xh, M, K, sg, block, w, sh, bh, N, yh, dev_status, s);
 }
 

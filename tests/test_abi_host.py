@@ -84,11 +84,12 @@ def test_packed_linear_refuses_bad_arguments(lib):
 
 def test_workspace_size_query(lib):
     ws = lib.tb_packed_linear_workspace_size
-    assert ws(1, 5120, 17408, 1024) == 0            # decode path: none
-    assert ws(8, 5120, 17408, 1024) == 0
-    assert ws(512, 5120, 17408, 1024) == 512 * 5120 * 2
+    fix = ws(1, 5120, 17408, 1024)                  # decode path: the fixup region only
+    assert 0 < fix <= 2 << 20 and fix % 1024 == 0
+    assert ws(8, 5120, 17408, 1024) == fix
+    assert ws(512, 5120, 17408, 1024) == fix + 512 * 5120 * 2
     assert ws(512, 1000, 17408, 1024) == 0          # invalid shape -> 0
-    assert lib.tb_packed_linear_algo_workspace_size(4, 2048, 64, 1024, 2) == 4 * 2048 * 2
+    assert lib.tb_packed_linear_algo_workspace_size(4, 2048, 64, 1024, 2) == fix + 4 * 2048 * 2
 
 
 def test_other_entry_points_refuse_bad_arguments(lib):

@@ -38,18 +38,27 @@ def dev(a):
     return torch.from_numpy(np.ascontiguousarray(a)).cuda()
 
 
-def run_linear(tb, x16, signs, block, w, s, b, N, algo=0):
+def run_linear(tb, x16, signs, block, w, s, b, N, algo=0, workspace="zeros", repeat=1):
+    """One tb_packed_linear call (or `repeat` calls reusing one workspace)."""
     M, K = x16.shape
     xd = dev(x16)
     sd = dev(signs) if signs is not None else None
-    y = torch.full((M, N), float("nan"), dtype=torch.float16, device="cuda")
     nws = tb.tb_packed_linear_workspace_size(M, K, N, block, algo)
-    ws = torch.empty(max(nws, 16), dtype=torch.uint8, device="cuda") if nws else None
+    ws = torch.zeros(nws, dtype=torch.uint8, device="cuda") if workspace == "zeros" else None
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
-    tb.tb_packed_linear(xd, sd, block, w, s, b, y, ws, st, algo=algo)
+    outs = []
+    for _ in range(repeat):
+        y = torch.full((M, N), float("nan"), dtype=torch.float16, device="cuda")
+        tb.tb_packed_linear(xd, sd, block, w, s, b, y, ws, st, algo=algo)
+        outs.append(y)
     torch.cuda.synchronize()
     assert int(st.item()) == 0
-    return y.cpu().numpy()
+    if ws is not None:  # the fixup region (tile sums and counters) is left zero for the next call
+        fix = tb.tb_packed_linear_workspace_size(1, K, N, block, 1)
+        assert int(ws[:fix].count_nonzero().item()) == 0
+    if repeat > 1:
+        return [o.cpu().numpy() for o in outs]
+    return outs[0].cpu().numpy()
 
 
 # ---------------------------------------------------------------- packing
@@ -153,6 +162,26 @@ def test_linear_tokens_and_ragged_rows(tb, M, algo):
     y = run_linear(tb, x, sg, 1024, w, s, b, N, algo=algo)
     ref, bound = linear_reference(x, sg, 1024, L)
     assert_linear_close(y, ref, bound, f"M={M} algo={algo}")
+
+
+@pytest.mark.parametrize("K,N", [(2048, 77), (17408, 5120), (5120, 1024), (1024, 33)])
+@pytest.mark.parametrize("M", [1, 3])
+def test_gemv_split_schedule_and_reuse(tb, K, N, M):
+    # stream-K ranges split row tiles between SMs; the same workspace serves two calls in a
+    # row; without a workspace the ranges stay on tile boundaries and agree
+    x = ti.activations(40 + M, M, K)
+    sg = ti.rademacher_signs(40, K)
+    L = HostLayer(40, N, K)
+    w, s, b = device_layer(40, N, K, from_host=L)
+    ref, bound = linear_reference(x, sg, 1024, L)
+    y1, y2 = run_linear(tb, x, sg, 1024, w, s, b, N, algo=1, repeat=2)
+    y3 = run_linear(tb, x, sg, 1024, w, s, b, N, algo=1, workspace=None)
+    for y, what in ((y1, "split"), (y2, "split, second call"), (y3, "tile aligned")):
+        assert_linear_close(y, ref, bound, f"{what} M={M} {K}->{N}")
+    # stage partials of a tile meet in fp32 shared-memory atomics, whose order may change
+    # between calls: the two calls agree to an fp16 unit in the last place or two
+    ulp = np.spacing(np.abs(y1).astype(np.float16)).astype(np.float64)
+    assert (np.abs(y1.astype(np.float64) - y2.astype(np.float64)) <= 2 * ulp).all()
 
 
 @pytest.mark.parametrize("algo", [1, 2])
