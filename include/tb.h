@@ -54,7 +54,8 @@ enum {
   TB_ERR_VALUE = -4,       /* a host-checked value is invalid */
   TB_ERR_CUDA = -5,        /* a CUDA launch or query failed (see tb_last_cuda_error) */
   TB_ERR_ALIGN = -6,       /* a device pointer is not 16-byte aligned */
-  TB_ERR_WORKSPACE = -7    /* workspace NULL or smaller than the size query returned */
+  TB_ERR_WORKSPACE = -7,   /* workspace NULL or smaller than the size query returned */
+  TB_ERR_TOO_LARGE = -8    /* beyond what the fixed scratch of tb_packed_linear_gemv_noalloc holds */
 };
 
 /* bits OR-ed into *dev_status by kernels */
@@ -165,6 +166,29 @@ int tb_packed_linear_algo(const uint16_t* x, int64_t M, int64_t K, const int8_t*
 int tb_embed_lookup(const int32_t* ids, int64_t T, const uint32_t* w, const uint16_t* scales,
                     const uint16_t* biases, int64_t V, int64_t D, const int8_t* signs, int block,
                     uint16_t* out, int32_t* dev_status, void* stream);
+
+/*
+ * tb_packed_linear_gemv_noalloc — the decode GEMV of tb_packed_linear for callers that
+ * cannot provide device memory.  (No counterpart on the pages: it exists for callers
+ * that are not allowed to allocate, e.g. code running under CUDA graph capture, plugins
+ * inside a host runtime that owns all device memory, or services with a fixed memory
+ * budget after start-up.)
+ * Same arguments and result as tb_packed_linear for M <= 8 tokens, without workspace.
+ * The state of the GEMV's split schedule lives in a fixed array inside the library
+ * (about 1 MiB on every GPU that loads it, held until the process exits).
+ *   - It allocates nothing: no cudaMalloc, no cudaFree, no allocating library call.
+ *   - Limits: M <= 8 and a GPU with at most 256 SMs, else TB_ERR_TOO_LARGE;
+ *     K a positive multiple of 1024 (block 1024, or block 0 with such a K), else TB_ERR_SHAPE.
+ *   - The first call on each device looks up the array's device address for that device
+ *     (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   - Each call clears the array on `stream` before using it (cudaMemsetAsync).  All calls
+ *     share the one array: calls that can overlap on the GPU (different streams, or
+ *     different host threads) race and give wrong results; order them on one stream.
+ */
+int tb_packed_linear_gemv_noalloc(const uint16_t* x, int64_t M, int64_t K, const int8_t* signs,
+                                  int block, const uint32_t* w, const uint16_t* scales,
+                                  const uint16_t* biases, int64_t N, uint16_t* y,
+                                  int32_t* dev_status, void* stream);
 
 #ifdef __cplusplus
 }

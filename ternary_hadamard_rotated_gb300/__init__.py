@@ -25,6 +25,7 @@ TB_ERR_VALUE = -4
 TB_ERR_CUDA = -5
 TB_ERR_ALIGN = -6
 TB_ERR_WORKSPACE = -7
+TB_ERR_TOO_LARGE = -8
 
 TB_DEV_BAD_CODE = 1
 TB_DEV_BAD_ID = 2
@@ -54,6 +55,7 @@ _SIGNATURES = {
     "tb_packed_linear_algo": (_INT, [_P, _I64, _I64, _P, _INT, _P, _P, _P, _I64, _P, _P, _SZ, _P,
                                      _INT, _P]),
     "tb_embed_lookup": (_INT, [_P, _I64, _P, _P, _P, _I64, _I64, _P, _INT, _P, _P, _P]),
+    "tb_packed_linear_gemv_noalloc": (_INT, [_P, _I64, _I64, _P, _INT, _P, _P, _P, _I64, _P, _P, _P]),
 }
 
 EXPORTED = tuple(_SIGNATURES)
@@ -147,3 +149,13 @@ def tb_embed_lookup(ids, w, scales, biases, signs, block, out, dev_status=None, 
     _check("tb_embed_lookup",
            load().tb_embed_lookup(_ptr(ids), T, _ptr(w), _ptr(scales), _ptr(biases), V, D,
                                   _ptr(signs), block, _ptr(out), _ptr(dev_status), _stream(stream)))
+
+
+def tb_packed_linear_gemv_noalloc(x, signs, block, w, scales, biases, y, dev_status=None, stream=None):
+    """Decode GEMV (M <= 8) without a workspace: its scratch is a fixed array in the library."""
+    M, K = x.shape
+    N = y.shape[-1]
+    _check("tb_packed_linear_gemv_noalloc",
+           load().tb_packed_linear_gemv_noalloc(_ptr(x), M, K, _ptr(signs), block, _ptr(w),
+                                                _ptr(scales), _ptr(biases), N, _ptr(y),
+                                                _ptr(dev_status), _stream(stream)))

@@ -54,6 +54,7 @@ extern "C" const char* tb_status_string(int status) {
     case TB_ERR_CUDA: return "CUDA error (see tb_last_cuda_error)";
     case TB_ERR_ALIGN: return "device pointer not 16-byte aligned";
     case TB_ERR_WORKSPACE: return "workspace missing or too small";
+    case TB_ERR_TOO_LARGE: return "problem exceeds the fixed scratch of the no-allocation entry point";
     default: return "unknown status";
   }
 }
