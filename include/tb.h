@@ -154,6 +154,23 @@ int tb_packed_linear_algo(const uint16_t* x, int64_t M, int64_t K, const int8_t*
                           int32_t* dev_status, int algo, void* stream);
 
 /*
+ * tb_packed_linear_multi — tb_packed_linear for n (1..4) packed matrices that read the same
+ * input x, as the q/k/v, gate/up and in_proj_qkv/in_proj_z modules of one layer do
+ * ([ARCH] "Hadamard 旋转": the folded transform depends only on the input width, so the
+ * modules that share x also share x' = fwht(x)).  x' is computed once per launch; matrix i
+ * writes y[i] (fp16 [M, N[i]]).  w, scales, biases, N, y are HOST arrays of n entries holding
+ * device pointers / row counts; K must be a positive multiple of 1024.  Workspace as for
+ * tb_packed_linear, sized with tb_packed_linear_workspace_size(M, K, max N, block).
+ * M <= 8: one decode GEMV launch for all matrices.  M > 8: one rotation, then one tensor-core
+ * GEMM per matrix.
+ */
+int tb_packed_linear_multi(const uint16_t* x, int64_t M, int64_t K, const int8_t* signs, int block,
+                           int n, const uint32_t* const* w, const uint16_t* const* scales,
+                           const uint16_t* const* biases, const int64_t* N, uint16_t* const* y,
+                           void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                           void* stream);
+
+/*
  * tb_embed_lookup — Packed.__call__ on the embedding path.
  * [ARCH] "Hadamard 旋转" (return fwht(out, block, signs, inverse=True)) and
  * [PACK] "文本模型加载" (mx.dequantize of the looked-up rows, then the inverse transform).

@@ -7,7 +7,7 @@ on the current torch stream unless a stream is given.  There is no CPU path:
 if the library is not built, importing the calls raises.
 
 Names follow the C ABI: ``tb_pack_w2``, ``tb_unpack_w2``, ``tb_fwht``,
-``tb_packed_linear``, ``tb_embed_lookup``.
+``tb_packed_linear``, ``tb_packed_linear_multi``, ``tb_embed_lookup``.
 """
 from __future__ import annotations
 
@@ -56,6 +56,8 @@ _SIGNATURES = {
                                      _INT, _P]),
     "tb_embed_lookup": (_INT, [_P, _I64, _P, _P, _P, _I64, _I64, _P, _INT, _P, _P, _P]),
     "tb_packed_linear_gemv_noalloc": (_INT, [_P, _I64, _I64, _P, _INT, _P, _P, _P, _I64, _P, _P, _P]),
+    "tb_packed_linear_multi": (_INT, [_P, _I64, _I64, _P, _INT, _INT, _P, _P, _P, _P, _P, _P, _SZ, _P,
+                                      _P]),
 }
 
 EXPORTED = tuple(_SIGNATURES)
@@ -140,6 +142,25 @@ def tb_packed_linear(x, signs, block, w, scales, biases, y, workspace=None, dev_
            load().tb_packed_linear_algo(_ptr(x), M, K, _ptr(signs), block, _ptr(w), _ptr(scales),
                                         _ptr(biases), N, _ptr(y), _ptr(workspace), ws_bytes,
                                         _ptr(dev_status), algo, _stream(stream)))
+
+
+def tb_packed_linear_multi(x, signs, block, mats, ys, workspace=None, dev_status=None, stream=None):
+    """One call for several packed matrices reading the same x.
+
+    mats: sequence of (w, scales, biases); ys: matching outputs [M, N_i].
+    """
+    M, K = x.shape
+    n = len(mats)
+    arr_p = ctypes.c_void_p * n
+    w = arr_p(*[_ptr(m[0]) for m in mats])
+    sc = arr_p(*[_ptr(m[1]) for m in mats])
+    bi = arr_p(*[_ptr(m[2]) for m in mats])
+    Ns = (ctypes.c_int64 * n)(*[int(y.shape[-1]) for y in ys])
+    yp = arr_p(*[_ptr(y) for y in ys])
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("tb_packed_linear_multi",
+           load().tb_packed_linear_multi(_ptr(x), M, K, _ptr(signs), block, n, w, sc, bi, Ns, yp,
+                                         _ptr(workspace), ws_bytes, _ptr(dev_status), _stream(stream)))
 
 
 def tb_embed_lookup(ids, w, scales, biases, signs, block, out, dev_status=None, stream=None):

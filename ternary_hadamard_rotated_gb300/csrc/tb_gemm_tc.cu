@@ -283,13 +283,11 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_tiled_fn() {
 
 size_t gemm_tc_workspace(int64_t M, int64_t K) { return (size_t)M * (size_t)K * 2; }
 
-int launch_gemm_tc(const __half* x, int64_t M, int64_t K, const int8_t* signs, int block,
-                   const uint32_t* w, const __half* scales, const __half* biases, int64_t N,
-                   __half* y, void* workspace, int32_t* status, cudaStream_t s) {
+// the GEMM alone, on x' already rotated into pair order in xp (fp16 [M, K])
+int launch_gemm_tc_rotated(const __half* xp, int64_t M, int64_t K, const uint32_t* w,
+                           const __half* scales, const __half* biases, int64_t N, __half* y,
+                           int32_t* status, cudaStream_t s) {
   if (M > 0x7fffffffLL || N > 0x7fffffffLL || K > (1 << 24)) return TB_ERR_SHAPE;
-  __half* xp = static_cast<__half*>(workspace);
-  int rc = launch_rotate_pairorder(x, xp, signs, M, K, block != 0, s);
-  if (rc != TB_OK) return rc;
 
   CUtensorMap tm;
   const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
@@ -298,7 +296,7 @@ int launch_gemm_tc(const __half* x, int64_t M, int64_t K, const int8_t* signs, i
   const cuuint32_t estr[2] = {1, 1};
   PFN_cuTensorMapEncodeTiled_v12000 encode = encode_tiled_fn();
   if (!encode) return TB_ERR_CUDA;
-  CUresult cr = encode(&tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, xp, dims, strides,
+  CUresult cr = encode(&tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<__half*>(xp), dims, strides,
                                        box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -323,6 +321,16 @@ int launch_gemm_tc(const __half* x, int64_t M, int64_t K, const int8_t* signs, i
   dim3 grid((unsigned)((N + kTcBN - 1) / kTcBN), (unsigned)((M + kTcBM - 1) / kTcBM));
   w2_gemm_tc_kernel<<<grid, kTcThreads, kTcSmemBytes, s>>>(tm, a);
   return check_launch();
+}
+
+int launch_gemm_tc(const __half* x, int64_t M, int64_t K, const int8_t* signs, int block,
+                   const uint32_t* w, const __half* scales, const __half* biases, int64_t N,
+                   __half* y, void* workspace, int32_t* status, cudaStream_t s) {
+  if (M > 0x7fffffffLL || N > 0x7fffffffLL || K > (1 << 24)) return TB_ERR_SHAPE;
+  __half* xp = static_cast<__half*>(workspace);
+  int rc = launch_rotate_pairorder(x, xp, signs, M, K, block != 0, s);
+  if (rc != TB_OK) return rc;
+  return launch_gemm_tc_rotated(xp, M, K, w, scales, biases, N, y, status, s);
 }
 
 }  // namespace tb

@@ -48,23 +48,40 @@ constexpr int kTmaConsumers = kGroupsOfWarps * kWarpsPerUnit;
 constexpr int kTmaThreads = (kTmaConsumers + 1) * 32;
 constexpr int kTmaFwhtWarps = 8;
 constexpr int kMaxSlotsPerGroup = 4;
-constexpr int kScaleStageBytes = 32 * kUnitGroups * 2 * 2;  // per warp: 32 rows x 4 groups, s and b
+constexpr int kScaleStageBytes = 32 * kUnitGroups * 8;  // per warp: 32 rows x 4 groups of fp32 (s, b)
 constexpr uint32_t kMagic1024 = 0x64006400u;
 
+constexpr int kMaxMats = 4;  // matrices sharing one input in one launch
+
 struct GemvTmaArgs {
-  const __half* x;        // [Mc, K]
-  const int8_t* signs;    // [K] or null
-  const __half* scales;   // [N, G]
-  const __half* biases;   // [N, G]
-  __half* y;              // [Mc, N]
-  float* ws_partial;      // [kFixupCtas][128][MT] fp32 sums of shared tiles, or null (tile-aligned)
-  int* ws_count;          // [kFixupCtas]
-  int Mc, K, N, G, C;     // C = units per tile = K / 512
+  const __half* x;               // [Mc, K]
+  const int8_t* signs;           // [K] or null
+  const __half* scales[kMaxMats];  // [N_i, G]
+  const __half* biases[kMaxMats];  // [N_i, G]
+  __half* y[kMaxMats];           // [Mc, N_i]
+  int N[kMaxMats];               // rows of matrix i
+  int tile0[kMaxMats + 1];       // first 128-row tile of matrix i in the concatenated tile list
+  int nmat;
+  float* ws_partial;             // [kFixupCtas][128][MT] fp32 sums of shared tiles, or null (tile-aligned)
+  int* ws_count;                 // [kFixupCtas]
+  int Mc, K, G, C;               // C = units per tile = K / 512
   int rotate, dw, tslots;
-  int n_tiles;            // ceil(N / 128)
-  int split;              // 1: stream-K ranges; 0: ranges on tile boundaries
+  int n_tiles;                   // total 128-row tiles of all matrices
+  int split;                     // 1: stream-K ranges; 0: ranges on tile boundaries
   int32_t* status;
 };
+
+struct CodeMaps {
+  CUtensorMap m[kMaxMats];
+};
+
+// matrix of a global tile index
+TB_DEVI int mat_of(const GemvTmaArgs& a, int tile) {
+  int i = 0;
+#pragma unroll
+  for (int k = 1; k < kMaxMats; ++k) i += (k < a.nmat && tile >= a.tile0[k]);
+  return i;
+}
 
 struct GemvTmaLayout {
   int codes, img, cs, scratch, sstage, accs, cnt, bars, total;
@@ -88,9 +105,9 @@ __host__ __device__ inline GemvTmaLayout gemv_tma_layout(int G, int dw, int tslo
   L.sstage = off;
   off += kTmaConsumers * kScaleStageBytes;
   L.accs = off;
-  off += tslots * kUnitRows * MT * 4;
+  off += (tslots + 1) * kUnitRows * MT * 4;
   L.cnt = off;
-  off += tslots * 4;
+  off += (tslots + 1) * 4;
   off = rup(off, 8);
   L.bars = off;
   off += 2 * kGroupsOfWarps * dw * 8;
@@ -140,7 +157,7 @@ TB_DEVI void tma2d(uint32_t dst, const CUtensorMap* tm, int x, int y, uint64_t* 
 // independent accumulator chains sharing one B fragment), scale epilogue.
 //   box:  the unit's code box; R0, R0 + 16: this lane's A rows of block 0 (block 1 = + 16)
 //   imgt: B-fragment image entry of this lane; csa: (C, S) pairs [G][MT]
-//   ss:   this warp's staged scales [32 rows][4] (biases follow after 256 B)
+//   ss:   this warp's staged (scale, bias) pairs, fp32 [32 rows][4 groups]
 template <int MT>
 TB_DEVI void unit_group(uint32_t box, int R0, int t, int gi, int grp, uint32_t imgt, uint32_t ss,
                         int rA, uint32_t csa, int t0, int t1, float (&acc)[2][4]) {
@@ -154,7 +171,7 @@ TB_DEVI void unit_group(uint32_t box, int R0, int t, int gi, int grp, uint32_t i
       w[j][h] = ld_shared_v2(box + R * 128 + ((c ^ (rA & 7)) << 4) + (t & 1) * 8);
     }
   const float2 cs0 = ld_shared_f2(csa + (grp * MT + t0) * 8);
-  const float2 cs1 = ld_shared_f2(csa + (grp * MT + t1) * 8);
+  const float2 cs1 = MT > 1 ? ld_shared_f2(csa + (grp * MT + t1) * 8) : cs0;
   float d[2][4];
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
@@ -185,27 +202,27 @@ TB_DEVI void unit_group(uint32_t box, int R0, int t, int gi, int grp, uint32_t i
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
     const int ra = 16 * j + rA, rb = ra + 8;  // rows within the warp's 32
-    const float sA = ld_shared_half(ss + (ra * kUnitGroups + gi) * 2);
-    const float bA = ld_shared_half(ss + 256 + (ra * kUnitGroups + gi) * 2);
-    const float sB = ld_shared_half(ss + (rb * kUnitGroups + gi) * 2);
-    const float bB = ld_shared_half(ss + 256 + (rb * kUnitGroups + gi) * 2);
-    acc[j][0] = fmaf(sA, d[j][0], fmaf(bA, cs0.y, acc[j][0]));
-    acc[j][1] = fmaf(sA, d[j][1], fmaf(bA, cs1.y, acc[j][1]));
-    acc[j][2] = fmaf(sB, d[j][2], fmaf(bB, cs0.y, acc[j][2]));
-    acc[j][3] = fmaf(sB, d[j][3], fmaf(bB, cs1.y, acc[j][3]));
+    const float2 A = ld_shared_f2(ss + (ra * kUnitGroups + gi) * 8);  // (s, b) of row ra
+    const float2 B = ld_shared_f2(ss + (rb * kUnitGroups + gi) * 8);
+    acc[j][0] = fmaf(A.x, d[j][0], fmaf(A.y, cs0.y, acc[j][0]));
+    acc[j][2] = fmaf(B.x, d[j][2], fmaf(B.y, cs0.y, acc[j][2]));
+    if (MT > 1) {  // D columns 2t+1 hold a second token only when there is one
+      acc[j][1] = fmaf(A.x, d[j][1], fmaf(A.y, cs1.y, acc[j][1]));
+      acc[j][3] = fmaf(B.x, d[j][3], fmaf(B.y, cs1.y, acc[j][3]));
+    }
   }
 }
 
 template <int MT>
 __global__ void __launch_bounds__(kTmaThreads, 1)
-    w2_gemv_tma_kernel(const __grid_constant__ CUtensorMap tmW, const GemvTmaArgs a) {
+    w2_gemv_tma_kernel(const __grid_constant__ CodeMaps maps, const __grid_constant__ GemvTmaArgs a) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   // unit group u owns slots [u*DW, (u+1)*DW) and takes the CTA's units u, u + 3, ... in
   // order, so no wait is ever more than one phase ahead of its barrier
-  const int DW = a.dw, TS = a.tslots, C = a.C, G = a.G, K = a.K, N = a.N;
+  const int DW = a.dw, TS = a.tslots, C = a.C, G = a.G, K = a.K;
   const GemvTmaLayout L = gemv_tma_layout<MT>(G, DW, TS);
   const uint32_t codes_u32 = smem_u32(smem + L.codes);
   __half* img = reinterpret_cast<__half*>(smem + L.img);
@@ -231,6 +248,21 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
   }
   const int nst = (int)(hi - lo);
   const int64_t tile_lo = lo / C;
+  // Order of this CTA's units: a partial tail tile first, then a partial head tile, then the
+  // complete tiles in order, so the cross-CTA sums of the shared tiles overlap the rest of
+  // the work.  The partial tail tile has its own accumulator slot (TS).
+  const int64_t last_tile = (hi - 1) / C;
+  const bool one_tile = tile_lo == last_tile;
+  const int hp = (!one_tile && lo % C) ? (int)((tile_lo + 1) * C - lo) : 0;
+  const int tp = (!one_tile && hi % C) ? (int)(hi - last_tile * C) : 0;
+  auto unit_of = [&](int q) -> int64_t {
+    if (q < tp) return last_tile * C + q;
+    if (q < tp + hp) return lo + (q - tp);
+    return lo + (q - tp);  // head and middle in order after the tail
+  };
+  auto slot_of = [&](int64_t tile) -> int {
+    return (tp > 0 && tile == last_tile) ? TS : (int)((tile - tile_lo) % TS);
+  };
 
   if (threadIdx.x == 0) {
     aborted = 0;
@@ -240,8 +272,8 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     }
     fence_barrier_init();
   }
-  for (int i = threadIdx.x; i < TS * kUnitRows * MT; i += blockDim.x) accs[i] = 0.f;
-  for (int i = threadIdx.x; i < TS; i += blockDim.x) cnt[i] = 0;
+  for (int i = threadIdx.x; i < (TS + 1) * kUnitRows * MT; i += blockDim.x) accs[i] = 0.f;
+  for (int i = threadIdx.x; i <= TS; i += blockDim.x) cnt[i] = 0;
   __syncthreads();
 
   auto wait = [&](uint64_t* bar, uint32_t parity) {
@@ -260,10 +292,12 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         const int n = q / kGroupsOfWarps, j = n % DW, k = n / DW;
         const int slot = (q % kGroupsOfWarps) * DW + j;
         if (k > 0) wait(empty + slot, (k - 1) & 1);
-        const int64_t s = lo + q;
+        const int64_t s = unit_of(q);
         const int tile = (int)(s / C), chunk = (int)(s - (int64_t)tile * C);
+        const int mi = mat_of(a, tile);
         mbar_arrive_expect_tx(full + slot, kBoxBytes);
-        tma2d(codes_u32 + slot * kBoxBytes, &tmW, chunk * 32, tile * kUnitRows, full + slot, pol);
+        tma2d(codes_u32 + slot * kBoxBytes, &maps.m[mi], chunk * 32, (tile - a.tile0[mi]) * kUnitRows,
+              full + slot, pol);
       }
       // leave no copy in flight: the last use of every slot has completed
       for (int q = nst - 1; q >= 0 && q >= nst - kGroupsOfWarps * DW; --q) {
@@ -283,13 +317,14 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     sv = make_uint2(0, 0);
     bv = make_uint2(0, 0);
     if (q >= nst) return;
-    const int64_t s = lo + q;
+    const int64_t s = unit_of(q);
     const int tile = (int)(s / C), chunk = (int)(s - (int64_t)tile * C);
-    const int row = tile * kUnitRows + 32 * wi + lane;
-    if (row < N) {
+    const int mi = mat_of(a, tile);
+    const int row = (tile - a.tile0[mi]) * kUnitRows + 32 * wi + lane;
+    if (row < a.N[mi]) {
       const int64_t off = (int64_t)row * G + chunk * kUnitGroups;
-      sv = __ldg(reinterpret_cast<const uint2*>(a.scales + off));
-      bv = __ldg(reinterpret_cast<const uint2*>(a.biases + off));
+      sv = __ldg(reinterpret_cast<const uint2*>(a.scales[mi] + off));
+      bv = __ldg(reinterpret_cast<const uint2*>(a.biases[mi] + off));
     }
   };
   uint2 s0, b0, s1, b1;
@@ -304,24 +339,34 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
       float* sw = scratch + warp * kWarpScratchFloats;
       for (int it = warp; it < MT * nchunk; it += kTmaFwhtWarps) {
         const int tok = it / nchunk, b = it - tok * nchunk;
+        // layout A: v[r] = element b*1024 + lane*32 + r (four 16-byte loads of x, two of signs)
         float v[32];
         if (tok < a.Mc) {
+          const uint4* xs = reinterpret_cast<const uint4*>(a.x + (int64_t)tok * K + b * kBlock + lane * 32);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            float f = __half2float(a.x[(int64_t)tok * K + b * kBlock + j * 32 + lane]);
-            if (a.signs && a.signs[b * kBlock + j * 32 + lane] < 0) f = -f;
-            v[j] = f;
+          for (int q4 = 0; q4 < 4; ++q4) {
+            const uint4 u = __ldg(xs + q4);
+            const __half* h = reinterpret_cast<const __half*>(&u);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v[8 * q4 + e] = __half2float(h[e]);
+          }
+          if (a.signs) {
+            const uint4* sp = reinterpret_cast<const uint4*>(a.signs + b * kBlock + lane * 32);
+            const uint4 s01[2] = {__ldg(sp), __ldg(sp + 1)};
+            const int8_t* sg = reinterpret_cast<const int8_t*>(s01);
+#pragma unroll
+            for (int r = 0; r < 32; ++r)
+              if (sg[r] < 0) v[r] = -v[r];
           }
         } else {
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] = 0.f;
         }
         if (a.rotate) {
-          wht1024_b_to_a(v, sw, lane);
+          wht1024_a_to_b(v, sw, lane);   // bits 0..4 and 5..9 of the element index
+          transpose_b_to_a(v, sw, lane);  // back to layout A for the image
 #pragma unroll
           for (int r = 0; r < 32; ++r) v[r] *= kInvSqrtBlock;
-        } else {
-          transpose_b_to_a(v, sw, lane);
         }
         const int grp = b * (kBlock / kGroup) + (lane >> 2);
         float ssum = 0.f, csum = 0.f;
@@ -367,9 +412,13 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
   for (int q = ug, n = 0; q < nst; q += kGroupsOfWarps, ++n) {
     // stage this unit's scales and biases, prefetch the ones two units ahead
     {
-      const uint32_t r = ss + lane * kUnitGroups * 2;
-      asm volatile("st.shared.v2.u32 [%0], {%1,%2};" ::"r"(r), "r"(s0.x), "r"(s0.y) : "memory");
-      asm volatile("st.shared.v2.u32 [%0], {%1,%2};" ::"r"(r + 256), "r"(b0.x), "r"(b0.y) : "memory");
+      const uint32_t r = ss + lane * kUnitGroups * 8;
+      const __half2 sh0 = *reinterpret_cast<const __half2*>(&s0.x), sh1 = *reinterpret_cast<const __half2*>(&s0.y);
+      const __half2 bh0 = *reinterpret_cast<const __half2*>(&b0.x), bh1 = *reinterpret_cast<const __half2*>(&b0.y);
+      const float2 sf0 = __half22float2(sh0), sf1 = __half22float2(sh1);
+      const float2 bf0 = __half22float2(bh0), bf1 = __half22float2(bh1);
+      asm volatile("st.shared.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(r), "f"(sf0.x), "f"(bf0.x), "f"(sf0.y), "f"(bf0.y) : "memory");
+      asm volatile("st.shared.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(r + 16), "f"(sf1.x), "f"(bf1.x), "f"(sf1.y), "f"(bf1.y) : "memory");
       s0 = s1;
       b0 = b1;
       load_sb(q + 2 * kGroupsOfWarps, s1, b1);
@@ -377,19 +426,18 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     }
     const int slot = ug * DW + n % DW;
     wait(full + slot, (n / DW) & 1);
-    const int64_t s = lo + q;
+    const int64_t s = unit_of(q);
     const int tile = (int)(s / C), chunk = (int)(s - (int64_t)tile * C);
     const uint32_t box = codes_u32 + slot * kBoxBytes;
     float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll 1
+#pragma unroll
     for (int gi = 0; gi < kUnitGroups; ++gi)
       unit_group<MT>(box, 32 * wi + rA, t, gi, chunk * kUnitGroups + gi, imgt, ss, rA, csa, t0, t1, acc);
     __syncwarp();
     if (lane == 0) mbar_arrive(empty + slot);
 
     // add this warp's 32 rows into the tile's shared accumulator
-    const int lt = (int)(tile - tile_lo);
-    const int ts = lt % TS;
+    const int ts = slot_of(tile);
     const uint32_t atu = accs_u32 + ts * kUnitRows * MT * 4;
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
@@ -418,6 +466,9 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     // this warp finishes the tile for this CTA
     __threadfence_block();
     float* at = accs + ts * kUnitRows * MT;
+    const int mi = mat_of(a, tile);
+    const int N = a.N[mi], row0 = (tile - a.tile0[mi]) * kUnitRows;
+    __half* yo = a.y[mi];
     const bool complete = t_beg >= lo && t_end <= hi;
     // a tile shared with other CTAs is summed in the workspace slot of its first CTA
     const int first = complete ? 0 : stage_owner(t_beg, S, gridDim.x);
@@ -427,8 +478,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
       at[e] = 0.f;
       const int r_ = e / MT, k_ = e - r_ * MT;
       if (complete) {
-        if (tile * kUnitRows + r_ < N && k_ < a.Mc)
-          a.y[(int64_t)k_ * N + tile * kUnitRows + r_] = __float2half_rn(u);
+        if (row0 + r_ < N && k_ < a.Mc) yo[(int64_t)k_ * N + row0 + r_] = __float2half_rn(u);
       } else {
         atomicAdd(wsum + e, u);
       }
@@ -451,8 +501,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
       const float v = __ldcg(wsum + e);
       wsum[e] = 0.f;
       const int r_ = e / MT, k_ = e - r_ * MT;
-      if (tile * kUnitRows + r_ < N && k_ < a.Mc)
-        a.y[(int64_t)k_ * N + tile * kUnitRows + r_] = __float2half_rn(v);
+      if (row0 + r_ < N && k_ < a.Mc) yo[(int64_t)k_ * N + row0 + r_] = __float2half_rn(v);
     }
     if (lane == 0) a.ws_count[first] = 0;
   }
@@ -524,7 +573,7 @@ constexpr size_t kFixupPartialBytes = (size_t)kFixupCtas * kUnitRows * 8 * 4;
 size_t gemv_fixup_bytes() { return kFixupPartialBytes + kFixupCtas * 4; }
 
 template <int MT>
-static int launch_tma_mt(GemvTmaArgs a, const CUtensorMap& m, int64_t M, int64_t K, int64_t N,
+static int launch_tma_mt(GemvTmaArgs a, const CodeMaps& maps, int64_t M, int64_t K,
                          const DeviceFacts& f, cudaStream_t s) {
   // slots per unit group from what is left of shared memory
   int dw = kMaxSlotsPerGroup;
@@ -544,10 +593,11 @@ static int launch_tma_mt(GemvTmaArgs a, const CUtensorMap& m, int64_t M, int64_t
   if (!a.split && a.n_tiles < grid) grid = a.n_tiles;
   if (S < grid) grid = (int)S;
   const __half* x0 = a.x;
-  __half* y0 = a.y;
+  __half* y0[kMaxMats];
+  for (int i = 0; i < a.nmat; ++i) y0[i] = a.y[i];
   for (int64_t m0 = 0; m0 < M; m0 += MT) {
     a.x = x0 + m0 * K;
-    a.y = y0 + m0 * N;
+    for (int i = 0; i < a.nmat; ++i) a.y[i] = y0[i] + m0 * a.N[i];
     a.Mc = (int)((M - m0) < MT ? (M - m0) : MT);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
@@ -559,7 +609,7 @@ static int launch_tma_mt(GemvTmaArgs a, const CUtensorMap& m, int64_t M, int64_t
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, w2_gemv_tma_kernel<MT>, m, a);
+    e = cudaLaunchKernelEx(&cfg, w2_gemv_tma_kernel<MT>, maps, a);
     if (e != cudaSuccess) {
       record_cuda_error(e);
       return TB_ERR_CUDA;
@@ -584,43 +634,61 @@ static int tma_tokens_per_pass(int64_t M, int G, int C, int smem_optin) {
   return mt;
 }
 
-int launch_gemv_tma(const __half* x, int64_t M, int64_t K, const int8_t* signs, int block,
-                    const uint32_t* w, const __half* scales, const __half* biases, int64_t N,
-                    __half* y, void* workspace, size_t ws_bytes, int32_t* status, cudaStream_t s) {
+// One launch for up to kMaxMats packed matrices that read the same x (their row tiles are
+// concatenated; the rotated x' is computed once per CTA for all of them).
+int launch_gemv_tma_multi(const __half* x, int64_t M, int64_t K, const int8_t* signs, int block,
+                          int nmat, const uint32_t* const* w, const __half* const* scales,
+                          const __half* const* biases, const int64_t* N, __half* const* y,
+                          void* workspace, size_t ws_bytes, int32_t* status, cudaStream_t s) {
   DeviceFacts f;
   int rc = device_facts(&f);
   if (rc != TB_OK) return rc;
-  if (N > (1LL << 30) || K > (1 << 22) || K % kBlock) return TB_ERR_SHAPE;
-  CUtensorMap m;
-  rc = code_map(w, N, K, &m);
-  if (rc != TB_OK) return rc;
-  GemvTmaArgs a;
+  if (nmat < 1 || nmat > kMaxMats) return TB_ERR_SHAPE;
+  if (K > (1 << 22) || K % kBlock) return TB_ERR_SHAPE;
+  GemvTmaArgs a = {};
+  CodeMaps maps;
+  int tiles = 0;
+  for (int i = 0; i < nmat; ++i) {
+    if (N[i] < 1 || N[i] > (1LL << 30)) return TB_ERR_SHAPE;
+    rc = code_map(w[i], N[i], K, &maps.m[i]);
+    if (rc != TB_OK) return rc;
+    a.scales[i] = scales[i];
+    a.biases[i] = biases[i];
+    a.y[i] = y[i];
+    a.N[i] = (int)N[i];
+    a.tile0[i] = tiles;
+    tiles += (int)((N[i] + kUnitRows - 1) / kUnitRows);
+  }
+  for (int i = nmat; i <= kMaxMats; ++i) a.tile0[i] = tiles;
+  for (int i = nmat; i < kMaxMats; ++i) maps.m[i] = maps.m[0];
+  a.nmat = nmat;
   a.x = x;
   a.signs = signs;
-  a.scales = scales;
-  a.biases = biases;
-  a.y = y;
   const bool split = workspace && ws_bytes >= gemv_fixup_bytes() && f.sms <= kFixupCtas;
   a.ws_partial = split ? static_cast<float*>(workspace) : nullptr;
   a.ws_count = split ? reinterpret_cast<int*>(static_cast<char*>(workspace) + kFixupPartialBytes)
                      : nullptr;
   a.split = split ? 1 : 0;
-  a.Mc = 0;
   a.K = (int)K;
-  a.N = (int)N;
   a.G = (int)(K / kGroup);
   a.C = (int)(K / (kUnitGroups * kGroup));
   a.rotate = block != 0;
-  a.dw = a.tslots = 0;
-  a.n_tiles = (int)((N + kUnitRows - 1) / kUnitRows);
+  a.n_tiles = tiles;
   a.status = status;
   const int mt = tma_tokens_per_pass(M, a.G, a.C, f.smem_optin);
   switch (mt) {
-    case 8: return launch_tma_mt<8>(a, m, M, K, N, f, s);
-    case 4: return launch_tma_mt<4>(a, m, M, K, N, f, s);
-    case 2: return launch_tma_mt<2>(a, m, M, K, N, f, s);
-    default: return launch_tma_mt<1>(a, m, M, K, N, f, s);
+    case 8: return launch_tma_mt<8>(a, maps, M, K, f, s);
+    case 4: return launch_tma_mt<4>(a, maps, M, K, f, s);
+    case 2: return launch_tma_mt<2>(a, maps, M, K, f, s);
+    default: return launch_tma_mt<1>(a, maps, M, K, f, s);
   }
+}
+
+int launch_gemv_tma(const __half* x, int64_t M, int64_t K, const int8_t* signs, int block,
+                    const uint32_t* w, const __half* scales, const __half* biases, int64_t N,
+                    __half* y, void* workspace, size_t ws_bytes, int32_t* status, cudaStream_t s) {
+  return launch_gemv_tma_multi(x, M, K, signs, block, 1, &w, &scales, &biases, &N, &y, workspace,
+                               ws_bytes, status, s);
 }
 
 }  // namespace tb

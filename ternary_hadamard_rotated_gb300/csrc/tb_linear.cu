@@ -23,6 +23,16 @@ int launch_gemv_tma(const __half* x, int64_t M, int64_t K, const int8_t* signs, 
                     const uint32_t* w, const __half* scales, const __half* biases, int64_t N,
                     __half* y, void* workspace, size_t ws_bytes, int32_t* status, cudaStream_t s);
 size_t gemv_fixup_bytes();
+int launch_gemv_tma_multi(const __half* x, int64_t M, int64_t K, const int8_t* signs, int block,
+                          int nmat, const uint32_t* const* w, const __half* const* scales,
+                          const __half* const* biases, const int64_t* N, __half* const* y,
+                          void* workspace, size_t ws_bytes, int32_t* status, cudaStream_t s);
+int launch_rotate_pairorder(const __half* x, __half* out, const int8_t* signs, int64_t M,
+                            int64_t K, int rotate, cudaStream_t s);
+int launch_gemm_tc_rotated(const __half* xp, int64_t M, int64_t K, const uint32_t* w,
+                           const __half* scales, const __half* biases, int64_t N, __half* y,
+                           int32_t* status, cudaStream_t s);
+constexpr int kMaxMulti = 4;
 
 // Workspace layout: [fixup region of the GEMV split schedule (zero before the first call,
 // left zero by every completed call)][x' of the tensor-core path], 1 KB aligned.
@@ -94,4 +104,44 @@ extern "C" int tb_packed_linear(const uint16_t* x, int64_t M, int64_t K, const i
                                 size_t workspace_bytes, int32_t* dev_status, void* stream) {
   return tb_packed_linear_algo(x, M, K, signs, block, w, scales, biases, N, y, workspace,
                                workspace_bytes, dev_status, TB_ALGO_AUTO, stream);
+}
+
+extern "C" int tb_packed_linear_multi(const uint16_t* x, int64_t M, int64_t K, const int8_t* signs,
+                                      int block, int n, const uint32_t* const* w,
+                                      const uint16_t* const* scales, const uint16_t* const* biases,
+                                      const int64_t* N, uint16_t* const* y, void* workspace,
+                                      size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  using namespace tb;
+  if (!x || !w || !scales || !biases || !N || !y) return TB_ERR_NULL;
+  if (n < 1 || n > kMaxMulti) return TB_ERR_SHAPE;
+  if (block != 0 && block != kBlock) return TB_ERR_UNSUPPORTED;
+  if (M < 1 || K < kBlock || K % kBlock) return TB_ERR_SHAPE;
+  if (!aligned16(x) || (signs && !aligned16(signs)) || (workspace && !aligned16(workspace)))
+    return TB_ERR_ALIGN;
+  const __half* sh[kMaxMulti];
+  const __half* bh[kMaxMulti];
+  __half* yh[kMaxMulti];
+  for (int i = 0; i < n; ++i) {
+    if (!w[i] || !scales[i] || !biases[i] || !y[i]) return TB_ERR_NULL;
+    if (N[i] < 1) return TB_ERR_SHAPE;
+    if (!aligned16(w[i]) || !aligned16(scales[i]) || !aligned16(biases[i]) || !aligned16(y[i]))
+      return TB_ERR_ALIGN;
+    sh[i] = reinterpret_cast<const __half*>(scales[i]);
+    bh[i] = reinterpret_cast<const __half*>(biases[i]);
+    yh[i] = reinterpret_cast<__half*>(y[i]);
+  }
+  const int8_t* sg = block ? signs : nullptr;
+  const __half* xh = reinterpret_cast<const __half*>(x);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (M <= kGemvMaxTokens)
+    return launch_gemv_tma_multi(xh, M, K, sg, block, n, w, sh, bh, N, yh, workspace, workspace_bytes,
+                                 dev_status, s);
+  // prefill: one rotation of x into the workspace, then one GEMM per matrix
+  const size_t need = fixup_region() + gemm_tc_workspace(M, K);
+  if (!workspace || workspace_bytes < need) return TB_ERR_WORKSPACE;
+  __half* xp = reinterpret_cast<__half*>(static_cast<char*>(workspace) + fixup_region());
+  int rc = launch_rotate_pairorder(xh, xp, sg, M, K, block != 0, s);
+  for (int i = 0; i < n && rc == TB_OK; ++i)
+    rc = launch_gemm_tc_rotated(xp, M, K, w[i], sh[i], bh[i], N[i], yh[i], dev_status, s);
+  return rc;
 }

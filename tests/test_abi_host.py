@@ -106,3 +106,22 @@ def test_other_entry_points_refuse_bad_arguments(lib):
     assert e(P, 4, P, P, P, 0, 1024, None, 1024, P, None, None) == -2
     assert e(P, 0, P, P, P, 100, 1024, None, 1024, P, None, None) == 0   # T = 0: no-op
     assert e(None, 4, P, P, P, 100, 1024, None, 1024, P, None, None) == -1
+
+
+def test_multi_refuses_bad_arguments(lib):
+    import ctypes
+
+    arr = (ctypes.c_void_p * 5)(*([P] * 5))
+    ns = (ctypes.c_int64 * 5)(*([16] * 5))
+    f = lib.tb_packed_linear_multi
+    assert f(P, 1, 1024, P, 1024, 5, arr, arr, arr, ns, arr, None, 0, None, None) == -2   # n > 4
+    assert f(P, 1, 1024, P, 1024, 0, arr, arr, arr, ns, arr, None, 0, None, None) == -2   # n < 1
+    assert f(P, 1, 1536, P, 1024, 2, arr, arr, arr, ns, arr, None, 0, None, None) == -2   # K % 1024
+    assert f(P, 1, 1024, P, 512, 2, arr, arr, arr, ns, arr, None, 0, None, None) == -3
+    assert f(None, 1, 1024, P, 1024, 2, arr, arr, arr, ns, arr, None, 0, None, None) == -1
+    nul = (ctypes.c_void_p * 2)(P, None)
+    assert f(P, 1, 1024, P, 1024, 2, nul, arr, arr, ns, arr, None, 0, None, None) == -1
+    bad = (ctypes.c_int64 * 2)(16, 0)
+    assert f(P, 1, 1024, P, 1024, 2, arr, arr, arr, bad, arr, None, 0, None, None) == -2
+    # the prefill path of a multi call needs the x' workspace
+    assert f(P, 64, 1024, P, 1024, 2, arr, arr, arr, ns, arr, None, 0, None, None) == -7

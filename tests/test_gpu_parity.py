@@ -209,6 +209,26 @@ def test_linear_tiny_output_counts(tb, N):
         assert_linear_close(y, ref, bound, f"N={N} algo={algo}")
 
 
+@pytest.mark.parametrize("M", [1, 3, 200])
+@pytest.mark.parametrize("K,Ns", [(5120, (6144, 1024, 1024)), (2048, (300, 77)), (1024, (17,))])
+def test_linear_multi_shared_input(tb, M, K, Ns):
+    # several matrices reading the same x in one call (q/k/v, gate/up, qkv/z of one layer)
+    x = ti.activations(60 + M, M, K)
+    sg = ti.rademacher_signs(60, K)
+    layers = [HostLayer(61 + i, N, K) for i, N in enumerate(Ns)]
+    mats = [device_layer(61 + i, N, K, from_host=L) for i, (N, L) in enumerate(zip(Ns, layers))]
+    ys = [torch.full((M, N), float("nan"), dtype=torch.float16, device="cuda") for N in Ns]
+    ws = torch.zeros(tb.tb_packed_linear_workspace_size(M, K, max(Ns), 1024), dtype=torch.uint8,
+                     device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    tb.tb_packed_linear_multi(dev(x), dev(sg), 1024, mats, ys, ws, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    for y, L in zip(ys, layers):
+        ref, bound = linear_reference(x, sg, 1024, L)
+        assert_linear_close(y.cpu().numpy(), ref, bound, f"multi M={M} N={L.N}")
+
+
 # ---------------------------------------------------------------- tensor-core path
 @pytest.mark.parametrize("M,K,N", [(128, 1024, 256), (200, 2048, 300), (512, 1024, 520)])
 def test_linear_tc_tiles(tb, M, K, N):
