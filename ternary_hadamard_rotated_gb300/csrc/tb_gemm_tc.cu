@@ -25,13 +25,9 @@
 
 namespace tb {
 
-constexpr int kTcBM = 128, kTcBN = 256, kTcBK = 64, kTcStages = 4;
+constexpr int kTcBM = 128, kTcBN = 256, kTcBK = 64;
 constexpr int kTcThreads = 320;
 constexpr int kTcABytes = kTcBM * kTcBK * 2;  // 16 KB
-constexpr int kTcBBytes = kTcBN * kTcBK * 2;  // 32 KB
-constexpr int kTcStageBytes = kTcABytes + kTcBBytes;
-constexpr int kTcSmemBytes = kTcStages * kTcStageBytes + 1024 /*barriers*/ + 1024 /*align*/;
-constexpr int kTcTmemCols = 256;
 
 struct TcArgs {
   const uint32_t* w;     // [N, K/16]
@@ -53,8 +49,6 @@ TB_DEVI uint64_t umma_desc_sw128(uint32_t saddr) {
   return d;
 }
 
-// kind::f16 instruction descriptor: fp16 A and B, fp32 D, both K-major, M = 128, N = 256
-constexpr uint32_t kTcIdesc = (1u << 4) | ((uint32_t)(kTcBN >> 3) << 17) | ((uint32_t)(kTcBM >> 4) << 24);
 
 TB_DEVI void tma_load_2d(void* dst, const CUtensorMap* tm, int x, int y, uint64_t* bar) {
   asm volatile(
@@ -111,27 +105,44 @@ TB_DEVI void decode_word_affine(uint32_t w, __half2 s2, __half2 b2, uint32_t (&o
   }
 }
 
+// NSUB M-subtiles of 128 tokens share every decoded B tile (NSUB = 2: 256 tokens per CTA,
+// the decode cost per flop halves).  Stage s holds A[sub] (16 KB each) then B (32 KB).
+template <int NSUB, int BN>
+struct TcCfg {
+  static constexpr int kBBytes = BN * kTcBK * 2;
+  static constexpr int kStageBytes = NSUB * kTcABytes + kBBytes;
+  static constexpr int kStages = (192 * 1024) / kStageBytes;
+  static constexpr int kSmem = kStages * kStageBytes + 1024 + 1024;
+  static constexpr int kTmemCols = NSUB * BN;
+  // kind::f16 instruction descriptor: fp16 A and B, fp32 D, both K-major, M = 128, N = BN
+  static constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(kTcBM >> 4) << 24);
+  static constexpr int kThreadsPerRow = 256 / BN;  // decoder threads per B row
+};
+
+template <int NSUB, int BN>
 __global__ void __launch_bounds__(kTcThreads, 1)
     w2_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const TcArgs a) {
+  using Cfg = TcCfg<NSUB, BN>;
+  constexpr int S = Cfg::kStages;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (base - raw);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kTcStages * kTcStageBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * Cfg::kStageBytes);
   uint64_t* fullA = bars;
-  uint64_t* fullB = bars + kTcStages;
-  uint64_t* empty = bars + 2 * kTcStages;
-  uint64_t* accum = bars + 3 * kTcStages;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * kTcStages + 1);
+  uint64_t* fullB = bars + S;
+  uint64_t* empty = bars + 2 * S;
+  uint64_t* accum = bars + 3 * S;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * S + 1);
   __shared__ volatile int aborted;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n0 = blockIdx.x * kTcBN, m0 = blockIdx.y * kTcBM;
+  const int n0 = blockIdx.x * BN, m0 = blockIdx.y * (NSUB * kTcBM);
   const int nkb = a.K / kTcBK;
 
   if (threadIdx.x == 0) {
     aborted = 0;
-    for (int s = 0; s < kTcStages; ++s) {
+    for (int s = 0; s < S; ++s) {
       mbar_init(fullA + s, 1);
       mbar_init(fullB + s, 256);
       mbar_init(empty + s, 1);
@@ -142,7 +153,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(tmem_slot)),
-                 "r"(kTcTmemCols)
+                 "r"(Cfg::kTmemCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
@@ -163,53 +174,80 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (lane == 0) {
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
       for (int kb = 0; kb < nkb; ++kb) {
-        const int s = kb % kTcStages, it = kb / kTcStages;
+        const int s = kb % S, it = kb / S;
         if (it > 0) wait(empty + s, (it - 1) & 1);
-        mbar_arrive_expect_tx(fullA + s, kTcABytes);
-        tma_load_2d(smem + s * kTcStageBytes, &tmA, kb * kTcBK, m0, fullA + s);
+        mbar_arrive_expect_tx(fullA + s, NSUB * kTcABytes);
+#pragma unroll
+        for (int sub = 0; sub < NSUB; ++sub)
+          tma_load_2d(smem + s * Cfg::kStageBytes + sub * kTcABytes, &tmA, kb * kTcBK,
+                      m0 + sub * kTcBM, fullA + s);
       }
     }
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) {
       for (int kb = 0; kb < nkb; ++kb) {
-        const int s = kb % kTcStages, it = kb / kTcStages;
+        const int s = kb % S, it = kb / S;
         wait(fullA + s, it & 1);
         wait(fullB + s, it & 1);
         tc_fence_after();
-        const uint32_t sa = smem_u32(smem + s * kTcStageBytes);
-        const uint64_t ad = umma_desc_sw128(sa), bd = umma_desc_sw128(sa + kTcABytes);
+        const uint32_t sa = smem_u32(smem + s * Cfg::kStageBytes);
+        const uint64_t bd = umma_desc_sw128(sa + NSUB * kTcABytes);
 #pragma unroll
         for (int k = 0; k < kTcBK / 16; ++k)
-          tc_mma(tmem_d, ad + 2 * k, bd + 2 * k, kTcIdesc, (kb | k) != 0);
+#pragma unroll
+          for (int sub = 0; sub < NSUB; ++sub)
+            tc_mma(tmem_d + sub * BN, umma_desc_sw128(sa + sub * kTcABytes) + 2 * k, bd + 2 * k,
+                   Cfg::kIdesc, (kb | k) != 0);
         tc_commit(empty + s);
       }
       tc_commit(accum);
     }
     __syncwarp();
   } else {
-    // ---- decoders: thread d owns row n0 + d of the B tile ----
-    const int d = threadIdx.x - 64;
+    // ---- decoders: thread d owns (part of) row n0 + d % BN of the B tile ----
+    constexpr int WPT = 4 / Cfg::kThreadsPerRow;  // packed words per thread per k-block
+    const int d = (threadIdx.x - 64) % BN;
+    const int wq = ((threadIdx.x - 64) / BN) * WPT;  // first word of this thread
     const int row = n0 + d;
     const bool valid = row < a.N;
     const uint4* wrow = reinterpret_cast<const uint4*>(a.w + (int64_t)(valid ? row : 0) * (a.K / 16));
     const __half* srow = a.scales + (int64_t)(valid ? row : 0) * a.G;
     const __half* brow = a.biases + (int64_t)(valid ? row : 0) * a.G;
-    uint4 cur = valid ? __ldg(wrow) : make_uint4(0, 0, 0, 0);
+    const uint32_t* wrow32 = reinterpret_cast<const uint32_t*>(wrow) + wq;
+    auto load_words = [&](int kb, uint32_t (&wv)[WPT]) {
+      if constexpr (WPT == 4) {
+        const uint4 u = __ldg(wrow + kb);
+        wv[0] = u.x;
+        wv[1] = u.y;
+        wv[2] = u.z;
+        wv[3] = u.w;
+      } else {
+        const uint2 u = __ldg(reinterpret_cast<const uint2*>(wrow32 + kb * 4));
+        wv[0] = u.x; wv[1] = u.y;
+      }
+    };
+    uint32_t cur[WPT];
+    if (valid) load_words(0, cur);
+    else
+#pragma unroll
+      for (int j = 0; j < WPT; ++j) cur[j] = 0;
     for (int kb = 0; kb < nkb; ++kb) {
-      const int s = kb % kTcStages, it = kb / kTcStages;
-      uint4 nxt = make_uint4(0, 0, 0, 0);
-      if (valid && kb + 1 < nkb) nxt = __ldg(wrow + kb + 1);
+      const int s = kb % S, it = kb / S;
+      uint32_t nxt[WPT];
+#pragma unroll
+      for (int j = 0; j < WPT; ++j) nxt[j] = 0;
+      if (valid && kb + 1 < nkb) load_words(kb + 1, nxt);
       const __half sv = srow[kb >> 1], bv = brow[kb >> 1];
       if (it > 0) wait(empty + s, (it - 1) & 1);
-      const uint32_t bt = smem_u32(smem + s * kTcStageBytes + kTcABytes) + d * 128;
+      const uint32_t bt = smem_u32(smem + s * Cfg::kStageBytes + NSUB * kTcABytes) + d * 128;
       const uint32_t sw = d & 7;
-      const uint32_t words[4] = {cur.x, cur.y, cur.z, cur.w};
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
+      for (int jj = 0; jj < WPT; ++jj) {
+        const int j = wq + jj;  // word of the row's 64-k slice: 16-byte chunks 2j, 2j+1
         uint32_t o[8];
         if (valid) {
-          decode_word_affine(words[j], __half2half2(sv), __half2half2(bv), o);
+          decode_word_affine(cur[jj], __half2half2(sv), __half2half2(bv), o);
         } else {
 #pragma unroll
           for (int p = 0; p < 8; ++p) o[p] = 0;
@@ -219,20 +257,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       fence_proxy_async_smem();
       mbar_arrive(fullB + s);
-      cur = nxt;
+#pragma unroll
+      for (int j = 0; j < WPT; ++j) cur[j] = nxt[j];
     }
     // ---- epilogue: TMEM -> fp16 y ----
     wait(accum, 0);
     tc_fence_after();
-    const int q = warp & 3;                // TMEM lane quarter this warp may read
-    const int colbase = ((warp - 2) >> 2) * (kTcBN / 2);
-    const int tok = m0 + q * 32 + lane;
+    const int q = warp & 3;                 // TMEM lane quarter this warp may read
+    const int part = (warp - 2) >> 2;       // which half of the columns / which subtile
+    const int sub = NSUB == 2 ? part : 0;
+    const int c0 = NSUB == 2 ? 0 : part * (BN / 2);
+    const int tok = m0 + sub * kTcBM + q * 32 + lane;
     const bool vec = (a.N % 8) == 0;
 #pragma unroll 1
-    for (int c = 0; c < kTcBN / 2; c += 32) {
+    for (int c = 0; c < (NSUB == 2 ? BN : BN / 2); c += 32) {
       uint32_t r[32];
-      tc_ld32(tmem_d + ((uint32_t)(q * 32) << 16) + (uint32_t)(colbase + c), r);
-      const int n = n0 + colbase + c;
+      tc_ld32(tmem_d + ((uint32_t)(q * 32) << 16) + (uint32_t)(sub * BN + c0 + c), r);
+      const int n = n0 + c0 + c;
       if (tok < a.M && n < a.N) {
         __half* dst = a.y + (int64_t)tok * a.N + n;
         if (vec && n + 32 <= a.N) {
@@ -245,7 +286,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             *reinterpret_cast<uint4*>(dst + 8 * v) = make_uint4(h[0], h[1], h[2], h[3]);
           }
         } else {
-          for (int e = 0; e < 32 && n + e < a.N; ++e) dst[e] = __float2half_rn(__uint_as_float(r[e]));
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (n + e < a.N) dst[e] = __float2half_rn(__uint_as_float(r[e]));
         }
       }
     }
@@ -256,7 +299,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (warp == 1) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_d),
-                 "r"(kTcTmemCols)
+                 "r"(Cfg::kTmemCols)
                  : "memory");
   }
 }
@@ -302,12 +345,21 @@ int launch_gemm_tc_rotated(const __half* xp, int64_t M, int64_t K, const uint32_
                                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (cr != CUDA_SUCCESS) return TB_ERR_CUDA;
 
-  cudaError_t e = cudaFuncSetAttribute(w2_gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       kTcSmemBytes);
-  if (e != cudaSuccess) {
-    record_cuda_error(e);
-    return TB_ERR_CUDA;
-  }
+  // Tile choice: two 128-token subtiles per CTA halve the decode work per flop; 256-row
+  // weight tiles halve the activation reads per flop; both only while the grid still fills
+  // the SMs (about one CTA each).
+  DeviceFacts f;
+  int rcf = device_facts(&f);
+  if (rcf != TB_OK) return rcf;
+  auto ctas = [&](int nsub, int bn) { return ((N + bn - 1) / bn) * ((M + nsub * kTcBM - 1) / (nsub * kTcBM)); };
+  const int64_t full = (int64_t)f.sms * 4 / 5;
+  const int64_t sms = f.sms;
+  auto ok128 = [&](int64_t c) { return c >= full && (c <= sms || c >= 3 * sms); };  // no near-empty last wave
+  int nsub = 1, bn = 256;
+  if (M > kTcBM && ctas(2, 256) >= full) { nsub = 2; bn = 256; }
+  else if (M > kTcBM && ok128(ctas(2, 128))) { nsub = 2; bn = 128; }
+  else if (ctas(1, 256) >= full) { nsub = 1; bn = 256; }
+  else if (ctas(1, 128) <= sms) { nsub = 1; bn = 128; }
   TcArgs a;
   a.w = w;
   a.scales = scales;
@@ -318,8 +370,25 @@ int launch_gemm_tc_rotated(const __half* xp, int64_t M, int64_t K, const uint32_
   a.K = (int)K;
   a.G = (int)(K / kGroup);
   a.status = status;
-  dim3 grid((unsigned)((N + kTcBN - 1) / kTcBN), (unsigned)((M + kTcBM - 1) / kTcBM));
-  w2_gemm_tc_kernel<<<grid, kTcThreads, kTcSmemBytes, s>>>(tm, a);
+  cudaError_t e = cudaSuccess;
+  const unsigned gm = (unsigned)((M + nsub * kTcBM - 1) / (nsub * kTcBM));
+  const unsigned gn = (unsigned)((N + bn - 1) / bn);
+#define TB_LAUNCH_TC(NS, B)                                                                        \
+  do {                                                                                            \
+    e = cudaFuncSetAttribute(w2_gemm_tc_kernel<NS, B>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                             TcCfg<NS, B>::kSmem);                                                 \
+    if (e == cudaSuccess)                                                                         \
+      w2_gemm_tc_kernel<NS, B><<<dim3(gn, gm), kTcThreads, TcCfg<NS, B>::kSmem, s>>>(tm, a);       \
+  } while (0)
+  if (nsub == 2 && bn == 256) TB_LAUNCH_TC(2, 256);
+  else if (nsub == 2) TB_LAUNCH_TC(2, 128);
+  else if (bn == 256) TB_LAUNCH_TC(1, 256);
+  else TB_LAUNCH_TC(1, 128);
+#undef TB_LAUNCH_TC
+  if (e != cudaSuccess) {
+    record_cuda_error(e);
+    return TB_ERR_CUDA;
+  }
   return check_launch();
 }
 

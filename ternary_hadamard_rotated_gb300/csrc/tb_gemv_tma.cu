@@ -100,14 +100,15 @@ __host__ __device__ inline GemvTmaLayout gemv_tma_layout(int G, int dw, int tslo
   L.cs = off;
   off += G * MT * 8;
   off = rup(off, 16);
+  // the FWHT scratch is only used by the prologue; the scale staging and the tile
+  // accumulators only after it: they share one region
   L.scratch = off;
-  off += kTmaFwhtWarps * kWarpScratchFloats * 4;
+  const int fw = kTmaFwhtWarps * kWarpScratchFloats * 4;
   L.sstage = off;
-  off += kTmaConsumers * kScaleStageBytes;
-  L.accs = off;
-  off += (tslots + 1) * kUnitRows * MT * 4;
-  L.cnt = off;
-  off += (tslots + 1) * 4;
+  L.accs = L.sstage + kTmaConsumers * kScaleStageBytes;
+  L.cnt = L.accs + (tslots + 1) * kUnitRows * MT * 4;
+  const int after = L.cnt + (tslots + 1) * 4;
+  off = off + fw > after ? off + fw : after;
   off = rup(off, 8);
   L.bars = off;
   off += 2 * kGroupsOfWarps * dw * 8;
@@ -272,8 +273,6 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     }
     fence_barrier_init();
   }
-  for (int i = threadIdx.x; i < (TS + 1) * kUnitRows * MT; i += blockDim.x) accs[i] = 0.f;
-  for (int i = threadIdx.x; i <= TS; i += blockDim.x) cnt[i] = 0;
   __syncthreads();
 
   auto wait = [&](uint64_t* bar, uint32_t parity) {
@@ -397,6 +396,10 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         if (t == 0) cs[grp * MT + tok] = make_float2(1024.f * csum, ssum);
       }
     }
+    asm volatile("bar.sync 1, %0;" ::"n"(kTmaConsumers * 32) : "memory");
+    // the FWHT scratch becomes the tile accumulators (zeroed) and the scale staging
+    for (int i = threadIdx.x; i < (TS + 1) * kUnitRows * MT; i += kTmaConsumers * 32) accs[i] = 0.f;
+    for (int i = threadIdx.x; i <= TS; i += kTmaConsumers * 32) cnt[i] = 0;
     asm volatile("bar.sync 1, %0;" ::"n"(kTmaConsumers * 32) : "memory");
   }
 
