@@ -380,6 +380,21 @@ def run_sweep(args, dist, tb, tdev, torch):
     return line
 
 
+def profile_step(args, dist, tb, tdev, torch):
+    """One eager decode step (embedding + 257 calls) after a warm-up step, nothing timed."""
+    layers, emb, xs, signs, ys = build_sweep(tb, tdev, torch)
+    groups = launch_groups(layers)
+    dev = torch.device("cuda")
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    ids = torch.tensor([7], dtype=torch.int32, device=dev)
+    e_out = torch.empty((1, ti.HIDDEN), dtype=torch.float16, device=dev)
+    ws = torch.zeros(tb.tb_packed_linear_workspace_size(1, ti.MLP, ti.HIDDEN), dtype=torch.uint8, device=dev)
+    for _ in range(2):
+        sweep_step(tb, groups, emb, xs, signs, ys, ids, e_out, ws, status)
+    torch.cuda.synchronize()
+    return {"profile_step": "done", "calls_per_step": 1 + len(groups), "status": int(status.item())}
+
+
 def run_layers(args, dist, tb, tdev, torch):
     """Per-shape decode GEMV at the 27B layer shapes (M = 1)."""
     hbm, _, _, peak_kind = peaks()
@@ -566,6 +581,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="sweep", choices=["sweep", "layers", "prefill", "batched", "embed", "all"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-step", action="store_true",
+                    help="build the decode sweep, run one eager step and exit (for an ncu launch list)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -586,9 +603,11 @@ def main():
 
     tb.load()
     configs = ["sweep", "layers", "prefill", "batched", "embed"] if args.config == "all" else [args.config]
+    if args.profile_step:
+        configs = ["profile"]
     for c in configs:
         fn = {"sweep": run_sweep, "layers": run_layers, "prefill": run_prefill, "batched": run_batched,
-              "embed": run_embed}[c]
+              "embed": run_embed, "profile": profile_step}[c]
         line = fn(args, dist, tb, tdev, torch)
         if rank == 0:
             print(json.dumps(line), flush=True)

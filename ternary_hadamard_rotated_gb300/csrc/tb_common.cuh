@@ -224,4 +224,20 @@ TB_DEVI void wht1024_a_to_b(float (&v)[32], float* scratch, int lane) {
 
 constexpr int kWarpScratchFloats = 32 * 33;
 
+// Unnormalised Walsh-Hadamard transform of a 1024-block in layout A without shared memory:
+// five butterfly stages over the register index (element bits 0..4), then five over the
+// lane index (element bits 5..9) with xor-shuffles; the result stays in layout A.
+TB_DEVI void wht1024_a_shfl(float (&v)[32], int lane) {
+  butterfly32(v);
+#pragma unroll
+  for (int h = 1; h < 32; h <<= 1) {
+    const float sg = (lane & h) ? -1.0f : 1.0f;  // upper partner keeps a - b
+#pragma unroll
+    for (int r = 0; r < 32; ++r) {
+      const float p = __shfl_xor_sync(0xffffffffu, v[r], h);
+      v[r] = fmaf(sg, v[r], p);
+    }
+  }
+}
+
 }  // namespace tb

@@ -25,7 +25,7 @@
 
 namespace tb {
 
-constexpr int kTcBM = 128, kTcBN = 256, kTcBK = 64;
+constexpr int kTcBM = 128, kTcBK = 64;  // token subtile, k per stage
 constexpr int kTcThreads = 320;
 constexpr int kTcABytes = kTcBM * kTcBK * 2;  // 16 KB
 

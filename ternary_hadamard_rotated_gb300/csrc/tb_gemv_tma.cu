@@ -46,8 +46,8 @@ constexpr int kGroupsOfWarps = 3;                    // unit groups
 constexpr int kWarpsPerUnit = 4;                     // 32 rows each
 constexpr int kTmaConsumers = kGroupsOfWarps * kWarpsPerUnit;
 constexpr int kTmaThreads = (kTmaConsumers + 1) * 32;
-constexpr int kTmaFwhtWarps = 8;
-constexpr int kMaxSlotsPerGroup = 4;
+constexpr int kTmaFwhtWarps = kTmaConsumers;  // every consumer warp transforms blocks
+constexpr int kMaxSlotsPerGroup = 5;
 constexpr int kScaleStageBytes = 32 * kUnitGroups * 8;  // per warp: 32 rows x 4 groups of fp32 (s, b)
 constexpr uint32_t kMagic1024 = 0x64006400u;
 
@@ -100,10 +100,9 @@ __host__ __device__ inline GemvTmaLayout gemv_tma_layout(int G, int dw, int tslo
   L.cs = off;
   off += G * MT * 8;
   off = rup(off, 16);
-  // the FWHT scratch is only used by the prologue; the scale staging and the tile
-  // accumulators only after it: they share one region
+  // scale staging and tile accumulators (the prologue needs no scratch)
   L.scratch = off;
-  const int fw = kTmaFwhtWarps * kWarpScratchFloats * 4;
+  const int fw = 0;
   L.sstage = off;
   L.accs = L.sstage + kTmaConsumers * kScaleStageBytes;
   L.cnt = L.accs + (tslots + 1) * kUnitRows * MT * 4;
@@ -228,7 +227,6 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
   const uint32_t codes_u32 = smem_u32(smem + L.codes);
   __half* img = reinterpret_cast<__half*>(smem + L.img);
   float2* cs = reinterpret_cast<float2*>(smem + L.cs);    // [G][MT] = (1024 sum x'/sigma, sum x')
-  float* scratch = reinterpret_cast<float*>(smem + L.scratch);
   float* accs = reinterpret_cast<float*>(smem + L.accs);  // [TS][128][MT]
   int* cnt = reinterpret_cast<int*>(smem + L.cnt);         // [TS]
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
@@ -332,72 +330,86 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
 
   asm volatile("griddepcontrol.wait;" ::: "memory");
   {
-    // prologue: x' = fwht(signs * x) -> B-fragment image, (C, S) per group and token
+    // prologue: x' = fwht(signs * x) -> B-fragment image, (C, S) per group and token.
+    // Every consumer warp takes blocks (token, 1024-slice) warp, warp + 12, ...; the loads of
+    // two blocks are issued before either is transformed, so a warp waits once per pair.
     const int nchunk = K / kBlock;
-    if (warp < kTmaFwhtWarps) {
-      float* sw = scratch + warp * kWarpScratchFloats;
-      for (int it = warp; it < MT * nchunk; it += kTmaFwhtWarps) {
-        const int tok = it / nchunk, b = it - tok * nchunk;
-        // layout A: v[r] = element b*1024 + lane*32 + r (four 16-byte loads of x, two of signs)
-        float v[32];
-        if (tok < a.Mc) {
-          const uint4* xs = reinterpret_cast<const uint4*>(a.x + (int64_t)tok * K + b * kBlock + lane * 32);
+    auto load_block = [&](int it, uint4 (&xr)[4], uint4 (&sr)[2]) {
+      const int tok = it / nchunk, b = it - tok * nchunk;
+      if (tok < a.Mc) {
+        const uint4* xs = reinterpret_cast<const uint4*>(a.x + (int64_t)tok * K + b * kBlock + lane * 32);
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            const uint4 u = __ldg(xs + q4);
-            const __half* h = reinterpret_cast<const __half*>(&u);
+        for (int q4 = 0; q4 < 4; ++q4) xr[q4] = __ldg(xs + q4);
+      } else {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) v[8 * q4 + e] = __half2float(h[e]);
-          }
-          if (a.signs) {
-            const uint4* sp = reinterpret_cast<const uint4*>(a.signs + b * kBlock + lane * 32);
-            const uint4 s01[2] = {__ldg(sp), __ldg(sp + 1)};
-            const int8_t* sg = reinterpret_cast<const int8_t*>(s01);
-#pragma unroll
-            for (int r = 0; r < 32; ++r)
-              if (sg[r] < 0) v[r] = -v[r];
-          }
-        } else {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = 0.f;
-        }
-        if (a.rotate) {
-          wht1024_a_to_b(v, sw, lane);   // bits 0..4 and 5..9 of the element index
-          transpose_b_to_a(v, sw, lane);  // back to layout A for the image
-#pragma unroll
-          for (int r = 0; r < 32; ++r) v[r] *= kInvSqrtBlock;
-        }
-        const int grp = b * (kBlock / kGroup) + (lane >> 2);
-        float ssum = 0.f, csum = 0.f;
-#pragma unroll
-        for (int r = 0; r < 32; ++r) {
-          v[r] = __half2float(__float2half_rn(v[r]));  // x' rounded to fp16
-          ssum += v[r];
-        }
-#pragma unroll
-        for (int mp = 0; mp < 4; ++mp) {
-          uint32_t pk[4];
-#pragma unroll
-          for (int e2 = 0; e2 < 4; ++e2) {
-            const int p = 4 * (mp & 1) + e2;
-            const int r = (mp >> 1) * 16 + p;
-            const float is = inv_sigma_p(p);
-            const __half lo_ = __float2half_rn(v[r] * is), hi_ = __float2half_rn(v[r + 8] * is);
-            csum += __half2float(lo_) + __half2float(hi_);
-            pk[e2] = (uint32_t)__half_as_ushort(lo_) | ((uint32_t)__half_as_ushort(hi_) << 16);
-          }
-          *reinterpret_cast<uint4*>(img + ((size_t)(grp * 4 + mp) * MT + tok) * 32 + t * 8) =
-              make_uint4(pk[0], pk[1], pk[2], pk[3]);
-        }
-        ssum += __shfl_xor_sync(0xffffffffu, ssum, 1);
-        ssum += __shfl_xor_sync(0xffffffffu, ssum, 2);
-        csum += __shfl_xor_sync(0xffffffffu, csum, 1);
-        csum += __shfl_xor_sync(0xffffffffu, csum, 2);
-        if (t == 0) cs[grp * MT + tok] = make_float2(1024.f * csum, ssum);
+        for (int q4 = 0; q4 < 4; ++q4) xr[q4] = make_uint4(0, 0, 0, 0);
       }
+      if (a.signs) {
+        const uint4* sp = reinterpret_cast<const uint4*>(a.signs + b * kBlock + lane * 32);
+        sr[0] = __ldg(sp);
+        sr[1] = __ldg(sp + 1);
+      }
+    };
+    auto transform_block = [&](int it, const uint4 (&xr)[4], const uint4 (&sr)[2]) {
+      const int tok = it / nchunk, b = it - tok * nchunk;
+      // layout A: v[r] = element b*1024 + lane*32 + r
+      float v[32];
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        const __half* h = reinterpret_cast<const __half*>(&xr[q4]);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[8 * q4 + e] = __half2float(h[e]);
+      }
+      if (a.signs) {
+        const int8_t* sg = reinterpret_cast<const int8_t*>(sr);
+#pragma unroll
+        for (int r = 0; r < 32; ++r)
+          if (sg[r] < 0) v[r] = -v[r];
+      }
+      if (a.rotate) {
+        wht1024_a_shfl(v, lane);  // all ten stages, layout A kept
+#pragma unroll
+        for (int r = 0; r < 32; ++r) v[r] *= kInvSqrtBlock;
+      }
+      const int grp = b * (kBlock / kGroup) + (lane >> 2);
+      float ssum = 0.f, csum = 0.f;
+#pragma unroll
+      for (int r = 0; r < 32; ++r) {
+        v[r] = __half2float(__float2half_rn(v[r]));  // x' rounded to fp16
+        ssum += v[r];
+      }
+#pragma unroll
+      for (int mp = 0; mp < 4; ++mp) {
+        uint32_t pk[4];
+#pragma unroll
+        for (int e2 = 0; e2 < 4; ++e2) {
+          const int p = 4 * (mp & 1) + e2;
+          const int r = (mp >> 1) * 16 + p;
+          const float is = inv_sigma_p(p);
+          const __half lo_ = __float2half_rn(v[r] * is), hi_ = __float2half_rn(v[r + 8] * is);
+          csum += __half2float(lo_) + __half2float(hi_);
+          pk[e2] = (uint32_t)__half_as_ushort(lo_) | ((uint32_t)__half_as_ushort(hi_) << 16);
+        }
+        *reinterpret_cast<uint4*>(img + ((size_t)(grp * 4 + mp) * MT + tok) * 32 + t * 8) =
+            make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      }
+      ssum += __shfl_xor_sync(0xffffffffu, ssum, 1);
+      ssum += __shfl_xor_sync(0xffffffffu, ssum, 2);
+      csum += __shfl_xor_sync(0xffffffffu, csum, 1);
+      csum += __shfl_xor_sync(0xffffffffu, csum, 2);
+      if (t == 0) cs[grp * MT + tok] = make_float2(1024.f * csum, ssum);
+    };
+    const int items = MT * nchunk;
+    for (int it = warp; it < items; it += 2 * kTmaFwhtWarps) {
+      const int it2 = it + kTmaFwhtWarps;
+      uint4 xa[4], sa[2], xb[4], sb2[2];
+      load_block(it, xa, sa);
+      if (it2 < items) load_block(it2, xb, sb2);
+      transform_block(it, xa, sa);
+      if (it2 < items) transform_block(it2, xb, sb2);
     }
     asm volatile("bar.sync 1, %0;" ::"n"(kTmaConsumers * 32) : "memory");
-    // the FWHT scratch becomes the tile accumulators (zeroed) and the scale staging
+    // zero the tile accumulators
     for (int i = threadIdx.x; i < (TS + 1) * kUnitRows * MT; i += kTmaConsumers * 32) accs[i] = 0.f;
     for (int i = threadIdx.x; i <= TS; i += kTmaConsumers * 32) cnt[i] = 0;
     asm volatile("bar.sync 1, %0;" ::"n"(kTmaConsumers * 32) : "memory");
