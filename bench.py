@@ -29,6 +29,10 @@ import numpy as np  # noqa: E402
 import tb_inputs as ti  # noqa: E402
 
 METRIC = "decode tok/s at 27B shapes (M=1) + fused W2 GEMV HBM GB/s as % of GB300 peak"
+# DRAM bytes per launch of the decode GEMV over its algorithmic bytes, from one ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum) of the 5120 -> 17408 launch:
+# 25.22 MB read, 0 written, 25.07 MB algorithmic (profiles/w2_gemv_tma_lm_head.md)
+GEMV_TRAFFIC_RATIO = 25.22 / 25.07
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 
@@ -357,7 +361,8 @@ def run_sweep(args, dist, tb, tdev, torch):
             "peak": hbm,
             "unit": "GB/s",
             "frac": round(achieved / hbm, 4),
-            "traffic": None,
+            "traffic": round(GEMV_TRAFFIC_RATIO * gemv_bytes / len(groups)),
+            "traffic_note": "ncu DRAM bytes of the 5120->17408 launch, scaled to the step's average launch",
             "kernel": "w2_gemv_tma_kernel<1> (fused FWHT prologue + W2-g128 GEMV), its 257 launches per token averaged",
             "peak_kind": f"{peak_kind} hbm_gbs",
         },
@@ -393,6 +398,25 @@ def profile_step(args, dist, tb, tdev, torch):
         sweep_step(tb, groups, emb, xs, signs, ys, ids, e_out, ws, status)
     torch.cuda.synchronize()
     return {"profile_step": "done", "calls_per_step": 1 + len(groups), "status": int(status.item())}
+
+
+def profile_linear(args, dist, tb, tdev, torch):
+    """Four calls of one K -> N packed linear on M tokens with algorithm ALGO, nothing timed."""
+    K, N, M, algo = args.profile_linear
+    dev = torch.device("cuda")
+    tmp = torch.empty(min(N * K, 1 << 30), dtype=torch.int8, device=dev)
+    p = Packed(tb, tdev, torch, 1, N, K, tmp)
+    del tmp
+    x = torch.from_numpy(ti.activations(1, M, K)).to(dev)
+    sg = torch.from_numpy(ti.rademacher_signs(1, K)).to(dev)
+    y = torch.empty((M, N), dtype=torch.float16, device=dev)
+    ws = torch.zeros(max(16, tb.tb_packed_linear_workspace_size(M, K, N, 1024, algo)), dtype=torch.uint8,
+                     device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    for _ in range(4):
+        tb.tb_packed_linear(x, sg, 1024, p.w, p.s, p.b, y, ws, status, algo=algo)
+    torch.cuda.synchronize()
+    return {"profile_linear": [K, N, M, algo], "status": int(status.item())}
 
 
 def run_layers(args, dist, tb, tdev, torch):
@@ -543,8 +567,15 @@ def run_reference(args):
         shapes[(K, N)] = shapes.get((K, N), 0) + 1
     rows = 32
 
+    emb_codes = ti.ternary_codes(12, 0, 16, ti.HIDDEN)
+    emb_sc = ti.group_scales(12, 0, 16, ti.HIDDEN // 128)
+    emb_w = oracle.pack_w2(emb_codes)
+    emb_sg = ti.rademacher_signs(1, ti.HIDDEN)
+
     def one_step():
-        sec = 0.0
+        t0 = time.perf_counter()
+        oracle.embed_lookup(np.array([3]), emb_w, emb_sc, oracle.biases_for(emb_sc), emb_sg, 1024)
+        sec = time.perf_counter() - t0
         for (K, N), count in sorted(shapes.items()):
             x = ti.activations(7, 1, K)
             sg = ti.rademacher_signs(7, K)
@@ -565,8 +596,9 @@ def run_reference(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sec * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
-            "config": {"workload": "decode step, M=1: 401 W2-g128 linears of the 64-layer 27B stack "
-                                   "(float64 CPU oracle, extrapolated from sampled rows)"},
+            "config": {"workload": "decode step, M=1: embedding of 1 id + 401 W2-g128 linears of the "
+                                   "64-layer 27B stack (float64 CPU oracle, linears extrapolated from "
+                                   "sampled rows)"},
             "cpu_baseline": {"value": round(v, 6), "unit": "tok/s", "cores": len(os.sched_getaffinity(0)),
                              "kind": "oracle",
                              "sample": f"{rows} rows of each distinct shape per step, extrapolated"},
@@ -583,6 +615,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-step", action="store_true",
                     help="build the decode sweep, run one eager step and exit (for an ncu launch list)")
+    ap.add_argument("--profile-linear", type=int, nargs=4, metavar=("K", "N", "M", "ALGO"),
+                    help="one packed K->N matrix, four tb_packed_linear calls on M tokens (for ncu)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -605,9 +639,11 @@ def main():
     configs = ["sweep", "layers", "prefill", "batched", "embed"] if args.config == "all" else [args.config]
     if args.profile_step:
         configs = ["profile"]
+    if args.profile_linear:
+        configs = ["profile_linear"]
     for c in configs:
         fn = {"sweep": run_sweep, "layers": run_layers, "prefill": run_prefill, "batched": run_batched,
-              "embed": run_embed, "profile": profile_step}[c]
+              "embed": run_embed, "profile": profile_step, "profile_linear": profile_linear}[c]
         line = fn(args, dist, tb, tdev, torch)
         if rank == 0:
             print(json.dumps(line), flush=True)
