@@ -9,18 +9,21 @@
 // Work unit: 128 output rows x 512 k (4 groups of 128) = one 16 KB TMA box of packed codes
 // (128 rows x 128 B, 128-byte swizzle; rows past N are zero-filled).  Each SM can keep only
 // a handful of TMA requests in flight, so requests are made large: 16 KB boxes stream at
-// the HBM rate where 2-4 KB requests stall at a fraction of it.  Scales and biases (8 B
-// per row per unit) are read by the consumer warps themselves, two units ahead, and staged
+// the HBM rate where 2-4 KB requests stall at a fraction of it.  Scales and biases (8 B per
+// row per unit) are read by the consumer warps themselves, two units ahead, and staged
 // through shared memory.
 //
 // Schedule (stream-K): the units of all 128-row tiles, tile-major, are cut into one
-// contiguous, equal range per CTA (one persistent CTA per SM).  A producer warp keeps a
-// ring of 16 KB slots in flight; 12 consumer warps form 3 unit groups of 4 warps; group u
-// takes the CTA's units u, u + 3, ... and warp i of the group the rows 32i..32i+31 of the
-// unit.  Every warp adds its 32-row partial sums into a per-tile shared accumulator; the
-// warp that completes a tile's count in this CTA writes y, or, when the tile continues in a
-// neighbouring CTA, adds the CTA's partial into the tile's fp32 sum in the workspace, and
-// the last of the tile's CTAs converts that sum to y and returns sum and counter to zero.
+// contiguous, equal range per CTA (one persistent CTA per SM), and each CTA's range into
+// three contiguous sub-ranges, one per unit group of 4 consumer warps (warp i of a group owns
+// rows 32i..32i+31 of every unit).  The first two groups walk their sub-range forwards, the
+// last one backwards, so a tile shared with a neighbouring CTA is finished first.  A group
+// keeps its partial sums in registers while it stays in one tile; a tile that lies wholly in
+// the group's sub-range is written straight from registers; a tile cut by a group boundary is
+// summed in shared memory, and one cut by a CTA boundary is summed in an fp32 workspace slot
+// whose last contributor converts it to y and returns slot and counter to zero.  A producer
+// warp keeps a ring of slots in flight; before the activations are loaded it issues only one
+// unit per group, so the loads of x are not queued behind megabytes of weight traffic.
 //
 // Arithmetic (per group of 128, per token): LOP3 puts each 2-bit code into the mantissa of
 // an fp16 1024.0 (1024 + sigma*q, exact; sigma = 4^j from the field's bit position j);
@@ -40,14 +43,15 @@
 namespace tb {
 
 constexpr int kUnitRows = 128;
-constexpr int kUnitGroups = 4;                       // groups per unit (512 k)
-constexpr int kBoxBytes = kUnitRows * 128;           // 16 KB
-constexpr int kGroupsOfWarps = 3;                    // unit groups
-constexpr int kWarpsPerUnit = 4;                     // 32 rows each
+constexpr int kUnitGroups = 4;                          // groups per unit (512 k)
+constexpr int kSlotBytes = kUnitRows * 128;             // 16 KB box of packed codes
+constexpr int kGroupsOfWarps = 3;                       // unit groups
+constexpr int kWarpsPerUnit = 4;                        // 32 rows each
 constexpr int kTmaConsumers = kGroupsOfWarps * kWarpsPerUnit;
 constexpr int kTmaThreads = (kTmaConsumers + 1) * 32;
-constexpr int kTmaFwhtWarps = kTmaConsumers;  // every consumer warp transforms blocks
-constexpr int kMaxSlotsPerGroup = 5;
+constexpr int kMaxSlotsPerGroup = 4;
+constexpr int kPreIssue = 1;        // units per group issued before the activations are loaded
+constexpr int kCutSlots = 4;        // shared sums of tiles cut by a group or CTA boundary
 constexpr int kScaleStageBytes = 32 * kUnitGroups * 8;  // per warp: 32 rows x 4 groups of fp32 (s, b)
 constexpr uint32_t kMagic1024 = 0x64006400u;
 
@@ -65,14 +69,14 @@ struct GemvTmaArgs {
   float* ws_partial;             // [kFixupCtas][128][MT] fp32 sums of shared tiles, or null (tile-aligned)
   int* ws_count;                 // [kFixupCtas]
   int Mc, K, G, C;               // C = units per tile = K / 512
-  int rotate, dw, tslots;
+  int rotate, dw;
   int n_tiles;                   // total 128-row tiles of all matrices
   int split;                     // 1: stream-K ranges; 0: ranges on tile boundaries
   int32_t* status;
 };
 
 struct CodeMaps {
-  CUtensorMap m[kMaxMats];
+  CUtensorMap codes[kMaxMats];   // uint32 [N][K/16], box 32 x 128, 128-byte swizzle
 };
 
 // matrix of a global tile index
@@ -84,33 +88,32 @@ TB_DEVI int mat_of(const GemvTmaArgs& a, int tile) {
 }
 
 struct GemvTmaLayout {
-  int codes, img, cs, scratch, sstage, accs, cnt, bars, total;
+  int codes, img, cs, sstage, accs, cnt, bars, total;
 };
 
 __host__ __device__ inline int rup(int v, int a) { return (v + a - 1) / a * a; }
 
+
 template <int MT>
-__host__ __device__ inline GemvTmaLayout gemv_tma_layout(int G, int dw, int tslots) {
+__host__ __device__ inline GemvTmaLayout gemv_tma_layout(int G, int dw) {
   GemvTmaLayout L;
   int off = 0;
-  L.codes = off;  // 1024-aligned boxes (the 128-byte swizzle repeats every 1024 bytes)
-  off += kGroupsOfWarps * dw * kBoxBytes;
+  L.codes = off;  // 1024-aligned slots (the 128-byte swizzle repeats every 1024 bytes)
+  off += kGroupsOfWarps * dw * kSlotBytes;
   L.img = off;
   off += G * 256 * MT;
   L.cs = off;
   off += G * MT * 8;
   off = rup(off, 16);
-  // scale staging and tile accumulators (the prologue needs no scratch)
-  L.scratch = off;
-  const int fw = 0;
   L.sstage = off;
-  L.accs = L.sstage + kTmaConsumers * kScaleStageBytes;
-  L.cnt = L.accs + (tslots + 1) * kUnitRows * MT * 4;
-  const int after = L.cnt + (tslots + 1) * 4;
-  off = off + fw > after ? off + fw : after;
+  off += kTmaConsumers * kScaleStageBytes;
+  L.accs = off;
+  off += kCutSlots * kUnitRows * MT * 4;
+  L.cnt = off;
+  off += kCutSlots * 4;
   off = rup(off, 8);
   L.bars = off;
-  off += 2 * kGroupsOfWarps * dw * 8;
+  off += (2 * kGroupsOfWarps * dw + 1) * 8;
   L.total = off + 1024;  // slack to align the base to 1024
   return L;
 }
@@ -213,6 +216,19 @@ TB_DEVI void unit_group(uint32_t box, int R0, int t, int gi, int grp, uint32_t i
   }
 }
 
+// the unit after (or before) (tile, chunk) in tile-major order
+TB_DEVI void step_unit(int& tile, int& chunk, int C, bool back) {
+  if (back) {
+    if (--chunk < 0) {
+      chunk = C - 1;
+      --tile;
+    }
+  } else if (++chunk == C) {
+    chunk = 0;
+    ++tile;
+  }
+}
+
 template <int MT>
 __global__ void __launch_bounds__(kTmaThreads, 1)
     w2_gemv_tma_kernel(const __grid_constant__ CodeMaps maps, const __grid_constant__ GemvTmaArgs a) {
@@ -220,48 +236,32 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  // unit group u owns slots [u*DW, (u+1)*DW) and takes the CTA's units u, u + 3, ... in
-  // order, so no wait is ever more than one phase ahead of its barrier
-  const int DW = a.dw, TS = a.tslots, C = a.C, G = a.G, K = a.K;
-  const GemvTmaLayout L = gemv_tma_layout<MT>(G, DW, TS);
-  const uint32_t codes_u32 = smem_u32(smem + L.codes);
+  const int DW = a.dw, C = a.C, G = a.G, K = a.K;
+  const GemvTmaLayout L = gemv_tma_layout<MT>(G, DW);
+  const uint32_t slots_u32 = smem_u32(smem + L.codes);
   __half* img = reinterpret_cast<__half*>(smem + L.img);
   float2* cs = reinterpret_cast<float2*>(smem + L.cs);    // [G][MT] = (1024 sum x'/sigma, sum x')
-  float* accs = reinterpret_cast<float*>(smem + L.accs);  // [TS][128][MT]
-  int* cnt = reinterpret_cast<int*>(smem + L.cnt);         // [TS]
+  float* accs = reinterpret_cast<float*>(smem + L.accs);  // [kCutSlots][128][MT]
+  int* cnt = reinterpret_cast<int*>(smem + L.cnt);         // [kCutSlots]
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* empty = full + kGroupsOfWarps * DW;
+  uint64_t* xready = empty + kGroupsOfWarps * DW;
   __shared__ volatile int aborted;
 
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-  // this CTA's unit range
-  const int64_t S = (int64_t)a.n_tiles * C;
-  int64_t lo, hi;
+  // this CTA's unit range [lo, hi) and its cut into the groups' sub-ranges [bnd[u], bnd[u+1])
+  const int S = a.n_tiles * C;
+  int lo, hi;
   if (a.split) {
-    lo = S * blockIdx.x / gridDim.x;
-    hi = S * (blockIdx.x + 1) / gridDim.x;
+    lo = (int)((int64_t)S * blockIdx.x / gridDim.x);
+    hi = (int)((int64_t)S * (blockIdx.x + 1) / gridDim.x);
   } else {
-    lo = (int64_t)C * ((int64_t)a.n_tiles * blockIdx.x / gridDim.x);
-    hi = (int64_t)C * ((int64_t)a.n_tiles * (blockIdx.x + 1) / gridDim.x);
+    lo = C * (int)((int64_t)a.n_tiles * blockIdx.x / gridDim.x);
+    hi = C * (int)((int64_t)a.n_tiles * (blockIdx.x + 1) / gridDim.x);
   }
-  const int nst = (int)(hi - lo);
-  const int64_t tile_lo = lo / C;
-  // Order of this CTA's units: a partial tail tile first, then a partial head tile, then the
-  // complete tiles in order, so the cross-CTA sums of the shared tiles overlap the rest of
-  // the work.  The partial tail tile has its own accumulator slot (TS).
-  const int64_t last_tile = (hi - 1) / C;
-  const bool one_tile = tile_lo == last_tile;
-  const int hp = (!one_tile && lo % C) ? (int)((tile_lo + 1) * C - lo) : 0;
-  const int tp = (!one_tile && hi % C) ? (int)(hi - last_tile * C) : 0;
-  auto unit_of = [&](int q) -> int64_t {
-    if (q < tp) return last_tile * C + q;
-    if (q < tp + hp) return lo + (q - tp);
-    return lo + (q - tp);  // head and middle in order after the tail
-  };
-  auto slot_of = [&](int64_t tile) -> int {
-    return (tp > 0 && tile == last_tile) ? TS : (int)((tile - tile_lo) % TS);
-  };
+  const int nst = hi - lo;
+  const int bnd1 = lo + nst / 3, bnd2 = lo + (2 * nst) / 3;
 
   if (threadIdx.x == 0) {
     aborted = 0;
@@ -269,8 +269,11 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
       mbar_init(full + i, 1);
       mbar_init(empty + i, kWarpsPerUnit);
     }
+    mbar_init(xready, kTmaConsumers);
     fence_barrier_init();
   }
+  for (int i = threadIdx.x; i < kCutSlots * kUnitRows * MT; i += blockDim.x) accs[i] = 0.f;
+  if (threadIdx.x < kCutSlots) cnt[threadIdx.x] = 0;
   __syncthreads();
 
   auto wait = [&](uint64_t* bar, uint32_t parity) {
@@ -280,27 +283,47 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
       set_status(a.status, TB_DEV_TIMEOUT);
     }
   };
+  auto group_range = [&](int u, int& glo, int& ghi) {
+    glo = u == 0 ? lo : u == 1 ? bnd1 : bnd2;
+    ghi = u == 0 ? bnd1 : u == 1 ? bnd2 : hi;
+  };
 
   if (warp == kTmaConsumers) {
-    // ---- producer: the packed codes never depend on the previous kernel ----
+    // ---- producer: the packed weights never depend on the previous kernel ----
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
-      for (int q = 0; q < nst; ++q) {
-        const int n = q / kGroupsOfWarps, j = n % DW, k = n / DW;
-        const int slot = (q % kGroupsOfWarps) * DW + j;
-        if (k > 0) wait(empty + slot, (k - 1) & 1);
-        const int64_t s = unit_of(q);
-        const int tile = (int)(s / C), chunk = (int)(s - (int64_t)tile * C);
-        const int mi = mat_of(a, tile);
-        mbar_arrive_expect_tx(full + slot, kBoxBytes);
-        tma2d(codes_u32 + slot * kBoxBytes, &maps.m[mi], chunk * 32, (tile - a.tile0[mi]) * kUnitRows,
-              full + slot, pol);
+      int tl[kGroupsOfWarps], ch[kGroupsOfWarps], cntu[kGroupsOfWarps];
+      int maxcnt = 0;
+#pragma unroll
+      for (int u = 0; u < kGroupsOfWarps; ++u) {
+        int glo, ghi;
+        group_range(u, glo, ghi);
+        cntu[u] = ghi - glo;
+        const int first = u == kGroupsOfWarps - 1 ? ghi - 1 : glo;
+        tl[u] = first / C;
+        ch[u] = first - tl[u] * C;
+        maxcnt = cntu[u] > maxcnt ? cntu[u] : maxcnt;
       }
-      // leave no copy in flight: the last use of every slot has completed
-      for (int q = nst - 1; q >= 0 && q >= nst - kGroupsOfWarps * DW; --q) {
-        const int n = q / kGroupsOfWarps;
-        wait(full + (q % kGroupsOfWarps) * DW + n % DW, (n / DW) & 1);
+      for (int n = 0; n < maxcnt; ++n) {
+        if (n == kPreIssue) wait(xready, 0);  // the activations have been read
+#pragma unroll
+        for (int u = 0; u < kGroupsOfWarps; ++u) {
+          if (n >= cntu[u]) continue;
+          const int slot = u * DW + n % DW;
+          if (n >= DW) wait(empty + slot, ((n / DW) - 1) & 1);
+          const int mi = mat_of(a, tl[u]);
+          const int row = (tl[u] - a.tile0[mi]) * kUnitRows;
+          mbar_arrive_expect_tx(full + slot, kSlotBytes);
+          tma2d(slots_u32 + slot * kSlotBytes, &maps.codes[mi], ch[u] * 32, row, full + slot, pol);
+          step_unit(tl[u], ch[u], C, u == kGroupsOfWarps - 1);
+        }
       }
+      // leave no copy in flight: wait (bounded, even after a timeout) for the last fill of
+      // every slot
+#pragma unroll
+      for (int u = 0; u < kGroupsOfWarps; ++u)
+        for (int n = cntu[u] - 1; n >= 0 && n >= cntu[u] - DW; --n)
+          if (!mbar_wait(full + u * DW + n % DW, (n / DW) & 1)) set_status(a.status, TB_DEV_TIMEOUT);
     }
     __syncwarp();
     return;
@@ -309,33 +332,63 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
   // ---- consumers ----
   const int g = lane >> 2, t = lane & 3;
   const int ug = warp / kWarpsPerUnit, wi = warp % kWarpsPerUnit;
-  // scale / bias prefetch for this warp's units (rows 32*wi + lane of the unit)
-  auto load_sb = [&](int q, uint2& sv, uint2& bv) {
+  int glo, ghi;
+  group_range(ug, glo, ghi);
+  const bool back = ug == kGroupsOfWarps - 1;
+  const int ncnt = ghi - glo;
+  int tile = 0, chunk = 0;
+  if (ncnt > 0) {
+    const int first = back ? ghi - 1 : glo;
+    tile = first / C;
+    chunk = first - tile * C;
+  }
+  // scale / bias prefetch (rows 32*wi + lane of a unit), two units ahead of the one computed
+  int ptile = tile, pchunk = chunk, pn = 0;
+  auto load_sb = [&](uint2& sv, uint2& bv) {
     sv = make_uint2(0, 0);
     bv = make_uint2(0, 0);
-    if (q >= nst) return;
-    const int64_t s = unit_of(q);
-    const int tile = (int)(s / C), chunk = (int)(s - (int64_t)tile * C);
-    const int mi = mat_of(a, tile);
-    const int row = (tile - a.tile0[mi]) * kUnitRows + 32 * wi + lane;
-    if (row < a.N[mi]) {
-      const int64_t off = (int64_t)row * G + chunk * kUnitGroups;
-      sv = __ldg(reinterpret_cast<const uint2*>(a.scales[mi] + off));
-      bv = __ldg(reinterpret_cast<const uint2*>(a.biases[mi] + off));
+    if (pn < ncnt) {
+      const int mi = mat_of(a, ptile);
+      const int row = (ptile - a.tile0[mi]) * kUnitRows + 32 * wi + lane;
+      if (row < a.N[mi]) {
+        const int64_t off = (int64_t)row * G + pchunk * kUnitGroups;
+        sv = __ldg(reinterpret_cast<const uint2*>(a.scales[mi] + off));
+        bv = __ldg(reinterpret_cast<const uint2*>(a.biases[mi] + off));
+      }
     }
+    ++pn;
+    step_unit(ptile, pchunk, C, back);
   };
-  uint2 s0, b0, s1, b1;
-  load_sb(ug, s0, b0);
-  load_sb(ug + kGroupsOfWarps, s1, b1);
+  uint2 sA, bA, sB, bB;
+  load_sb(sA, bA);
+  load_sb(sB, bB);
 
   asm volatile("griddepcontrol.wait;" ::: "memory");
   {
-    // prologue: x' = fwht(signs * x) -> B-fragment image, (C, S) per group and token.
-    // Every consumer warp takes blocks (token, 1024-slice) warp, warp + 12, ...; the loads of
-    // two blocks are issued before either is transformed, so a warp waits once per pair.
-    const int nchunk = K / kBlock;
+    // prologue: x' = fwht(signs * x) -> B-fragment image, (C, S) per group and token, for the
+    // 1024-blocks that this CTA's units read.  Every consumer warp takes items (token, block)
+    // warp, warp + 12, ...; the loads of two items are issued before either is transformed,
+    // so a warp waits once per pair.
+    const int nb = K / kBlock;
+    int b1 = 0, e1 = nb, b2 = 0, e2 = 0;  // the blocks needed: [b1, e1) and [b2, e2)
+    if (nst > 0 && nst < C) {
+      constexpr int kChunksPerBlock = kBlock / (kUnitGroups * kGroup);
+      const int clo = lo % C, cend = clo + nst;
+      b1 = clo / kChunksPerBlock;
+      if (cend <= C) {
+        e1 = (cend - 1) / kChunksPerBlock + 1;
+      } else {
+        e2 = (cend - C - 1) / kChunksPerBlock + 1;
+        if (e2 >= b1) {
+          b1 = 0;
+          e2 = 0;
+        }
+      }
+    }
+    const int nblk = (e1 - b1) + (e2 - b2);
     auto load_block = [&](int it, uint4 (&xr)[4], uint4 (&sr)[2]) {
-      const int tok = it / nchunk, b = it - tok * nchunk;
+      const int tok = it / nblk, bi = it - tok * nblk;
+      const int b = bi < e1 - b1 ? b1 + bi : b2 + (bi - (e1 - b1));
       if (tok < a.Mc) {
         const uint4* xs = reinterpret_cast<const uint4*>(a.x + (int64_t)tok * K + b * kBlock + lane * 32);
 #pragma unroll
@@ -351,7 +404,8 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
       }
     };
     auto transform_block = [&](int it, const uint4 (&xr)[4], const uint4 (&sr)[2]) {
-      const int tok = it / nchunk, b = it - tok * nchunk;
+      const int tok = it / nblk, bi = it - tok * nblk;
+      const int b = bi < e1 - b1 ? b1 + bi : b2 + (bi - (e1 - b1));
       // layout A: v[r] = element b*1024 + lane*32 + r
       float v[32];
 #pragma unroll
@@ -378,6 +432,8 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         v[r] = __half2float(__float2half_rn(v[r]));  // x' rounded to fp16
         ssum += v[r];
       }
+      ssum += __shfl_xor_sync(0xffffffffu, ssum, 1);
+      ssum += __shfl_xor_sync(0xffffffffu, ssum, 2);
 #pragma unroll
       for (int mp = 0; mp < 4; ++mp) {
         uint32_t pk[4];
@@ -393,70 +449,74 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         *reinterpret_cast<uint4*>(img + ((size_t)(grp * 4 + mp) * MT + tok) * 32 + t * 8) =
             make_uint4(pk[0], pk[1], pk[2], pk[3]);
       }
-      ssum += __shfl_xor_sync(0xffffffffu, ssum, 1);
-      ssum += __shfl_xor_sync(0xffffffffu, ssum, 2);
       csum += __shfl_xor_sync(0xffffffffu, csum, 1);
       csum += __shfl_xor_sync(0xffffffffu, csum, 2);
       if (t == 0) cs[grp * MT + tok] = make_float2(1024.f * csum, ssum);
     };
-    const int items = MT * nchunk;
-    for (int it = warp; it < items; it += 2 * kTmaFwhtWarps) {
-      const int it2 = it + kTmaFwhtWarps;
+    const int items = MT * nblk;
+    bool told = false;
+    for (int it = warp; it < items; it += 2 * kTmaConsumers) {
+      const int it2 = it + kTmaConsumers;
       uint4 xa[4], sa[2], xb[4], sb2[2];
       load_block(it, xa, sa);
       if (it2 < items) load_block(it2, xb, sb2);
       transform_block(it, xa, sa);
       if (it2 < items) transform_block(it2, xb, sb2);
+      if (!told) {  // this warp's first activations are in: the producer may stream on
+        told = true;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(xready);
+      }
     }
-    asm volatile("bar.sync 1, %0;" ::"n"(kTmaConsumers * 32) : "memory");
-    // zero the tile accumulators
-    for (int i = threadIdx.x; i < (TS + 1) * kUnitRows * MT; i += kTmaConsumers * 32) accs[i] = 0.f;
-    for (int i = threadIdx.x; i <= TS; i += kTmaConsumers * 32) cnt[i] = 0;
+    if (!told && lane == 0) mbar_arrive(xready);
     asm volatile("bar.sync 1, %0;" ::"n"(kTmaConsumers * 32) : "memory");
   }
 
   // mma row g <-> unit row 32*wi + 16*j + rA (and + 8): conflict-free swizzled reads
   const int rA = 2 * (g & 3) + (g >> 2);
+  const int R0 = 32 * wi + rA;
   const int tokc = g < MT ? g : 0;
   const uint32_t imgt = smem_u32(img) + tokc * 64 + t * 16;
   const uint32_t csa = smem_u32(cs);
-  const uint32_t ss = smem_u32(smem + L.sstage) + warp * kScaleStageBytes;
   const uint32_t accs_u32 = smem_u32(accs);
   const int t0 = min(2 * t, MT - 1), t1 = min(2 * t + 1, MT - 1);
+  const uint32_t ss = smem_u32(smem + L.sstage) + warp * kScaleStageBytes;
 
-  for (int q = ug, n = 0; q < nst; q += kGroupsOfWarps, ++n) {
-    // stage this unit's scales and biases, prefetch the ones two units ahead
-    {
-      const uint32_t r = ss + lane * kUnitGroups * 8;
-      const __half2 sh0 = *reinterpret_cast<const __half2*>(&s0.x), sh1 = *reinterpret_cast<const __half2*>(&s0.y);
-      const __half2 bh0 = *reinterpret_cast<const __half2*>(&b0.x), bh1 = *reinterpret_cast<const __half2*>(&b0.y);
-      const float2 sf0 = __half22float2(sh0), sf1 = __half22float2(sh1);
-      const float2 bf0 = __half22float2(bh0), bf1 = __half22float2(bh1);
-      asm volatile("st.shared.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(r), "f"(sf0.x), "f"(bf0.x), "f"(sf0.y), "f"(bf0.y) : "memory");
-      asm volatile("st.shared.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(r + 16), "f"(sf1.x), "f"(bf1.x), "f"(sf1.y), "f"(bf1.y) : "memory");
-      s0 = s1;
-      b0 = b1;
-      load_sb(q + 2 * kGroupsOfWarps, s1, b1);
-      __syncwarp();
-    }
-    const int slot = ug * DW + n % DW;
-    wait(full + slot, (n / DW) & 1);
-    const int64_t s = unit_of(q);
-    const int tile = (int)(s / C), chunk = (int)(s - (int64_t)tile * C);
-    const uint32_t box = codes_u32 + slot * kBoxBytes;
-    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+  // Add this warp's sums of tile T (all of the group's units of T) to wherever T is finished.
+  auto flush = [&](int T, float (&acc)[2][4]) {
+    const int mi = mat_of(a, T);
+    const int N = a.N[mi], row0 = (T - a.tile0[mi]) * kUnitRows;
+    __half* yo = a.y[mi];
+    const int tb = T * C, te = tb + C;
+    if (tb >= glo && te <= ghi) {  // the whole tile is this group's: these 32 rows are final
 #pragma unroll
-    for (int gi = 0; gi < kUnitGroups; ++gi)
-      unit_group<MT>(box, 32 * wi + rA, t, gi, chunk * kUnitGroups + gi, imgt, ss, rA, csa, t0, t1, acc);
-    __syncwarp();
-    if (lane == 0) mbar_arrive(empty + slot);
-
-    // add this warp's 32 rows into the tile's shared accumulator
-    const int ts = slot_of(tile);
-    const uint32_t atu = accs_u32 + ts * kUnitRows * MT * 4;
+      for (int j = 0; j < 2; ++j) {
+        const int ra = row0 + R0 + 16 * j, rb = ra + 8;
+        if (2 * t < a.Mc) {
+          if (ra < N) yo[(int64_t)(2 * t) * N + ra] = __float2half_rn(acc[j][0]);
+          if (rb < N) yo[(int64_t)(2 * t) * N + rb] = __float2half_rn(acc[j][2]);
+        }
+        if (2 * t + 1 < a.Mc) {
+          if (ra < N) yo[(int64_t)(2 * t + 1) * N + ra] = __float2half_rn(acc[j][1]);
+          if (rb < N) yo[(int64_t)(2 * t + 1) * N + rb] = __float2half_rn(acc[j][3]);
+        }
+      }
+      return;
+    }
+    // a tile cut by a boundary: its shared slot is the first boundary that falls in it
+    const int b = (lo / C == T) ? 0 : (bnd1 / C == T) ? 1 : (bnd2 / C == T) ? 2 : 3;
+    // contributions expected in this CTA: 4 warps of every group whose sub-range meets T
+    int groups = 0;
+#pragma unroll
+    for (int u = 0; u < kGroupsOfWarps; ++u) {
+      int ulo, uhi;
+      group_range(u, ulo, uhi);
+      groups += (ulo < uhi && ulo < te && uhi > tb);
+    }
+    const uint32_t atu = accs_u32 + b * kUnitRows * MT * 4;
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
-      const int ra = 32 * wi + 16 * j + rA, rb = ra + 8;
+      const int ra = R0 + 16 * j, rb = ra + 8;
       if (2 * t < MT) {
         red_shared_add(atu + (ra * MT + 2 * t) * 4, acc[j][0]);
         red_shared_add(atu + (rb * MT + 2 * t) * 4, acc[j][2]);
@@ -466,51 +526,38 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         red_shared_add(atu + (rb * MT + 2 * t + 1) * 4, acc[j][3]);
       }
     }
-    const int64_t t_beg = (int64_t)tile * C, t_end = t_beg + C;
-    const int64_t c_beg = t_beg > lo ? t_beg : lo, c_end = t_end < hi ? t_end : hi;
-    const int need = (int)(c_end - c_beg) * kWarpsPerUnit;
     __syncwarp();
     int last = 0;
     if (lane == 0) {
       __threadfence_block();
-      last = atomicAdd(cnt + ts, 1) == need - 1;
+      last = atomicAdd(cnt + b, 1) == groups * kWarpsPerUnit - 1;
     }
     last = __shfl_sync(0xffffffffu, last, 0);
-    if (!last) continue;
-
+    if (!last) return;
     // this warp finishes the tile for this CTA
     __threadfence_block();
-    float* at = accs + ts * kUnitRows * MT;
-    const int mi = mat_of(a, tile);
-    const int N = a.N[mi], row0 = (tile - a.tile0[mi]) * kUnitRows;
-    __half* yo = a.y[mi];
-    const bool complete = t_beg >= lo && t_end <= hi;
-    // a tile shared with other CTAs is summed in the workspace slot of its first CTA
-    const int first = complete ? 0 : stage_owner(t_beg, S, gridDim.x);
-    float* wsum = a.ws_partial + (int64_t)first * kUnitRows * MT;
-    for (int e = lane; e < kUnitRows * MT; e += 32) {
-      const float u = at[e];
-      at[e] = 0.f;
-      const int r_ = e / MT, k_ = e - r_ * MT;
-      if (complete) {
-        if (row0 + r_ < N && k_ < a.Mc) yo[(int64_t)k_ * N + row0 + r_] = __float2half_rn(u);
-      } else {
-        atomicAdd(wsum + e, u);
+    const float* at = accs + b * kUnitRows * MT;
+    if (tb >= lo && te <= hi) {
+      for (int e = lane; e < kUnitRows * MT; e += 32) {
+        const int r_ = e / MT, k_ = e - r_ * MT;
+        if (row0 + r_ < N && k_ < a.Mc) yo[(int64_t)k_ * N + row0 + r_] = __float2half_rn(at[e]);
       }
+      return;
     }
+    // shared with other CTAs: summed in the workspace slot of the tile's first CTA
+    const int first = stage_owner(tb, S, gridDim.x);
+    float* wsum = a.ws_partial + (int64_t)first * kUnitRows * MT;
+    for (int e = lane; e < kUnitRows * MT; e += 32) atomicAdd(wsum + e, at[e]);
     __syncwarp();
-    if (lane == 0) cnt[ts] = 0;
-    __threadfence_block();
-    if (complete) continue;
     // the last of the tile's CTAs converts the sum, then returns the slot and counter to zero
-    const int lastc = stage_owner(t_end - 1, S, gridDim.x);
+    const int lastc = stage_owner(te - 1, S, gridDim.x);
     int fin = 0;
     if (lane == 0) {
       __threadfence();
       fin = atomicAdd(a.ws_count + first, 1) == lastc - first;
     }
     fin = __shfl_sync(0xffffffffu, fin, 0);
-    if (!fin) continue;
+    if (!fin) return;
     __threadfence();
     for (int e = lane; e < kUnitRows * MT; e += 32) {
       const float v = __ldcg(wsum + e);
@@ -519,6 +566,43 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
       if (row0 + r_ < N && k_ < a.Mc) yo[(int64_t)k_ * N + row0 + r_] = __float2half_rn(v);
     }
     if (lane == 0) a.ws_count[first] = 0;
+  };
+
+  float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+  // unit n with its scales and biases in (sv, bv), which are then reloaded for unit n + 2
+  auto body = [&](int n, uint2& sv, uint2& bv) {
+    {
+      const uint32_t r = ss + lane * kUnitGroups * 8;
+      const float2 sf0 = __half22float2(*reinterpret_cast<const __half2*>(&sv.x));
+      const float2 sf1 = __half22float2(*reinterpret_cast<const __half2*>(&sv.y));
+      const float2 bf0 = __half22float2(*reinterpret_cast<const __half2*>(&bv.x));
+      const float2 bf1 = __half22float2(*reinterpret_cast<const __half2*>(&bv.y));
+      asm volatile("st.shared.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(r), "f"(sf0.x), "f"(bf0.x), "f"(sf0.y), "f"(bf0.y) : "memory");
+      asm volatile("st.shared.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(r + 16), "f"(sf1.x), "f"(bf1.x), "f"(sf1.y), "f"(bf1.y) : "memory");
+      load_sb(sv, bv);
+      __syncwarp();
+    }
+    const int slot = ug * DW + n % DW;
+    wait(full + slot, (n / DW) & 1);
+    const uint32_t box = slots_u32 + slot * kSlotBytes;
+#pragma unroll
+    for (int gi = 0; gi < kUnitGroups; ++gi)
+      unit_group<MT>(box, R0, t, gi, chunk * kUnitGroups + gi, imgt, ss, rA, csa, t0, t1, acc);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty + slot);
+    const int cur = tile;
+    step_unit(tile, chunk, C, back);
+    if (tile != cur || n == ncnt - 1) {
+      flush(cur, acc);
+#pragma unroll
+      for (int j = 0; j < 2; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[j][e] = 0.f;
+    }
+  };
+  for (int n = 0; n < ncnt; n += 2) {  // two bodies per pass: no register copies between loads
+    body(n, sA, bA);
+    if (n + 1 < ncnt) body(n + 1, sB, bB);
   }
 }
 
@@ -592,12 +676,10 @@ static int launch_tma_mt(GemvTmaArgs a, const CodeMaps& maps, int64_t M, int64_t
                          const DeviceFacts& f, cudaStream_t s) {
   // slots per unit group from what is left of shared memory
   int dw = kMaxSlotsPerGroup;
-  auto ts_for = [&](int d) { return kGroupsOfWarps * d / a.C + 3; };
-  while (dw >= 1 && gemv_tma_layout<MT>(a.G, dw, ts_for(dw)).total > f.smem_optin) --dw;
+  while (dw >= 1 && gemv_tma_layout<MT>(a.G, dw).total > f.smem_optin) --dw;
   if (dw < 1) return TB_ERR_SHAPE;
   a.dw = dw;
-  a.tslots = ts_for(dw);
-  const int bytes = gemv_tma_layout<MT>(a.G, dw, a.tslots).total;
+  const int bytes = gemv_tma_layout<MT>(a.G, dw).total;
   cudaError_t e = cudaFuncSetAttribute(w2_gemv_tma_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e != cudaSuccess) {
     record_cuda_error(e);
@@ -635,14 +717,13 @@ static int launch_tma_mt(GemvTmaArgs a, const CodeMaps& maps, int64_t M, int64_t
 
 // tokens per pass: the largest of 8, 4, 2, 1 (not above M rounded up) whose B image leaves
 // room for two slots per unit group
-static int tma_tokens_per_pass(int64_t M, int G, int C, int smem_optin) {
+static int tma_tokens_per_pass(int64_t M, int G, int smem_optin) {
   int mt = M >= 5 ? 8 : M >= 3 ? 4 : M == 2 ? 2 : 1;
   auto fits = [&](int total) { return total <= smem_optin; };
   while (mt > 1) {
-    const int ts = kGroupsOfWarps * 2 / C + 3;
-    const bool ok = mt == 8 ? fits(gemv_tma_layout<8>(G, 2, ts).total)
-                  : mt == 4 ? fits(gemv_tma_layout<4>(G, 2, ts).total)
-                            : fits(gemv_tma_layout<2>(G, 2, ts).total);
+    const bool ok = mt == 8 ? fits(gemv_tma_layout<8>(G, 2).total)
+                  : mt == 4 ? fits(gemv_tma_layout<4>(G, 2).total)
+                            : fits(gemv_tma_layout<2>(G, 2).total);
     if (ok) break;
     mt >>= 1;
   }
@@ -662,20 +743,22 @@ int launch_gemv_tma_multi(const __half* x, int64_t M, int64_t K, const int8_t* s
   if (K > (1 << 22) || K % kBlock) return TB_ERR_SHAPE;
   GemvTmaArgs a = {};
   CodeMaps maps;
-  int tiles = 0;
+  int64_t tiles = 0;
   for (int i = 0; i < nmat; ++i) {
     if (N[i] < 1 || N[i] > (1LL << 30)) return TB_ERR_SHAPE;
-    rc = code_map(w[i], N[i], K, &maps.m[i]);
+    rc = code_map(w[i], N[i], K, &maps.codes[i]);
     if (rc != TB_OK) return rc;
     a.scales[i] = scales[i];
     a.biases[i] = biases[i];
     a.y[i] = y[i];
     a.N[i] = (int)N[i];
-    a.tile0[i] = tiles;
-    tiles += (int)((N[i] + kUnitRows - 1) / kUnitRows);
+    a.tile0[i] = (int)tiles;
+    tiles += (N[i] + kUnitRows - 1) / kUnitRows;
   }
-  for (int i = nmat; i <= kMaxMats; ++i) a.tile0[i] = tiles;
-  for (int i = nmat; i < kMaxMats; ++i) maps.m[i] = maps.m[0];
+  // unit indices (tiles x K/512) are 32-bit in the kernel
+  if (tiles * (K / (kUnitGroups * kGroup)) > (int64_t)INT32_MAX / 2) return TB_ERR_SHAPE;
+  for (int i = nmat; i <= kMaxMats; ++i) a.tile0[i] = (int)tiles;
+  for (int i = nmat; i < kMaxMats; ++i) maps.codes[i] = maps.codes[0];
   a.nmat = nmat;
   a.x = x;
   a.signs = signs;
@@ -688,9 +771,9 @@ int launch_gemv_tma_multi(const __half* x, int64_t M, int64_t K, const int8_t* s
   a.G = (int)(K / kGroup);
   a.C = (int)(K / (kUnitGroups * kGroup));
   a.rotate = block != 0;
-  a.n_tiles = tiles;
+  a.n_tiles = (int)tiles;
   a.status = status;
-  const int mt = tma_tokens_per_pass(M, a.G, a.C, f.smem_optin);
+  const int mt = tma_tokens_per_pass(M, a.G, f.smem_optin);
   switch (mt) {
     case 8: return launch_tma_mt<8>(a, maps, M, K, f, s);
     case 4: return launch_tma_mt<4>(a, maps, M, K, f, s);
