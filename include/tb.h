@@ -115,11 +115,12 @@ int tb_fwht(const uint16_t* x, uint16_t* y, const int8_t* signs, int64_t M, int6
 
 /*
  * Bytes of workspace tb_packed_linear uses for these sizes.  Layout: a fixup region
- * (about 1 MB) for the decode GEMV's split schedule (fp32 sums and counters of output
- * tiles shared by several SMs), then, for the tensor-core path, the rotated activations
- * x' (fp16 [M, K]).  The fixup region must be zero-filled before the first call
- * that uses the workspace; every completed call leaves it zero (a call that reported
- * TB_DEV_TIMEOUT may not: zero it again).  Calls sharing one workspace must be
+ * (about 2 MB) for the decode GEMV's split schedule: counters of output tiles shared by
+ * several SMs in its first 1024 bytes, then the SMs' fp32 parts of those tiles; then, for
+ * the tensor-core path, the rotated activations x' (fp16 [M, K]).  The first 1024 bytes
+ * must be zero before the first call that uses the workspace (zero-filling the whole
+ * workspace will do); every completed call leaves them zero (a call that reported
+ * TB_DEV_TIMEOUT may not: zero them again).  Calls sharing one workspace must be
  * ordered on one stream.
  */
 size_t tb_packed_linear_workspace_size(int64_t M, int64_t K, int64_t N, int block);
@@ -192,13 +193,13 @@ int tb_embed_lookup(const int32_t* ids, int64_t T, const uint32_t* w, const uint
  * budget after start-up.)
  * Same arguments and result as tb_packed_linear for M <= 8 tokens, without workspace.
  * The state of the GEMV's split schedule lives in a fixed array inside the library
- * (about 1 MiB on every GPU that loads it, held until the process exits).
+ * (about 2 MiB on every GPU that loads it, held until the process exits).
  *   - It allocates nothing: no cudaMalloc, no cudaFree, no allocating library call.
  *   - Limits: M <= 8 and a GPU with at most 256 SMs, else TB_ERR_TOO_LARGE;
  *     K a positive multiple of 1024 (block 1024, or block 0 with such a K), else TB_ERR_SHAPE.
  *   - The first call on each device looks up the array's device address for that device
  *     (cudaGetSymbolAddress); make that first call before any stream capture.
- *   - Each call clears the array on `stream` before using it (cudaMemsetAsync).  All calls
+ *   - Each call clears the array's counters on `stream` before using it (cudaMemsetAsync).  All calls
  *     share the one array: calls that can overlap on the GPU (different streams, or
  *     different host threads) race and give wrong results; order them on one stream.
  */

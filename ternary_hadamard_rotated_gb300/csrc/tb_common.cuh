@@ -34,6 +34,11 @@ TB_DEVI uint64_t globaltimer_ns() {
   return t;
 }
 
+// gpu-scope release/acquire fence: orders this thread's earlier accesses (and, through a
+// preceding warp barrier, its warp's) before its later ones for every thread on the GPU,
+// without the cost of a sequentially consistent fence
+TB_DEVI void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
 TB_DEVI void set_status(int32_t* st, int bits) {
   if (st) atomicOr(st, bits);
 }

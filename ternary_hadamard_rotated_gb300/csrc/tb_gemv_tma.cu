@@ -66,8 +66,8 @@ struct GemvTmaArgs {
   int N[kMaxMats];               // rows of matrix i
   int tile0[kMaxMats + 1];       // first 128-row tile of matrix i in the concatenated tile list
   int nmat;
-  float* ws_partial;             // [kFixupCtas][128][MT] fp32 sums of shared tiles, or null (tile-aligned)
-  int* ws_count;                 // [kFixupCtas]
+  float* ws_partial;             // [kFixupCtas][2][128][MT] fp32 partial tiles, or null (tile-aligned)
+  int* ws_count;                 // [kFixupCtas] contributions counted per shared tile
   int Mc, K, G, C;               // C = units per tile = K / 512
   int rotate, dw;
   int n_tiles;                   // total 128-row tiles of all matrices
@@ -116,6 +116,13 @@ __host__ __device__ inline GemvTmaLayout gemv_tma_layout(int G, int dw) {
   off += (2 * kGroupsOfWarps * dw + 1) * 8;
   L.total = off + 1024;  // slack to align the base to 1024
   return L;
+}
+
+// stream-K unit range [lo, hi) of CTA c
+__host__ __device__ inline void cta_range_of(int c, int grid, int n_tiles, int C, int& lo, int& hi) {
+  const int64_t S = (int64_t)n_tiles * C;
+  lo = (int)(S * c / grid);
+  hi = (int)(S * (c + 1) / grid);
 }
 
 // owner of global unit s when S units are cut into grid ranges [S*i/grid, S*(i+1)/grid)
@@ -304,18 +311,22 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         ch[u] = first - tl[u] * C;
         maxcnt = cntu[u] > maxcnt ? cntu[u] : maxcnt;
       }
-      for (int n = 0; n < maxcnt; ++n) {
+      for (int n = 0, si = 0, k = 0; n < maxcnt; ++n) {  // si = n % DW, k = n / DW
         if (n == kPreIssue) wait(xready, 0);  // the activations have been read
 #pragma unroll
         for (int u = 0; u < kGroupsOfWarps; ++u) {
           if (n >= cntu[u]) continue;
-          const int slot = u * DW + n % DW;
-          if (n >= DW) wait(empty + slot, ((n / DW) - 1) & 1);
+          const int slot = u * DW + si;
+          if (k > 0) wait(empty + slot, (k - 1) & 1);
           const int mi = mat_of(a, tl[u]);
           const int row = (tl[u] - a.tile0[mi]) * kUnitRows;
           mbar_arrive_expect_tx(full + slot, kSlotBytes);
           tma2d(slots_u32 + slot * kSlotBytes, &maps.codes[mi], ch[u] * 32, row, full + slot, pol);
           step_unit(tl[u], ch[u], C, u == kGroupsOfWarps - 1);
+        }
+        if (++si == DW) {
+          si = 0;
+          ++k;
         }
       }
       // leave no copy in flight: wait (bounded, even after a timeout) for the last fill of
@@ -342,18 +353,26 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     tile = first / C;
     chunk = first - tile * C;
   }
-  // scale / bias prefetch (rows 32*wi + lane of a unit), two units ahead of the one computed
-  int ptile = tile, pchunk = chunk, pn = 0;
+  // scale / bias prefetch (rows 32*wi + lane of a unit), two units ahead of the one computed;
+  // the row's pointers are looked up only when the prefetch enters a new tile
+  int ptile = tile, pchunk = chunk, pn = 0, prow_tile = -1;
+  const __half* psrow = nullptr;
+  const __half* pbrow = nullptr;
   auto load_sb = [&](uint2& sv, uint2& bv) {
     sv = make_uint2(0, 0);
     bv = make_uint2(0, 0);
     if (pn < ncnt) {
-      const int mi = mat_of(a, ptile);
-      const int row = (ptile - a.tile0[mi]) * kUnitRows + 32 * wi + lane;
-      if (row < a.N[mi]) {
-        const int64_t off = (int64_t)row * G + pchunk * kUnitGroups;
-        sv = __ldg(reinterpret_cast<const uint2*>(a.scales[mi] + off));
-        bv = __ldg(reinterpret_cast<const uint2*>(a.biases[mi] + off));
+      if (ptile != prow_tile) {
+        prow_tile = ptile;
+        const int mi = mat_of(a, ptile);
+        const int row = (ptile - a.tile0[mi]) * kUnitRows + 32 * wi + lane;
+        const bool in = row < a.N[mi];
+        psrow = in ? a.scales[mi] + (int64_t)row * G : nullptr;
+        pbrow = in ? a.biases[mi] + (int64_t)row * G : nullptr;
+      }
+      if (psrow) {
+        sv = __ldg(reinterpret_cast<const uint2*>(psrow + pchunk * kUnitGroups));
+        bv = __ldg(reinterpret_cast<const uint2*>(pbrow + pchunk * kUnitGroups));
       }
     }
     ++pn;
@@ -544,31 +563,58 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
       }
       return;
     }
-    // shared with other CTAs: summed in the workspace slot of the tile's first CTA
-    const int first = stage_owner(tb, S, gridDim.x);
-    float* wsum = a.ws_partial + (int64_t)first * kUnitRows * MT;
-    for (int e = lane; e < kUnitRows * MT; e += 32) atomicAdd(wsum + e, at[e]);
+    // shared with other CTAs: this CTA's part goes to its own workspace slot (plain stores:
+    // float atomics into one shared slot wait far longer under the weight stream), slot 0
+    // for the tile of its first unit, 1 for the tile of its last
+    float* mine = a.ws_partial + ((int64_t)blockIdx.x * 2 + (lo / C == T ? 0 : 1)) * kUnitRows * MT;
+    for (int e = lane; e < kUnitRows * MT; e += 32) __stcg(mine + e, at[e]);
     __syncwarp();
-    // the last of the tile's CTAs converts the sum, then returns the slot and counter to zero
+    // the last of the tile's CTAs to count in adds the parts in CTA order (the result does
+    // not depend on which CTA finishes last) and returns the counter to zero
+    const int first = stage_owner(tb, S, gridDim.x);
     const int lastc = stage_owner(te - 1, S, gridDim.x);
     int fin = 0;
     if (lane == 0) {
-      __threadfence();
+      fence_acq_rel_gpu();  // the warp's part before the count
       fin = atomicAdd(a.ws_count + first, 1) == lastc - first;
     }
     fin = __shfl_sync(0xffffffffu, fin, 0);
     if (!fin) return;
-    __threadfence();
-    for (int e = lane; e < kUnitRows * MT; e += 32) {
-      const float v = __ldcg(wsum + e);
-      wsum[e] = 0.f;
-      const int r_ = e / MT, k_ = e - r_ * MT;
-      if (row0 + r_ < N && k_ < a.Mc) yo[(int64_t)k_ * N + row0 + r_] = __float2half_rn(v);
+    fence_acq_rel_gpu();  // every contributor's part after the count
+    // the tile starts inside CTA `first` (its slot 0 when the tile is also the tile of its
+    // first unit, else 1); every later contributor starts inside the tile (slot 0)
+    int flo, fhi;
+    cta_range_of(first, gridDim.x, a.n_tiles, C, flo, fhi);
+    const float* p0 = a.ws_partial + ((int64_t)first * 2 + (flo / C == T ? 0 : 1)) * kUnitRows * MT;
+    for (int eb = 0; eb < kUnitRows * MT; eb += 128) {  // four elements per lane per pass
+      float v[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int c = first; c <= lastc; c += 4) {  // four contributors' loads in flight at once
+        float l[4][4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int cc = c + q;
+          const float* pc = cc == first ? p0 : a.ws_partial + (int64_t)cc * 2 * kUnitRows * MT;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) l[q][k] = cc <= lastc ? __ldcg(pc + eb + lane + 32 * k) : 0.f;
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+#pragma unroll
+          for (int k = 0; k < 4; ++k) v[k] += l[q][k];
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int e = eb + lane + 32 * k;
+        const int r_ = e / MT, k_ = e - r_ * MT;
+        if (row0 + r_ < N && k_ < a.Mc) yo[(int64_t)k_ * N + row0 + r_] = __float2half_rn(v[k]);
+      }
     }
     if (lane == 0) a.ws_count[first] = 0;
   };
 
   float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+  int si = 0;        // ring slot of the current unit within the group's DW slots: n % DW
+  uint32_t ph = 0;   // its fill parity: (n / DW) & 1
   // unit n with its scales and biases in (sv, bv), which are then reloaded for unit n + 2
   auto body = [&](int n, uint2& sv, uint2& bv) {
     {
@@ -579,17 +625,23 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
       const float2 bf1 = __half22float2(*reinterpret_cast<const __half2*>(&bv.y));
       asm volatile("st.shared.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(r), "f"(sf0.x), "f"(bf0.x), "f"(sf0.y), "f"(bf0.y) : "memory");
       asm volatile("st.shared.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(r + 16), "f"(sf1.x), "f"(bf1.x), "f"(sf1.y), "f"(bf1.y) : "memory");
-      load_sb(sv, bv);
       __syncwarp();
     }
-    const int slot = ug * DW + n % DW;
-    wait(full + slot, (n / DW) & 1);
+    const int slot = ug * DW + si;
+    wait(full + slot, ph);
+    if (++si == DW) {
+      si = 0;
+      ph ^= 1;
+    }
     const uint32_t box = slots_u32 + slot * kSlotBytes;
 #pragma unroll
     for (int gi = 0; gi < kUnitGroups; ++gi)
       unit_group<MT>(box, R0, t, gi, chunk * kUnitGroups + gi, imgt, ss, rA, csa, t0, t1, acc);
     __syncwarp();
     if (lane == 0) mbar_arrive(empty + slot);
+    // the next loads are issued only after the release of the slot, which would otherwise
+    // wait for them to complete
+    load_sb(sv, bv);
     const int cur = tile;
     step_unit(tile, chunk, C, back);
     if (tile != cur || n == ncnt - 1) {
@@ -664,12 +716,15 @@ static int code_map(const uint32_t* w, int64_t N, int64_t K, CUtensorMap* out) {
   return TB_OK;
 }
 
-// workspace of the split (stream-K) schedule: fp32 sums [kFixupCtas][128][8] of tiles shared
-// by several CTAs (indexed by the tile's first CTA), then counters [kFixupCtas]; both must
-// be zero before a call and are zero after it
+// workspace of the split (stream-K) schedule: counters [kFixupCtas] of tiles shared by
+// several CTAs (indexed by the tile's first CTA; zero before a call and after it), then
+// each CTA's fp32 parts [kFixupCtas][2][128][8] of the shared tiles it computes (scratch)
 constexpr int kFixupCtas = 256;
-constexpr size_t kFixupPartialBytes = (size_t)kFixupCtas * kUnitRows * 8 * 4;
-size_t gemv_fixup_bytes() { return kFixupPartialBytes + kFixupCtas * 4; }
+constexpr size_t kFixupCounterBytes = 1024;
+constexpr size_t kFixupPartialBytes = (size_t)kFixupCtas * 2 * kUnitRows * 8 * 4;
+static_assert(kFixupCtas * 4 <= kFixupCounterBytes, "counters fit their region");
+size_t gemv_fixup_bytes() { return kFixupCounterBytes + kFixupPartialBytes; }
+size_t gemv_fixup_counter_bytes() { return kFixupCounterBytes; }
 
 template <int MT>
 static int launch_tma_mt(GemvTmaArgs a, const CodeMaps& maps, int64_t M, int64_t K,
@@ -763,9 +818,9 @@ int launch_gemv_tma_multi(const __half* x, int64_t M, int64_t K, const int8_t* s
   a.x = x;
   a.signs = signs;
   const bool split = workspace && ws_bytes >= gemv_fixup_bytes() && f.sms <= kFixupCtas;
-  a.ws_partial = split ? static_cast<float*>(workspace) : nullptr;
-  a.ws_count = split ? reinterpret_cast<int*>(static_cast<char*>(workspace) + kFixupPartialBytes)
-                     : nullptr;
+  a.ws_count = split ? static_cast<int*>(workspace) : nullptr;
+  a.ws_partial = split ? reinterpret_cast<float*>(static_cast<char*>(workspace) + kFixupCounterBytes)
+                       : nullptr;
   a.split = split ? 1 : 0;
   a.K = (int)K;
   a.G = (int)(K / kGroup);

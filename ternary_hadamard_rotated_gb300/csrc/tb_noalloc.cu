@@ -5,9 +5,9 @@
 // runtime that owns every byte of device memory through its own pool, or services that
 // forbid any allocation after start-up so their memory footprint stays fixed.  For them,
 // tb_packed_linear_gemv_noalloc runs the same decode GEMV as tb_packed_linear (M <= 8),
-// with the state of its split schedule (fp32 sums and counters of output tiles shared by
+// with the state of its split schedule (counters and fp32 parts of output tiles shared by
 // several SMs) kept in a fixed array compiled into this library instead of a caller's
-// workspace.  Every GPU that loads the library holds that array (about 1 MiB) until the
+// workspace.  Every GPU that loads the library holds that array (about 2 MiB) until the
 // process exits.
 #include <cuda_runtime.h>
 
@@ -22,9 +22,10 @@ int launch_gemv_tma(const __half* x, int64_t M, int64_t K, const int8_t* signs, 
                     const uint32_t* w, const __half* scales, const __half* biases, int64_t N,
                     __half* y, void* workspace, size_t ws_bytes, int32_t* status, cudaStream_t s);
 size_t gemv_fixup_bytes();
+size_t gemv_fixup_counter_bytes();
 
-// split-schedule state for up to 256 SMs: fp32 sums [256][128 rows][8 tokens] + counters [256]
-constexpr size_t kStaticScratchBytes = (size_t)256 * 128 * 8 * 4 + 256 * 4;
+// split-schedule state for up to 256 SMs: counters (1 KiB) + fp32 parts [256][2][128 rows][8 tokens]
+constexpr size_t kStaticScratchBytes = 1024 + (size_t)256 * 2 * 128 * 8 * 4;
 constexpr int64_t kNoallocMaxTokens = 8;
 
 }  // namespace tb
@@ -82,8 +83,9 @@ extern "C" int tb_packed_linear_gemv_noalloc(const uint16_t* x, int64_t M, int64
   rc = static_scratch(&scratch);
   if (rc != TB_OK) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // the array keeps whatever the previous call left: its sums and counters must start at zero
-  cudaError_t e = cudaMemsetAsync(scratch, 0, kStaticScratchBytes, s);
+  // the array keeps whatever the previous call left: its counters must start at zero (the
+  // parts behind them are written before they are read)
+  cudaError_t e = cudaMemsetAsync(scratch, 0, gemv_fixup_counter_bytes(), s);
   if (e != cudaSuccess) {
     record_cuda_error(e);
     return TB_ERR_CUDA;
