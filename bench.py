@@ -15,6 +15,7 @@ Prints ONE JSON line (rank 0).  ``--config`` picks other workloads for profiling
 from __future__ import annotations
 
 import argparse
+import datetime
 import json
 import os
 import subprocess
@@ -87,13 +88,18 @@ class Dist:
 class Clocks:
     """nvidia-smi sampling during the timed region."""
 
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, index: int):
         self.index = index
         self.proc = None
+        self.window = None
+
+    def mark(self, t0: float, t1: float):
+        """Keep only samples taken between these wall-clock times (the timed region)."""
+        self.window = (t0, t1)
 
     def start(self):
         try:
@@ -113,14 +119,21 @@ class Clocks:
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
         for line in out.strip().splitlines():
             f = [x.strip() for x in line.split(",")]
-            if len(f) < 8:
+            if len(f) < 9:
                 continue
+            if self.window is not None:
+                try:
+                    ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                except ValueError:
+                    ts = None
+                if ts is not None and not (self.window[0] <= ts <= self.window[1]):
+                    continue
             try:
-                sm.append(float(f[0]))
-                mx = float(f[1])
+                sm.append(float(f[1]))
+                mx = float(f[2])
             except ValueError:
                 continue
-            for n, v in zip(names, f[4:8]):
+            for n, v in zip(names, f[5:9]):
                 if v.lower() == "active":
                     reasons.add(n)
         return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": mx,
@@ -289,12 +302,18 @@ def run_sweep(args, dist, tb, tdev, torch):
     single_graph = capture(torch, lambda: sweep_step(tb, singles, emb, xs, signs, ys, ids, e_out, ws, status))
     launches_per_step = 1 + len(groups)
 
+    clocks = Clocks(dist.local)
+    clocks.start()
     for _ in range(args.warmup):
         step_graph.replay()
     torch.cuda.synchronize()
-    clocks = Clocks(dist.local)
-    clocks.start()
+    t_pre = time.time()
+    while time.time() - t_pre < 0.3:  # the sampler is up and the GPU busy before the timed region
+        step_graph.replay()
+        torch.cuda.synchronize()
+    w0 = time.time()
     secs = dist.max(time_graph(torch, step_graph, args.steps, dist))
+    clocks.mark(w0, time.time())
     clk = clocks.stop()
     # the dominant kernel alone: the 401 fused FWHT + GEMV launches
     for _ in range(2):
@@ -608,7 +627,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="sweep", choices=["sweep", "layers", "prefill", "batched", "embed", "all"])
