@@ -30,10 +30,13 @@ import numpy as np  # noqa: E402
 import tb_inputs as ti  # noqa: E402
 
 METRIC = "decode tok/s at 27B shapes (M=1) + fused W2 GEMV HBM GB/s as % of GB300 peak"
-# DRAM bytes per launch of the decode GEMV over its algorithmic bytes, from one ncu capture
-# (dram__bytes_read.sum + dram__bytes_write.sum) of the 5120 -> 17408 launch:
+# DRAM bytes (read + write) of one chain launch from an ncu capture, or None until taken
+CHAIN_TRAFFIC = None
+# DRAM bytes per launch of the per-call decode GEMV over its algorithmic bytes, from one ncu
+# capture (dram__bytes_read.sum + dram__bytes_write.sum) of the 5120 -> 17408 launch:
 # 25.18 MB read, 0 written, 25.07 MB algorithmic (profiles/w2_gemv_tma_lm_head.md)
 GEMV_TRAFFIC_RATIO = 25.18 / 25.07
+CHAIN_TRAFFIC_NOTE = "not captured yet for this kernel"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 
@@ -163,58 +166,85 @@ class Packed:
         return ti.packed_bytes(self.K, self.N)
 
 
-def build_sweep(tb, tdev, torch):
-    dev = torch.device("cuda")
-    tmp = torch.empty(1 << 30, dtype=torch.int8, device=dev)
-    layers = []
-    for i, (name, K, N) in enumerate(ti.sweep_layers()):
-        layers.append((name, Packed(tb, tdev, torch, ti.config_seed(3, i), N, K, tmp)))
-    emb = Packed(tb, tdev, torch, ti.config_seed(3, 999), ti.VOCAB, ti.HIDDEN, tmp)
-    del tmp
-    torch.cuda.synchronize()
-    xs = {K: torch.from_numpy(ti.activations(ti.config_seed(3, 1000 + K), 1, K)).to(dev)
-          for K in (ti.HIDDEN, 6144, ti.MLP)}
-    signs = {K: torch.from_numpy(ti.rademacher_signs(ti.config_seed(3, 2000 + K), K)).to(dev)
-             for K in (ti.HIDDEN, 6144, ti.MLP)}
-    ymax = max(p.N for _, p in layers)
-    ys = [torch.empty((1, ymax), dtype=torch.float16, device=dev) for _ in range(3)]
-    return layers, emb, xs, signs, ys
+class Stack:
+    """The synthetic 64-layer stack on the device, wired as a dependent chain of links.
+
+    Every link is one call of the layer: an input x and the 1..3 matrices of one layer that
+    read it (in_proj_qkv + in_proj_z, q + k + v, gate + up) or one matrix alone.  A link's
+    input is an earlier link's output, as in the model's decode step (the ops the model runs
+    between the linears, attention, norms and the MLP gate, are not part of this layer and
+    are left out): layer l reads h (x0 for l = 0); out_proj reads the in_proj_z output and
+    o_proj the q output, and both write h; gate + up read h; down reads the gate output and
+    writes h; lm_head reads h.  257 links per token.
+    """
+
+    def __init__(self, tb, tdev, torch):
+        dev = torch.device("cuda")
+        tmp = torch.empty(1 << 30, dtype=torch.int8, device=dev)
+        self.layers = []
+        for i, (name, K, N) in enumerate(ti.sweep_layers()):
+            self.layers.append((name, Packed(tb, tdev, torch, ti.config_seed(3, i), N, K, tmp), i))
+        self.emb = Packed(tb, tdev, torch, ti.config_seed(3, 999), ti.VOCAB, ti.HIDDEN, tmp)
+        del tmp
+        torch.cuda.synchronize()
+        H, MLPW = ti.HIDDEN, ti.MLP
+        self.x0 = torch.from_numpy(ti.activations(ti.config_seed(3, 1000), 1, H)).to(dev)
+        self.signs = {K: torch.from_numpy(ti.rademacher_signs(ti.config_seed(3, 2000 + K), K)).to(dev)
+                      for K in (H, 6144, MLPW)}
+
+        def buf(n):
+            return torch.zeros((1, n), dtype=torch.float16, device=dev)
+
+        self.h, self.qkv, self.z = buf(H), buf(10240), buf(6144)
+        self.q, self.k, self.v = buf(6144), buf(1024), buf(1024)
+        self.gate, self.up = buf(MLPW), buf(MLPW)
+        self.logits = buf(ti.VOCAB)
+        out_of = {"in_proj_qkv": self.qkv, "in_proj_z": self.z, "out_proj": self.h, "q_proj": self.q,
+                  "k_proj": self.k, "v_proj": self.v, "o_proj": self.h, "gate_proj": self.gate,
+                  "up_proj": self.up, "down_proj": self.h, "lm_head": self.logits}
+        in_of = {"out_proj": self.z, "o_proj": self.q, "down_proj": self.gate}
+        # links: (x, K, [(name, Packed, layer index, y)])
+        self.links = []
+        first, i = True, 0
+        while i < len(self.layers):
+            name = self.layers[i][0]
+            fam = next((f for f in SHARED_INPUT if name in f), None)
+            j = i + 1
+            if fam is not None:
+                while j < len(self.layers) and self.layers[j][0] in fam and self.layers[j][0] != name:
+                    j += 1
+            grp = self.layers[i:j]
+            x = in_of.get(name, self.h)
+            if first:
+                x, first = self.x0, False
+            self.links.append((x, grp[0][1].K, [(n, p, li, out_of[n]) for n, p, li in grp]))
+            i = j
+
+    def link_args(self):
+        """Arguments of every link for tb.chain_link / tb_packed_linear_multi."""
+        return [(x, self.signs[K], 1024, [(p.w, p.s, p.b) for _, p, _, _ in mats],
+                 [y[:, : p.N] for _, p, _, y in mats]) for x, K, mats in self.links]
+
+    @property
+    def algo_bytes(self):
+        return sum(p.algo_bytes for _, p, _ in self.layers)
 
 
 SHARED_INPUT = ({"in_proj_qkv", "in_proj_z"}, {"q_proj", "k_proj", "v_proj"}, {"gate_proj", "up_proj"})
 
 
-def launch_groups(layers):
-    """The 401 linears grouped into calls: modules of one layer that read the same input
-    (in_proj_qkv + in_proj_z, q + k + v, gate + up) share one call; 257 calls per token."""
-    groups, i = [], 0
-    while i < len(layers):
-        name = layers[i][0]
-        fam = next((f for f in SHARED_INPUT if name in f), None)
-        j = i + 1
-        if fam is not None:
-            while j < len(layers) and layers[j][0] in fam and layers[j][0] != name:
-                j += 1
-        groups.append([p for _, p in layers[i:j]])
-        i = j
-    return groups
-
-
-def run_linears(tb, groups, xs, signs, ys, ws, status):
-    for grp in groups:
-        K = grp[0].K
-        if len(grp) == 1:
-            p = grp[0]
-            tb.tb_packed_linear(xs[K], signs[K], 1024, p.w, p.s, p.b, ys[0][:, : p.N], ws, status)
+def run_calls(tb, link_args, ws, status):
+    """The links as one tb_packed_linear(_multi) call each, in order on the current stream."""
+    for x, sg, block, mats, ys in link_args:
+        if len(mats) == 1:
+            w, s, b = mats[0]
+            tb.tb_packed_linear(x, sg, block, w, s, b, ys[0], ws, status)
         else:
-            tb.tb_packed_linear_multi(xs[K], signs[K], 1024, [(p.w, p.s, p.b) for p in grp],
-                                      [ys[k][:, : p.N] for k, p in enumerate(grp)], ws, status)
+            tb.tb_packed_linear_multi(x, sg, block, mats, ys, ws, status)
 
 
-def sweep_step(tb, groups, emb, xs, signs, ys, ids, e_out, ws, status):
-    """One decode token: embedding lookup + the 401 fused FWHT/GEMV linears."""
-    tb.tb_embed_lookup(ids, emb.w, emb.s, emb.b, signs[ti.HIDDEN], 1024, e_out, status)
-    run_linears(tb, groups, xs, signs, ys, ws, status)
+def embed(tb, st, ids, e_out, status):
+    tb.tb_embed_lookup(ids, st.emb.w, st.emb.s, st.emb.b, st.signs[ti.HIDDEN], 1024, e_out, status)
 
 
 def time_graph(torch, graph, steps, dist):
@@ -286,70 +316,112 @@ def cpu_baseline_sample(budget_s: float = 12.0):
 
 
 def run_sweep(args, dist, tb, tdev, torch):
+    """The decode step (embedding + 257 dependent links) timed on one of two paths:
+    `chain` (one persistent tb_chain_run launch for all links) or `calls` (one launch per
+    link, replayed as a CUDA graph).  The other path is timed too and reported in config."""
     hbm, _, _, peak_kind = peaks()
-    layers, emb, xs, signs, ys = build_sweep(tb, tdev, torch)
-    groups = launch_groups(layers)
-    singles = [[p] for _, p in layers]
+    st = Stack(tb, tdev, torch)
+    links = st.link_args()
     dev = torch.device("cuda")
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     ids = torch.tensor([int(ti.token_ids(ti.config_seed(3, 3000), 1, ti.VOCAB)[0])], dtype=torch.int32,
                        device=dev)
     e_out = torch.empty((1, ti.HIDDEN), dtype=torch.float16, device=dev)
+    chain = tb.Chain(links, 1)
+    n_links = len(links)
+    step_bytes = st.algo_bytes
     ws = torch.zeros(tb.tb_packed_linear_workspace_size(1, ti.MLP, ti.HIDDEN), dtype=torch.uint8, device=dev)
+    call_graph = capture(torch, lambda: (embed(tb, st, ids, e_out, status), run_calls(tb, links, ws, status)))
+    gemv_graph = capture(torch, lambda: run_calls(tb, links, ws, status))
 
-    step_graph = capture(torch, lambda: sweep_step(tb, groups, emb, xs, signs, ys, ids, e_out, ws, status))
-    gemv_graph = capture(torch, lambda: run_linears(tb, groups, xs, signs, ys, ws, status))
-    single_graph = capture(torch, lambda: sweep_step(tb, singles, emb, xs, signs, ys, ids, e_out, ws, status))
-    launches_per_step = 1 + len(groups)
+    def chain_step():
+        embed(tb, st, ids, e_out, status)
+        chain.run(status)
+
+    def calls_step():
+        call_graph.replay()
+
+    step = chain_step if args.path == "chain" else calls_step
+
+    def time_steps(fn, steps):
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        dist.barrier()
+        torch.cuda.synchronize()
+        start.record()
+        for _ in range(steps):
+            fn()
+        end.record()
+        torch.cuda.synchronize()
+        dist.barrier()
+        return start.elapsed_time(end) / 1e3
 
     clocks = Clocks(dist.local)
     clocks.start()
     for _ in range(args.warmup):
-        step_graph.replay()
+        step()
     torch.cuda.synchronize()
     t_pre = time.time()
     while time.time() - t_pre < 0.3:  # the sampler is up and the GPU busy before the timed region
-        step_graph.replay()
+        step()
         torch.cuda.synchronize()
     w0 = time.time()
-    secs = dist.max(time_graph(torch, step_graph, args.steps, dist))
+    secs = dist.max(time_steps(step, args.steps))
     clocks.mark(w0, time.time())
     clk = clocks.stop()
-    # the dominant kernel alone: the 401 fused FWHT + GEMV launches
-    for _ in range(2):
-        gemv_graph.replay()
-    gsecs = dist.max(time_graph(torch, gemv_graph, args.steps, dist))
+    # the dominant kernel alone: the chain launch, or the 257 per-link GEMV launches
+    if args.path == "chain":
+        ksecs = dist.max(time_steps(lambda: chain.run(status), args.steps))
+        launches_per_link = 1.0 / n_links
+        kernel = ("w2_gemv_chain_kernel<1> (257 links: fused FWHT prologue + W2-g128 GEMV each), "
+                  "algorithmic bytes of the 401 matrices per launch over its CUDA-event time")
+    else:
+        for _ in range(2):
+            gemv_graph.replay()
+        ksecs = dist.max(time_steps(gemv_graph.replay, args.steps))
+        launches_per_link = 1.0
+        kernel = ("w2_gemv_tma_kernel<1> (fused FWHT prologue + W2-g128 GEMV), its 257 launches per "
+                  "token averaged")
+    other = calls_step if args.path == "chain" else chain_step
+    for _ in range(3):
+        other()
+    osecs = dist.max(time_steps(other, args.steps))
     torch.cuda.synchronize()
     assert int(status.item()) == 0, f"device status {int(status.item())}"
+    assert bool(torch.isfinite(st.logits).all()), "non-finite logits"
+    launches = n_links * launches_per_link
+    achieved = step_bytes / launches / (ksecs / (args.steps * launches)) / 1e9
 
-    for _ in range(2):
-        single_graph.replay()
-    ssecs = dist.max(time_graph(torch, single_graph, args.steps, dist))
-    gemv_bytes = sum(p.algo_bytes for _, p in layers)
-    gemv_launch_s = gsecs / (args.steps * len(groups))
-    achieved = gemv_bytes / len(groups) / gemv_launch_s / 1e9
-
-    # end to end through the public C ABI with host buffers: H2D of the token id,
-    # the 402 calls, D2H of the logits, every step
+    # end to end through the public C ABI with host buffers: H2D of the token id, the
+    # step's calls, D2H of the logits, every step (no graph)
     h_id = torch.empty(1, dtype=torch.int32).pin_memory()
     h_id[0] = int(ids[0])
     h_logits = torch.empty((1, ti.VOCAB), dtype=torch.float16).pin_memory()
-    for _ in range(2):
+
+    def e2e_step():
         ids.copy_(h_id, non_blocking=True)
-        sweep_step(tb, groups, emb, xs, signs, ys, ids, e_out, ws, status)
-        h_logits.copy_(ys[0][:, : ti.VOCAB], non_blocking=True)
+        if args.path == "chain":
+            chain_step()
+        else:
+            embed(tb, st, ids, e_out, status)
+            run_calls(tb, links, ws, status)
+        h_logits.copy_(st.logits, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
     torch.cuda.synchronize()
     dist.barrier()
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        ids.copy_(h_id, non_blocking=True)
-        sweep_step(tb, groups, emb, xs, signs, ys, ids, e_out, ws, status)
-        h_logits.copy_(ys[0][:, : ti.VOCAB], non_blocking=True)
+        e2e_step()
     torch.cuda.synchronize()
     e2e_s = dist.max(time.perf_counter() - t0)
     dist.barrier()
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
 
     n = dist.world
+    per_step = 2 if args.path == "chain" else 1 + n_links
     line = {
         "metric": METRIC,
         "value": round(n * args.steps / secs, 3),
@@ -365,13 +437,15 @@ def run_sweep(args, dist, tb, tdev, torch):
         "data": "synthetic",
         "config": {
             "workload": "decode step, M=1: embedding of 1 id + 401 fused sign*FWHT-1024 + W2-g128 "
-                        "GEMV linears of a 64-layer 27B stack (hidden 5120, MLP 17408, vocab 248320)",
-            "weights_gb_per_step": round((gemv_bytes + ti.HIDDEN // 4 + ti.HIDDEN // 32) / 1e9, 4),
+                        "linears of a 64-layer 27B stack (hidden 5120, MLP 17408, vocab 248320) as a "
+                        "dependent chain of 257 links (each link reads an earlier link's output)",
+            "weights_gb_per_step": round((step_bytes + ti.HIDDEN // 4 + ti.HIDDEN // 32) / 1e9, 4),
             "l2": "no flush: 7.06 GB of weights per step, far larger than the 129 MB L2",
-            "graph": "one CUDA graph per step",
-            "calls_per_step": launches_per_step,
-            "shared_input_calls": "in_proj_qkv+in_proj_z, q+k+v and gate+up each in one tb_packed_linear_multi call",
-            "tok_s_one_call_per_module": round(n * args.steps / ssecs, 3),
+            "path": ("chain: embedding + one persistent tb_chain_run launch per step" if args.path == "chain"
+                     else "calls: embedding + one tb_packed_linear(_multi) launch per link, one CUDA graph per step"),
+            "links_per_step": n_links,
+            "shared_input_links": "in_proj_qkv+in_proj_z, q+k+v and gate+up each one link",
+            ("tok_s_calls_path" if args.path == "chain" else "tok_s_chain_path"): round(n * args.steps / osecs, 3),
             "parallelism": f"replicas x{n}",
         },
         "roofline": {
@@ -380,9 +454,10 @@ def run_sweep(args, dist, tb, tdev, torch):
             "peak": hbm,
             "unit": "GB/s",
             "frac": round(achieved / hbm, 4),
-            "traffic": round(GEMV_TRAFFIC_RATIO * gemv_bytes / len(groups)),
-            "traffic_note": "ncu DRAM bytes of the 5120->17408 launch, scaled to the step's average launch",
-            "kernel": "w2_gemv_tma_kernel<1> (fused FWHT prologue + W2-g128 GEMV), its 257 launches per token averaged",
+            "traffic": CHAIN_TRAFFIC if args.path == "chain" else round(GEMV_TRAFFIC_RATIO * step_bytes / n_links),
+            "traffic_note": CHAIN_TRAFFIC_NOTE if args.path == "chain" else
+            "ncu DRAM bytes of the 5120->17408 launch, scaled to the step's average launch",
+            "kernel": kernel,
             "peak_kind": f"{peak_kind} hbm_gbs",
         },
         "e2e": {
@@ -390,9 +465,9 @@ def run_sweep(args, dist, tb, tdev, torch):
             "unit": "tok/s",
             "h2d_bytes_per_step": 4,
             "d2h_bytes_per_step": ti.VOCAB * 2,
-            "note": "258 C-ABI calls per step on the host, no graph",
+            "note": "C-ABI calls per step from the host: token id H2D, the step's launches, logits D2H",
         },
-        "gpu_launches": launches_per_step * args.steps,
+        "gpu_launches": per_step * args.steps,
         "clocks": clk,
     }
     if dist.rank == 0 and n == 1 and not args.no_cpu_baseline:
@@ -405,18 +480,27 @@ def run_sweep(args, dist, tb, tdev, torch):
 
 
 def profile_step(args, dist, tb, tdev, torch):
-    """One eager decode step (embedding + 257 calls) after a warm-up step, nothing timed."""
-    layers, emb, xs, signs, ys = build_sweep(tb, tdev, torch)
-    groups = launch_groups(layers)
+    """Two decode steps (embedding + chain run) after building the stack, nothing timed; with
+    --per-call the 257 links run as one launch each instead of one chain launch."""
+    st = Stack(tb, tdev, torch)
+    links = st.link_args()
     dev = torch.device("cuda")
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     ids = torch.tensor([7], dtype=torch.int32, device=dev)
     e_out = torch.empty((1, ti.HIDDEN), dtype=torch.float16, device=dev)
-    ws = torch.zeros(tb.tb_packed_linear_workspace_size(1, ti.MLP, ti.HIDDEN), dtype=torch.uint8, device=dev)
-    for _ in range(2):
-        sweep_step(tb, groups, emb, xs, signs, ys, ids, e_out, ws, status)
+    if args.per_call:
+        ws = torch.zeros(tb.tb_packed_linear_workspace_size(1, ti.MLP, ti.HIDDEN), dtype=torch.uint8,
+                         device=dev)
+        for _ in range(2):
+            embed(tb, st, ids, e_out, status)
+            run_calls(tb, links, ws, status)
+    else:
+        chain = tb.Chain(links, 1)
+        for _ in range(2):
+            embed(tb, st, ids, e_out, status)
+            chain.run(status)
     torch.cuda.synchronize()
-    return {"profile_step": "done", "calls_per_step": 1 + len(groups), "status": int(status.item())}
+    return {"profile_step": "done", "links": len(links), "status": int(status.item())}
 
 
 def profile_linear(args, dist, tb, tdev, torch):
@@ -633,7 +717,11 @@ def main():
     ap.add_argument("--config", default="sweep", choices=["sweep", "layers", "prefill", "batched", "embed", "all"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-step", action="store_true",
-                    help="build the decode sweep, run one eager step and exit (for an ncu launch list)")
+                    help="build the decode stack, run two steps and exit (for an ncu launch list)")
+    ap.add_argument("--path", default="calls", choices=["chain", "calls"],
+                    help="decode step path timed for `value` (the other one is reported in config)")
+    ap.add_argument("--per-call", action="store_true",
+                    help="with --profile-step: one launch per link instead of the chain launch")
     ap.add_argument("--profile-linear", type=int, nargs=4, metavar=("K", "N", "M", "ALGO"),
                     help="one packed K->N matrix, four tb_packed_linear calls on M tokens (for ncu)")
     args = ap.parse_args()

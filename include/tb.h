@@ -55,13 +55,14 @@ enum {
   TB_ERR_CUDA = -5,        /* a CUDA launch or query failed (see tb_last_cuda_error) */
   TB_ERR_ALIGN = -6,       /* a device pointer is not 16-byte aligned */
   TB_ERR_WORKSPACE = -7,   /* workspace NULL or smaller than the size query returned */
-  TB_ERR_TOO_LARGE = -8    /* beyond what the fixed scratch of tb_packed_linear_gemv_noalloc holds */
+  TB_ERR_TOO_LARGE = -8    /* beyond a fixed limit: the no-allocation scratch, or the chain's M <= 8 and SM ring */
 };
 
 /* bits OR-ed into *dev_status by kernels */
 #define TB_DEV_BAD_CODE 1  /* tb_pack_w2: a code outside {-1,0,1} */
 #define TB_DEV_BAD_ID 2    /* tb_embed_lookup: an id outside [0, V) (its row is written as zeros) */
 #define TB_DEV_TIMEOUT 4   /* a bounded wait inside a kernel gave up; outputs are not valid */
+#define TB_DEV_BAD_PLAN 8  /* tb_chain_run: the plan does not match the launch (nothing computed) */
 
 /* algorithm choice for tb_packed_linear_algo */
 #define TB_ALGO_AUTO 0     /* GEMV for M <= 8, tensor-core GEMM above */
@@ -170,6 +171,67 @@ int tb_packed_linear_multi(const uint16_t* x, int64_t M, int64_t K, const int8_t
                            const uint16_t* const* biases, const int64_t* N, uint16_t* const* y,
                            void* workspace, size_t workspace_bytes, int32_t* dev_status,
                            void* stream);
+
+/*
+ * Chained decode: a sequence of Packed linears (M <= 8 tokens) in one persistent launch.
+ * [ARCH] "Hadamard 旋转": each linear is Packed.__call__ (fwht of its input, then the W2-g128
+ * matmul); a decode step runs the model's linears one after another, every one reading what
+ * an earlier one wrote.  [PACK] "文本模型加载": the modules and their packed tensors.
+ *
+ * Link i computes, for its input x and its n matrices (1..4, the modules that read the same
+ * input), exactly what tb_packed_linear_multi computes.  The result of the whole chain equals
+ * calling tb_packed_linear_multi once per link, in order, on one stream: link i reads x only
+ * after every output of links 0..i-1 is complete, so x of a link may be (a slice of) any
+ * earlier link's y.  The launch keeps one CTA per SM resident (a cooperative launch); while
+ * the SMs wait for link i to complete, they already stream the packed weights of link i+1.
+ */
+typedef struct tb_chain_link {
+  const uint16_t* x;          /* fp16 [M, K]; may be an output of an earlier link */
+  const int8_t* signs;        /* int8 [K] (+-1) or NULL (all +1); ignored when block = 0 */
+  int64_t K;                  /* positive multiple of 1024 (at most 2^20) */
+  int32_t block;              /* 1024, or 0 = module not folded */
+  int32_t n;                  /* matrices reading x: 1..4 */
+  const uint32_t* w[4];       /* uint32 [N[i], K/16] packed codes */
+  const uint16_t* scales[4];  /* fp16 [N[i], K/128] */
+  const uint16_t* biases[4];  /* fp16 [N[i], K/128] */
+  int64_t N[4];               /* rows of matrix i, >= 1 */
+  uint16_t* y[4];             /* fp16 [M, N[i]] (out) */
+} tb_chain_link;
+
+/* Bytes of device memory a plan of n_links links needs (an upper bound: 4 matrices per link). */
+size_t tb_chain_plan_size(int n_links);
+
+/*
+ * tb_chain_plan — validate the links (same rules as tb_packed_linear_multi; M in 1..8) and
+ * write the plan (link table + one TMA descriptor per matrix) to `plan`, device memory of at
+ * least tb_chain_plan_size(n_links) bytes, 128-byte aligned, owned by the caller.  Copies the
+ * plan on `stream` and waits for that copy (call it before any stream capture).  The plan
+ * stays valid while every pointer in the links stays valid; it holds no other state.
+ * Errors: TB_ERR_NULL, TB_ERR_SHAPE, TB_ERR_UNSUPPORTED, TB_ERR_ALIGN, TB_ERR_TOO_LARGE (M > 8),
+ * TB_ERR_WORKSPACE (plan_bytes too small), TB_ERR_CUDA.
+ */
+int tb_chain_plan(const tb_chain_link* links, int n_links, int64_t M, void* plan,
+                  size_t plan_bytes, void* stream);
+
+/*
+ * Bytes of workspace tb_chain_run uses (about 2 MB): counters in its first 1280 bytes, which
+ * must be zero before the first run (zero-filling the whole workspace will do) and which every
+ * completed run leaves zero (a run that reported TB_DEV_TIMEOUT may not: zero them again),
+ * then per-SM fp32 parts of output tiles shared by several SMs (scratch).
+ */
+size_t tb_chain_workspace_size(void);
+
+/*
+ * tb_chain_run — run a plan: one launch on `stream`, asynchronous.  n_links, M and max_K
+ * (the largest K of the links) must be the values the plan was made with; a mismatch that
+ * the device can see sets TB_DEV_BAD_PLAN and computes nothing.  Runs that share one
+ * workspace must be ordered on one stream.  Errors: TB_ERR_NULL, TB_ERR_SHAPE, TB_ERR_ALIGN,
+ * TB_ERR_WORKSPACE, TB_ERR_TOO_LARGE (more than 256 SMs, or M and max_K leave no room for
+ * the weight ring in shared memory), TB_ERR_CUDA.  dev_status optional (TB_DEV_TIMEOUT,
+ * TB_DEV_BAD_PLAN).
+ */
+int tb_chain_run(const void* plan, int n_links, int64_t M, int64_t max_K, void* workspace,
+                 size_t workspace_bytes, int32_t* dev_status, void* stream);
 
 /*
  * tb_embed_lookup — Packed.__call__ on the embedding path.

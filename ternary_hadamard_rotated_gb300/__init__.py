@@ -7,7 +7,8 @@ on the current torch stream unless a stream is given.  There is no CPU path:
 if the library is not built, importing the calls raises.
 
 Names follow the C ABI: ``tb_pack_w2``, ``tb_unpack_w2``, ``tb_fwht``,
-``tb_packed_linear``, ``tb_packed_linear_multi``, ``tb_embed_lookup``.
+``tb_packed_linear``, ``tb_packed_linear_multi``, ``tb_embed_lookup``, and the chained decode
+``tb_chain_plan`` / ``tb_chain_run`` (``ChainLink`` mirrors ``tb_chain_link``).
 """
 from __future__ import annotations
 
@@ -30,6 +31,7 @@ TB_ERR_TOO_LARGE = -8
 TB_DEV_BAD_CODE = 1
 TB_DEV_BAD_ID = 2
 TB_DEV_TIMEOUT = 4
+TB_DEV_BAD_PLAN = 8
 
 TB_ALGO_AUTO = 0
 TB_ALGO_GEMV = 1
@@ -58,6 +60,10 @@ _SIGNATURES = {
     "tb_packed_linear_gemv_noalloc": (_INT, [_P, _I64, _I64, _P, _INT, _P, _P, _P, _I64, _P, _P, _P]),
     "tb_packed_linear_multi": (_INT, [_P, _I64, _I64, _P, _INT, _INT, _P, _P, _P, _P, _P, _P, _SZ, _P,
                                       _P]),
+    "tb_chain_plan_size": (_SZ, [_INT]),
+    "tb_chain_workspace_size": (_SZ, []),
+    "tb_chain_plan": (_INT, [_P, _INT, _I64, _P, _SZ, _P]),
+    "tb_chain_run": (_INT, [_P, _INT, _I64, _I64, _P, _SZ, _P, _P]),
 }
 
 EXPORTED = tuple(_SIGNATURES)
@@ -180,3 +186,91 @@ def tb_packed_linear_gemv_noalloc(x, signs, block, w, scales, biases, y, dev_sta
            load().tb_packed_linear_gemv_noalloc(_ptr(x), M, K, _ptr(signs), block, _ptr(w),
                                                 _ptr(scales), _ptr(biases), N, _ptr(y),
                                                 _ptr(dev_status), _stream(stream)))
+
+
+class ChainLink(ctypes.Structure):
+    """ctypes image of ``tb_chain_link`` (include/tb.h)."""
+
+    _fields_ = [
+        ("x", ctypes.c_void_p),
+        ("signs", ctypes.c_void_p),
+        ("K", ctypes.c_int64),
+        ("block", ctypes.c_int32),
+        ("n", ctypes.c_int32),
+        ("w", ctypes.c_void_p * 4),
+        ("scales", ctypes.c_void_p * 4),
+        ("biases", ctypes.c_void_p * 4),
+        ("N", ctypes.c_int64 * 4),
+        ("y", ctypes.c_void_p * 4),
+    ]
+
+
+def chain_link(x, signs, block, mats, ys):
+    """One link: input x [M, K] (a tensor or a view of an earlier link's output), up to four
+    (w, scales, biases) matrices reading it and their outputs ys [M, N_i]."""
+    n = len(mats)
+    if not 1 <= n <= 4 or len(ys) != n:
+        raise ValueError("a chain link holds 1..4 matrices with one output each")
+    lk = ChainLink()
+    lk.x = _ptr(x)
+    lk.signs = _ptr(signs)
+    lk.K = int(x.shape[-1])
+    lk.block = int(block)
+    lk.n = n
+    for i, ((w, sc, bi), y) in enumerate(zip(mats, ys)):
+        lk.w[i] = _ptr(w)
+        lk.scales[i] = _ptr(sc)
+        lk.biases[i] = _ptr(bi)
+        lk.N[i] = int(y.shape[-1])
+        lk.y[i] = _ptr(y)
+    return lk
+
+
+def tb_chain_plan_size(n_links):
+    return load().tb_chain_plan_size(n_links)
+
+
+def tb_chain_workspace_size():
+    return load().tb_chain_workspace_size()
+
+
+def tb_chain_plan(links, M, plan, stream=None):
+    """Write the plan of ``links`` (ChainLink list) for M tokens into the device buffer ``plan``."""
+    n = len(links)
+    arr = (ChainLink * n)(*links)
+    nbytes = plan.numel() * plan.element_size()
+    _check("tb_chain_plan", load().tb_chain_plan(ctypes.cast(arr, ctypes.c_void_p), n, M, _ptr(plan), nbytes,
+                                                 _stream(stream)))
+
+
+def tb_chain_run(plan, n_links, M, max_K, workspace, dev_status=None, stream=None):
+    """Run a plan made by tb_chain_plan: one persistent launch for all its links."""
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check("tb_chain_run", load().tb_chain_run(_ptr(plan), n_links, M, max_K, _ptr(workspace), ws_bytes,
+                                               _ptr(dev_status), _stream(stream)))
+
+
+class Chain:
+    """A planned chain of packed linears on the current device.
+
+    ``links``: sequence of (x, signs, block, mats, ys) as for :func:`chain_link`.  Holds the
+    device plan (made once, here) and a zeroed workspace; ``run()`` launches the whole chain.
+    """
+
+    def __init__(self, links, M, device=None):
+        import torch
+
+        dev = torch.device("cuda") if device is None else device
+        self.links = [chain_link(*lk) for lk in links]
+        self.n = len(self.links)
+        self.M = int(M)
+        self.max_K = max(int(lk.K) for lk in self.links)
+        nbytes = tb_chain_plan_size(self.n)
+        self.plan = torch.empty(nbytes + 128, dtype=torch.uint8, device=dev)
+        off = (-self.plan.data_ptr()) % 128
+        self.plan = self.plan[off: off + nbytes]
+        self.workspace = torch.zeros(tb_chain_workspace_size(), dtype=torch.uint8, device=dev)
+        tb_chain_plan(self.links, self.M, self.plan)
+
+    def run(self, dev_status=None, stream=None):
+        tb_chain_run(self.plan, self.n, self.M, self.max_K, self.workspace, dev_status, stream)

@@ -1,0 +1,666 @@
+// Chained decode: a sequence of Packed linears (M <= 8 tokens) in one persistent launch.
+//
+// [ARCH] kwkr.cn/news/564617, section "Hadamard 旋转把量化误差抹平的免费午餐": every linear of
+// the stack is Packed.__call__ = fwht(x, block, signs) followed by the W2-g128 matmul; a decode
+// step runs them one after another, each reading what the ones before it wrote.  [PACK]
+// lpnh.cn/news/2438023, section "文本模型加载artifact.load_model 与 Packed 模块": the modules
+// and their packed tensors.
+//
+// Link i of the chain is what tb_packed_linear_multi does for one input x_i and up to four
+// matrices that read it.  Link i + 1 may read the outputs of link i (or of any earlier link):
+// the consumers of every CTA read x_{i+1} only after all CTAs have counted link i complete on
+// a device-wide counter (release by each CTA after its outputs of link i are written, acquire
+// before the prologue of link i + 1), which is the ordering a stream gives between launches.
+//
+// What the chain saves over one launch per link is the boundary between launches: the
+// producer warp of each CTA streams the packed weights of link i + 1 into its ring while the
+// consumers still finish link i, wait for the other CTAs and transform x_{i+1}; the weights
+// never depend on the activations.  Per link the work is the same as in the per-call decode
+// GEMV: the units (128 rows x 512 k, one 16 KB TMA box) of all row tiles of the link are cut
+// into one equal contiguous range per CTA and each range into three sub-ranges, one per group
+// of four consumer warps; tiles cut by a group boundary are summed in shared memory, tiles cut
+// by a CTA boundary through per-CTA fp32 parts in the workspace, added in CTA order by the
+// last contributor.
+//
+// The plan (tb_chain_plan) holds, in device memory written once by the host: a header, one
+// CUtensorMap per matrix (the TMA descriptor of its codes, read by the copies straight from
+// global memory) and one ChainLink per link.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <string.h>
+
+#include <vector>
+
+#include "tb_common.cuh"
+#include "tb_gemv_core.cuh"
+#include "tb_host.h"
+
+namespace tb {
+
+int code_map(const uint32_t* w, int64_t N, int64_t K, CUtensorMap* out);
+
+constexpr uint32_t kChainMagic = 0x54424348u;  // "TBCH"
+constexpr int kChainMaxCtas = 256;                // parts slots of the fixup region
+constexpr int64_t kChainMaxTokens = 8;
+constexpr int64_t kChainMaxK = 1 << 20;
+
+struct ChainLink {
+  const __half* x;                // [Mc, K]
+  const int8_t* signs;            // [K] or null
+  const __half* scales[kMaxMats];  // [N_i, G]
+  const __half* biases[kMaxMats];
+  __half* y[kMaxMats];            // [Mc, N_i]
+  int N[kMaxMats];
+  int tile0[kMaxMats + 1];        // first 128-row tile of matrix i in the link's tile list
+  int nmat, K, G, C, rotate, n_tiles, map0, pad;
+};
+
+struct ChainHeader {
+  uint32_t magic;
+  int32_t n_links, M, max_K;
+  int64_t maps_off, links_off, bytes;
+  int64_t pad[3];
+};
+static_assert(sizeof(ChainHeader) == 64, "header size");
+
+// Workspace: [fixup counters, 1 KiB][link counter, CTA exit counter, 256 B]
+//            [per-CTA fp32 parts of shared tiles: kChainMaxCtas x 2 x 128 rows x 8 tokens]
+constexpr size_t kChainCounterBytes = 1024;
+constexpr size_t kChainSyncBytes = 256;
+constexpr size_t kChainPartBytes = (size_t)kChainMaxCtas * 2 * kUnitRows * 8 * 4;
+size_t chain_workspace_bytes() { return kChainCounterBytes + kChainSyncBytes + kChainPartBytes; }
+
+struct ChainRun {
+  const CUtensorMap* maps;
+  const ChainHeader* header;
+  int n_links, Mc, max_K, dw;
+  int* ws_count;       // [kChainMaxCtas] contributions per shared tile (zero between links)
+  uint32_t* sync;      // [0] links completed, summed over CTAs; [1] CTAs finished
+  float* ws_partial;   // [kChainMaxCtas][2][128][MT]
+  int32_t* status;
+};
+
+TB_DEVI int link_mat_of(const int (&tile0)[kMaxMats + 1], int nmat, int tile) {
+  int i = 0;
+#pragma unroll
+  for (int k = 1; k < kMaxMats; ++k) i += (k < nmat && tile >= tile0[k]);
+  return i;
+}
+
+// same, reading the link's tile table from the plan (used only when a tile starts or ends)
+TB_DEVI int link_mat_of_g(const ChainLink* lk, int tile, int& tile0_of) {
+  const int nmat = __ldg(&lk->nmat);
+  int i = 0;
+#pragma unroll
+  for (int k = 1; k < kMaxMats; ++k) i += (k < nmat && tile >= __ldg(&lk->tile0[k]));
+  tile0_of = __ldg(&lk->tile0[i]);
+  return i;
+}
+
+// This CTA's unit range [lo, hi) of a link with n_tiles row tiles of C units each, and the
+// group boundaries in it.  With at least one unit per CTA the units are cut into equal ranges
+// (stream-K; no range is empty, so every CTA between the first and the last owner of a tile
+// contributes to it); with fewer, every tile goes whole to one CTA and the other CTAs idle.
+struct LinkRange {
+  int lo, hi, bnd1, bnd2;
+};
+TB_DEVI LinkRange link_range(int n_tiles, int C) {
+  LinkRange r;
+  const int S = n_tiles * C;
+  if (S >= (int)gridDim.x) {
+    r.lo = (int)((int64_t)S * blockIdx.x / gridDim.x);
+    r.hi = (int)((int64_t)S * (blockIdx.x + 1) / gridDim.x);
+  } else {
+    r.lo = C * (int)((int64_t)n_tiles * blockIdx.x / gridDim.x);
+    r.hi = C * (int)((int64_t)n_tiles * (blockIdx.x + 1) / gridDim.x);
+  }
+  const int nst = r.hi - r.lo;
+  r.bnd1 = r.lo + nst / 3;
+  r.bnd2 = r.lo + (2 * nst) / 3;
+  return r;
+}
+TB_DEVI void link_group_range(const LinkRange& r, int u, int& glo, int& ghi) {
+  glo = u == 0 ? r.lo : u == 1 ? r.bnd1 : r.bnd2;
+  ghi = u == 0 ? r.bnd1 : u == 1 ? r.bnd2 : r.hi;
+}
+
+template <int MT>
+__global__ void __launch_bounds__(kTmaThreads, 1) w2_gemv_chain_kernel(const __grid_constant__ ChainRun a) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int DW = a.dw;
+  const GemvTmaLayout L = gemv_tma_layout<MT>(a.max_K / kGroup, DW);
+  const uint32_t slots_u32 = smem_u32(smem + L.codes);
+  __half* img = reinterpret_cast<__half*>(smem + L.img);
+  float2* cs = reinterpret_cast<float2*>(smem + L.cs);
+  float* accs = reinterpret_cast<float*>(smem + L.accs);  // [kCutSlots][128][MT]
+  int* cnt = reinterpret_cast<int*>(smem + L.cnt);         // [kCutSlots]
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
+  uint64_t* empty = full + kGroupsOfWarps * DW;
+  __shared__ volatile int aborted;
+
+  // a plan that does not match the launch: every CTA returns before any wait
+  const ChainHeader* hdr = a.header;
+  if (hdr->magic != kChainMagic || hdr->n_links != a.n_links || hdr->M != a.Mc || hdr->max_K > a.max_K) {
+    if (threadIdx.x == 0 && blockIdx.x == 0) set_status(a.status, TB_DEV_BAD_PLAN);
+    return;
+  }
+  const ChainLink* links =
+      reinterpret_cast<const ChainLink*>(reinterpret_cast<const uint8_t*>(hdr) + hdr->links_off);
+
+  if (threadIdx.x == 0) {
+    aborted = 0;
+    for (int i = 0; i < kGroupsOfWarps * DW; ++i) {
+      mbar_init(full + i, 1);
+      mbar_init(empty + i, kWarpsPerUnit);
+    }
+    fence_barrier_init();
+  }
+  for (int i = threadIdx.x; i < kCutSlots * kUnitRows * MT; i += blockDim.x) accs[i] = 0.f;
+  if (threadIdx.x < kCutSlots) cnt[threadIdx.x] = 0;
+  __syncthreads();
+
+  auto wait = [&](uint64_t* bar, uint32_t parity) {
+    if (aborted) return;
+    if (!mbar_wait(bar, parity)) {
+      aborted = 1;
+      set_status(a.status, TB_DEV_TIMEOUT);
+    }
+  };
+
+  if (warp == kTmaConsumers) {
+    // ---- producer: streams the codes of every link in order; never waits for a link's input
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      int si[kGroupsOfWarps] = {0, 0, 0};  // ring position (fill index % DW) of each group
+      int kf[kGroupsOfWarps] = {0, 0, 0};  // fills of that slot so far (fill index / DW)
+      for (int li = 0; li < a.n_links; ++li) {
+        const ChainLink* lk = links + li;
+        const int C = lk->C, nmat = lk->nmat;
+        int tile0[kMaxMats + 1];
+#pragma unroll
+        for (int k = 0; k <= kMaxMats; ++k) tile0[k] = lk->tile0[k];
+        const CUtensorMap* maps = a.maps + lk->map0;
+        const LinkRange r = link_range(lk->n_tiles, C);
+        int tl[kGroupsOfWarps], ch[kGroupsOfWarps], cntu[kGroupsOfWarps];
+        int maxcnt = 0;
+#pragma unroll
+        for (int u = 0; u < kGroupsOfWarps; ++u) {
+          int glo, ghi;
+          link_group_range(r, u, glo, ghi);
+          cntu[u] = ghi - glo;
+          const int first = u == kGroupsOfWarps - 1 ? ghi - 1 : glo;
+          tl[u] = cntu[u] > 0 ? first / C : 0;
+          ch[u] = cntu[u] > 0 ? first - tl[u] * C : 0;
+          maxcnt = cntu[u] > maxcnt ? cntu[u] : maxcnt;
+        }
+        for (int n = 0; n < maxcnt; ++n) {
+#pragma unroll
+          for (int u = 0; u < kGroupsOfWarps; ++u) {
+            if (n >= cntu[u]) continue;
+            const int slot = u * DW + si[u];
+            if (kf[u] > 0) wait(empty + slot, (kf[u] - 1) & 1);
+            const int mi = link_mat_of(tile0, nmat, tl[u]);
+            const int row = (tl[u] - tile0[mi]) * kUnitRows;
+            mbar_arrive_expect_tx(full + slot, kSlotBytes);
+            tma2d(slots_u32 + slot * kSlotBytes, maps + mi, ch[u] * 32, row, full + slot, pol);
+            step_unit(tl[u], ch[u], C, u == kGroupsOfWarps - 1);
+            if (++si[u] == DW) {
+              si[u] = 0;
+              ++kf[u];
+            }
+          }
+        }
+      }
+      // leave no copy in flight: wait (bounded, even after a timeout) for the last fill of
+      // every slot that was filled
+#pragma unroll
+      for (int u = 0; u < kGroupsOfWarps; ++u) {
+        const int total = kf[u] * DW + si[u];
+        for (int n = total - 1; n >= 0 && n >= total - DW; --n)
+          if (!mbar_wait(full + u * DW + n % DW, (n / DW) & 1)) set_status(a.status, TB_DEV_TIMEOUT);
+      }
+    }
+    __syncwarp();
+    return;
+  }
+
+  // ---- consumers ----
+  const int g = lane >> 2, t = lane & 3;
+  const int ug = warp / kWarpsPerUnit, wi = warp % kWarpsPerUnit;
+  const bool back = ug == kGroupsOfWarps - 1;
+  const int rA = 2 * (g & 3) + (g >> 2);  // mma row g <-> unit row 32*wi + 16*j + rA (and + 8)
+  const int R0 = 32 * wi + rA;
+  const int tokc = g < MT ? g : 0;
+  const uint32_t imgt = smem_u32(img) + tokc * 64 + t * 16;
+  const uint32_t csa = smem_u32(cs);
+  const uint32_t accs_u32 = smem_u32(accs);
+  const int t0 = min(2 * t, MT - 1), t1 = min(2 * t + 1, MT - 1);
+  const uint32_t ss = smem_u32(smem + L.sstage) + warp * kScaleStageBytes;
+  const int Mc = a.Mc;
+  int si = 0;       // ring slot of the group's next unit within its DW slots
+  uint32_t ph = 0;  // its fill parity
+
+  for (int li = 0; li < a.n_links; ++li) {
+    const ChainLink* lk = links + li;
+    const int C = lk->C, G = lk->G, K = lk->K;
+    const int S = lk->n_tiles * C;
+    const LinkRange r = link_range(lk->n_tiles, C);
+    int glo, ghi;
+    link_group_range(r, ug, glo, ghi);
+    const int ncnt = ghi - glo;
+    int tile = 0, chunk = 0;
+    if (ncnt > 0) {
+      const int first = back ? ghi - 1 : glo;
+      tile = first / C;
+      chunk = first - tile * C;
+    }
+    // scale / bias prefetch (rows 32*wi + lane of a unit), two units ahead of the one computed
+    int ptile = tile, pchunk = chunk, pn = 0, prow_tile = -1;
+    const __half* psrow = nullptr;
+    const __half* pbrow = nullptr;
+    auto load_sb = [&](uint2& sv, uint2& bv) {
+      sv = make_uint2(0, 0);
+      bv = make_uint2(0, 0);
+      if (pn < ncnt) {
+        if (ptile != prow_tile) {
+          prow_tile = ptile;
+          int t0m;
+          const int mi = link_mat_of_g(lk, ptile, t0m);
+          const int row = (ptile - t0m) * kUnitRows + 32 * wi + lane;
+          const bool in = row < lk->N[mi];
+          psrow = in ? lk->scales[mi] + (int64_t)row * G : nullptr;
+          pbrow = in ? lk->biases[mi] + (int64_t)row * G : nullptr;
+        }
+        if (psrow) {
+          sv = __ldg(reinterpret_cast<const uint2*>(psrow + pchunk * kUnitGroups));
+          bv = __ldg(reinterpret_cast<const uint2*>(pbrow + pchunk * kUnitGroups));
+        }
+      }
+      ++pn;
+      step_unit(ptile, pchunk, C, back);
+    };
+    uint2 sA, bA, sB, bB;
+    load_sb(sA, bA);
+    load_sb(sB, bB);
+
+    // x of this link may be an output of the previous one: wait until every CTA has
+    // counted that link complete
+    if (li > 0) {
+      if (threadIdx.x == 0 && !aborted) {
+        const uint32_t target = (uint32_t)li * gridDim.x;
+        if (ld_acquire_gpu(a.sync) < target) {
+          const uint64_t t_0 = globaltimer_ns();
+          while (ld_acquire_gpu(a.sync) < target) {
+            if (globaltimer_ns() - t_0 > TB_WAIT_NS) {
+              aborted = 1;
+              set_status(a.status, TB_DEV_TIMEOUT);
+              break;
+            }
+          }
+        }
+      }
+      asm volatile("bar.sync 1, %0;" ::"n"(kTmaConsumers * 32) : "memory");
+    }
+    {
+      int b1, e1, b2, e2;
+      blocks_needed(r.lo, r.hi - r.lo, C, K, b1, e1, b2, e2);
+      prologue_image<MT>(lk->x, lk->signs, K, Mc, lk->rotate, b1, e1, b2, e2, warp, kTmaConsumers,
+                         lane, img, cs);
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(kTmaConsumers * 32) : "memory");
+
+    // Add this warp's sums of tile T (all of the group's units of T) to wherever T is finished.
+    auto flush = [&](int T, float (&acc)[2][4]) {
+      int t0m;
+      const int mi = link_mat_of_g(lk, T, t0m);
+      const int N = lk->N[mi], row0 = (T - t0m) * kUnitRows;
+      __half* yo = lk->y[mi];
+      const int tb = T * C, te = tb + C;
+      if (tb >= glo && te <= ghi) {  // the whole tile is this group's: these 32 rows are final
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const int ra = row0 + R0 + 16 * j, rb = ra + 8;
+          if (2 * t < Mc) {
+            if (ra < N) yo[(int64_t)(2 * t) * N + ra] = __float2half_rn(acc[j][0]);
+            if (rb < N) yo[(int64_t)(2 * t) * N + rb] = __float2half_rn(acc[j][2]);
+          }
+          if (2 * t + 1 < Mc) {
+            if (ra < N) yo[(int64_t)(2 * t + 1) * N + ra] = __float2half_rn(acc[j][1]);
+            if (rb < N) yo[(int64_t)(2 * t + 1) * N + rb] = __float2half_rn(acc[j][3]);
+          }
+        }
+        return;
+      }
+      // a tile cut by a boundary: its shared slot is the first boundary that falls in it
+      const int b = (r.lo / C == T) ? 0 : (r.bnd1 / C == T) ? 1 : (r.bnd2 / C == T) ? 2 : 3;
+      int groups = 0;  // contributions expected in this CTA: 4 warps of every group meeting T
+#pragma unroll
+      for (int u = 0; u < kGroupsOfWarps; ++u) {
+        int ulo, uhi;
+        link_group_range(r, u, ulo, uhi);
+        groups += (ulo < uhi && ulo < te && uhi > tb);
+      }
+      const uint32_t atu = accs_u32 + b * kUnitRows * MT * 4;
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int ra = R0 + 16 * j, rb = ra + 8;
+        if (2 * t < MT) {
+          red_shared_add(atu + (ra * MT + 2 * t) * 4, acc[j][0]);
+          red_shared_add(atu + (rb * MT + 2 * t) * 4, acc[j][2]);
+        }
+        if (2 * t + 1 < MT) {
+          red_shared_add(atu + (ra * MT + 2 * t + 1) * 4, acc[j][1]);
+          red_shared_add(atu + (rb * MT + 2 * t + 1) * 4, acc[j][3]);
+        }
+      }
+      __syncwarp();
+      int last = 0;
+      if (lane == 0) {
+        __threadfence_block();
+        last = atomicAdd(cnt + b, 1) == groups * kWarpsPerUnit - 1;
+      }
+      last = __shfl_sync(0xffffffffu, last, 0);
+      if (!last) return;
+      // this warp finishes the tile for this CTA, and returns the slot to zero for the next link
+      __threadfence_block();
+      float* at = accs + b * kUnitRows * MT;
+      if (lane == 0) cnt[b] = 0;
+      if (tb >= r.lo && te <= r.hi) {
+        for (int e = lane; e < kUnitRows * MT; e += 32) {
+          const int r_ = e / MT, k_ = e - r_ * MT;
+          if (row0 + r_ < N && k_ < Mc) yo[(int64_t)k_ * N + row0 + r_] = __float2half_rn(at[e]);
+          at[e] = 0.f;
+        }
+        return;
+      }
+      // shared with other CTAs: this CTA's part to its own workspace slot (slot 0 for the tile
+      // of its first unit, 1 for the tile of its last)
+      float* mine = a.ws_partial + ((int64_t)blockIdx.x * 2 + (r.lo / C == T ? 0 : 1)) * kUnitRows * MT;
+      for (int e = lane; e < kUnitRows * MT; e += 32) {
+        __stcg(mine + e, at[e]);
+        at[e] = 0.f;
+      }
+      __syncwarp();
+      // the last of the tile's CTAs to count in adds the parts in CTA order and returns the
+      // counter to zero
+      const int first = stage_owner(tb, S, gridDim.x);
+      const int lastc = stage_owner(te - 1, S, gridDim.x);
+      int fin = 0;
+      if (lane == 0) {
+        fence_acq_rel_gpu();
+        fin = atomicAdd(a.ws_count + first, 1) == lastc - first;
+      }
+      fin = __shfl_sync(0xffffffffu, fin, 0);
+      if (!fin) return;
+      fence_acq_rel_gpu();
+      int flo, fhi;
+      cta_range_of(first, gridDim.x, lk->n_tiles, C, flo, fhi);
+      const float* p0 = a.ws_partial + ((int64_t)first * 2 + (flo / C == T ? 0 : 1)) * kUnitRows * MT;
+      for (int eb = 0; eb < kUnitRows * MT; eb += 128) {
+        float v[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int c = first; c <= lastc; c += 4) {
+          float l[4][4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int cc = c + q;
+            const float* pc = cc == first ? p0 : a.ws_partial + (int64_t)cc * 2 * kUnitRows * MT;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) l[q][k] = cc <= lastc ? __ldcg(pc + eb + lane + 32 * k) : 0.f;
+          }
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) v[k] += l[q][k];
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int e = eb + lane + 32 * k;
+          const int r_ = e / MT, k_ = e - r_ * MT;
+          if (row0 + r_ < N && k_ < Mc) yo[(int64_t)k_ * N + row0 + r_] = __float2half_rn(v[k]);
+        }
+      }
+      if (lane == 0) a.ws_count[first] = 0;
+    };
+
+    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    auto body = [&](int n, uint2& sv, uint2& bv) {
+      {
+        const uint32_t rr = ss + lane * kUnitGroups * 8;
+        const float2 sf0 = __half22float2(*reinterpret_cast<const __half2*>(&sv.x));
+        const float2 sf1 = __half22float2(*reinterpret_cast<const __half2*>(&sv.y));
+        const float2 bf0 = __half22float2(*reinterpret_cast<const __half2*>(&bv.x));
+        const float2 bf1 = __half22float2(*reinterpret_cast<const __half2*>(&bv.y));
+        asm volatile("st.shared.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(rr), "f"(sf0.x), "f"(bf0.x), "f"(sf0.y), "f"(bf0.y) : "memory");
+        asm volatile("st.shared.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(rr + 16), "f"(sf1.x), "f"(bf1.x), "f"(sf1.y), "f"(bf1.y) : "memory");
+        __syncwarp();
+      }
+      const int slot = ug * DW + si;
+      wait(full + slot, ph);
+      if (++si == DW) {
+        si = 0;
+        ph ^= 1;
+      }
+      const uint32_t box = slots_u32 + slot * kSlotBytes;
+#pragma unroll
+      for (int gi = 0; gi < kUnitGroups; ++gi)
+        unit_group<MT>(box, R0, t, gi, chunk * kUnitGroups + gi, imgt, ss, rA, csa, t0, t1, acc);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty + slot);
+      load_sb(sv, bv);
+      const int cur = tile;
+      step_unit(tile, chunk, C, back);
+      if (tile != cur || n == ncnt - 1) {
+        flush(cur, acc);
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc[j][e] = 0.f;
+      }
+    };
+    for (int n = 0; n < ncnt; n += 2) {
+      body(n, sA, bA);
+      if (n + 1 < ncnt) body(n + 1, sB, bB);
+    }
+
+    // every output of this link from this CTA is written: count the link complete
+    asm volatile("bar.sync 1, %0;" ::"n"(kTmaConsumers * 32) : "memory");
+    if (threadIdx.x == 0) {
+      fence_acq_rel_gpu();
+      atomicAdd(a.sync, 1u);
+    }
+  }
+
+  // the last CTA to finish returns both counters to zero for the next launch (every CTA has
+  // passed its last wait on the link counter before it counts itself finished)
+  if (threadIdx.x == 0) {
+    fence_acq_rel_gpu();
+    if (atomicAdd(a.sync + 1, 1u) == gridDim.x - 1) {
+      atomicExch(a.sync, 0u);
+      atomicExch(a.sync + 1, 0u);
+    }
+  }
+}
+
+// ------------------------------------------------------------------ host side
+static size_t plan_bytes_for(int n_links, int n_maps) {
+  return sizeof(ChainHeader) + 64 + (size_t)n_maps * sizeof(CUtensorMap) +
+         (size_t)n_links * sizeof(ChainLink);
+}
+
+static int tokens_per_pass(int64_t M) { return M >= 5 ? 8 : M >= 3 ? 4 : M == 2 ? 2 : 1; }
+
+template <int MT>
+static int chain_slots(int max_K, int smem_optin) {
+  int dw = kMaxSlotsPerGroup;
+  while (dw >= 2 && gemv_tma_layout<MT>(max_K / kGroup, dw).total > smem_optin) --dw;
+  return dw >= 2 ? dw : 0;
+}
+
+static int chain_slots_for(int mt, int max_K, int smem_optin) {
+  switch (mt) {
+    case 8: return chain_slots<8>(max_K, smem_optin);
+    case 4: return chain_slots<4>(max_K, smem_optin);
+    case 2: return chain_slots<2>(max_K, smem_optin);
+    default: return chain_slots<1>(max_K, smem_optin);
+  }
+}
+
+template <int MT>
+static int launch_chain_mt(const ChainRun& a, int grid, cudaStream_t s) {
+  const int bytes = gemv_tma_layout<MT>(a.max_K / kGroup, a.dw).total;
+  cudaError_t e = cudaFuncSetAttribute(w2_gemv_chain_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) {
+    record_cuda_error(e);
+    return TB_ERR_CUDA;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kTmaThreads);
+  cfg.dynamicSmemBytes = bytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;  // every CTA resident at once: CTAs wait on each other
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, w2_gemv_chain_kernel<MT>, a);
+  if (e != cudaSuccess) {
+    record_cuda_error(e);
+    return TB_ERR_CUDA;
+  }
+  return TB_OK;
+}
+
+}  // namespace tb
+
+using namespace tb;
+
+extern "C" size_t tb_chain_plan_size(int n_links) {
+  if (n_links < 1) return 0;
+  return plan_bytes_for(n_links, n_links * kMaxMats);
+}
+
+extern "C" size_t tb_chain_workspace_size(void) { return chain_workspace_bytes(); }
+
+extern "C" int tb_chain_plan(const tb_chain_link* links, int n_links, int64_t M, void* plan,
+                             size_t plan_bytes, void* stream) {
+  if (!links || !plan) return TB_ERR_NULL;
+  if (n_links < 1 || M < 1) return TB_ERR_SHAPE;
+  if (M > kChainMaxTokens) return TB_ERR_TOO_LARGE;
+  if (reinterpret_cast<uintptr_t>(plan) & 127u) return TB_ERR_ALIGN;
+  int n_maps = 0;
+  int64_t max_K = 0;
+  for (int i = 0; i < n_links; ++i) {
+    const tb_chain_link& l = links[i];
+    if (l.block != 0 && l.block != kBlock) return TB_ERR_UNSUPPORTED;
+    if (!l.x) return TB_ERR_NULL;
+    if (l.n < 1 || l.n > kMaxMats) return TB_ERR_SHAPE;
+    if (l.K < kBlock || l.K % kBlock || l.K > kChainMaxK) return TB_ERR_SHAPE;
+    if (!aligned16(l.x) || (l.signs && !aligned16(l.signs))) return TB_ERR_ALIGN;
+    int64_t tiles = 0;
+    for (int j = 0; j < l.n; ++j) {
+      if (!l.w[j] || !l.scales[j] || !l.biases[j] || !l.y[j]) return TB_ERR_NULL;
+      if (l.N[j] < 1 || l.N[j] > (1LL << 30)) return TB_ERR_SHAPE;
+      if (!aligned16(l.w[j]) || !aligned16(l.scales[j]) || !aligned16(l.biases[j]) || !aligned16(l.y[j]))
+        return TB_ERR_ALIGN;
+      tiles += (l.N[j] + kUnitRows - 1) / kUnitRows;
+    }
+    if (tiles * (l.K / (kUnitGroups * kGroup)) > (int64_t)INT32_MAX / 2) return TB_ERR_SHAPE;
+    n_maps += l.n;
+    max_K = l.K > max_K ? l.K : max_K;
+  }
+  const size_t need = plan_bytes_for(n_links, n_maps);
+  if (plan_bytes < need) return TB_ERR_WORKSPACE;
+
+  std::vector<uint8_t> host(need, 0);
+  ChainHeader h = {};
+  h.magic = kChainMagic;
+  h.n_links = n_links;
+  h.M = (int32_t)M;
+  h.max_K = (int32_t)max_K;
+  h.maps_off = 128;  // 128-byte aligned tensor maps (a TMA descriptor needs 64)
+  h.links_off = h.maps_off + (int64_t)n_maps * sizeof(CUtensorMap);
+  h.bytes = (int64_t)need;
+  memcpy(host.data(), &h, sizeof(h));
+  CUtensorMap* maps = reinterpret_cast<CUtensorMap*>(host.data() + h.maps_off);
+  int map = 0;
+  for (int i = 0; i < n_links; ++i) {
+    const tb_chain_link& l = links[i];
+    ChainLink d = {};
+    d.x = reinterpret_cast<const __half*>(l.x);
+    d.signs = l.block ? l.signs : nullptr;
+    int64_t tiles = 0;
+    for (int j = 0; j < kMaxMats; ++j) {
+      if (j < l.n) {
+        int rc = code_map(l.w[j], l.N[j], l.K, &maps[map + j]);
+        if (rc != TB_OK) return rc;
+        d.scales[j] = reinterpret_cast<const __half*>(l.scales[j]);
+        d.biases[j] = reinterpret_cast<const __half*>(l.biases[j]);
+        d.y[j] = reinterpret_cast<__half*>(l.y[j]);
+        d.N[j] = (int)l.N[j];
+        d.tile0[j] = (int)tiles;
+        tiles += (l.N[j] + kUnitRows - 1) / kUnitRows;
+      } else {
+        d.tile0[j] = (int)tiles;
+      }
+    }
+    d.tile0[kMaxMats] = (int)tiles;
+    d.nmat = l.n;
+    d.K = (int)l.K;
+    d.G = (int)(l.K / kGroup);
+    d.C = (int)(l.K / (kUnitGroups * kGroup));
+    d.rotate = l.block != 0;
+    d.n_tiles = (int)tiles;
+    d.map0 = map;
+    memcpy(host.data() + h.links_off + (size_t)i * sizeof(ChainLink), &d, sizeof(d));
+    map += l.n;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(plan, host.data(), need, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);  // the host image is freed on return
+  if (e != cudaSuccess) {
+    record_cuda_error(e);
+    return TB_ERR_CUDA;
+  }
+  return TB_OK;
+}
+
+extern "C" int tb_chain_run(const void* plan, int n_links, int64_t M, int64_t max_K, void* workspace,
+                            size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  if (!plan) return TB_ERR_NULL;
+  if (n_links < 1 || M < 1 || max_K < kBlock || max_K % kBlock || max_K > kChainMaxK) return TB_ERR_SHAPE;
+  if (M > kChainMaxTokens) return TB_ERR_TOO_LARGE;
+  if (reinterpret_cast<uintptr_t>(plan) & 127u) return TB_ERR_ALIGN;
+  if (!workspace || workspace_bytes < chain_workspace_bytes()) return TB_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return TB_ERR_ALIGN;
+  DeviceFacts f;
+  int rc = device_facts(&f);
+  if (rc != TB_OK) return rc;
+  if (f.sms > kChainMaxCtas) return TB_ERR_TOO_LARGE;
+  const int mt = tokens_per_pass(M);
+  const int dw = chain_slots_for(mt, (int)max_K, f.smem_optin);
+  if (dw == 0) return TB_ERR_TOO_LARGE;
+  const uint8_t* p = static_cast<const uint8_t*>(plan);
+  ChainRun a = {};
+  a.header = reinterpret_cast<const ChainHeader*>(p);
+  a.maps = reinterpret_cast<const CUtensorMap*>(p + 128);  // the links follow the maps (header)
+  a.n_links = n_links;
+  a.Mc = (int)M;
+  a.max_K = (int)max_K;
+  a.dw = dw;
+  char* ws = static_cast<char*>(workspace);
+  a.ws_count = reinterpret_cast<int*>(ws);
+  a.sync = reinterpret_cast<uint32_t*>(ws + kChainCounterBytes);
+  a.ws_partial = reinterpret_cast<float*>(ws + kChainCounterBytes + kChainSyncBytes);
+  a.status = dev_status;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  switch (mt) {
+    case 8: return launch_chain_mt<8>(a, f.sms, s);
+    case 4: return launch_chain_mt<4>(a, f.sms, s);
+    case 2: return launch_chain_mt<2>(a, f.sms, s);
+    default: return launch_chain_mt<1>(a, f.sms, s);
+  }
+}

@@ -39,6 +39,13 @@ TB_DEVI uint64_t globaltimer_ns() {
 // without the cost of a sequentially consistent fence
 TB_DEVI void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
+// gpu-scope acquire load of a 32-bit counter in global memory
+TB_DEVI uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
 TB_DEVI void set_status(int32_t* st, int bits) {
   if (st) atomicOr(st, bits);
 }

@@ -38,24 +38,10 @@
 #include <unordered_map>
 
 #include "tb_common.cuh"
+#include "tb_gemv_core.cuh"
 #include "tb_host.h"
 
 namespace tb {
-
-constexpr int kUnitRows = 128;
-constexpr int kUnitGroups = 4;                          // groups per unit (512 k)
-constexpr int kSlotBytes = kUnitRows * 128;             // 16 KB box of packed codes
-constexpr int kGroupsOfWarps = 3;                       // unit groups
-constexpr int kWarpsPerUnit = 4;                        // 32 rows each
-constexpr int kTmaConsumers = kGroupsOfWarps * kWarpsPerUnit;
-constexpr int kTmaThreads = (kTmaConsumers + 1) * 32;
-constexpr int kMaxSlotsPerGroup = 4;
-constexpr int kPreIssue = 1;        // units per group issued before the activations are loaded
-constexpr int kCutSlots = 4;        // shared sums of tiles cut by a group or CTA boundary
-constexpr int kScaleStageBytes = 32 * kUnitGroups * 8;  // per warp: 32 rows x 4 groups of fp32 (s, b)
-constexpr uint32_t kMagic1024 = 0x64006400u;
-
-constexpr int kMaxMats = 4;  // matrices sharing one input in one launch
 
 struct GemvTmaArgs {
   const __half* x;               // [Mc, K]
@@ -85,155 +71,6 @@ TB_DEVI int mat_of(const GemvTmaArgs& a, int tile) {
 #pragma unroll
   for (int k = 1; k < kMaxMats; ++k) i += (k < a.nmat && tile >= a.tile0[k]);
   return i;
-}
-
-struct GemvTmaLayout {
-  int codes, img, cs, sstage, accs, cnt, bars, total;
-};
-
-__host__ __device__ inline int rup(int v, int a) { return (v + a - 1) / a * a; }
-
-
-template <int MT>
-__host__ __device__ inline GemvTmaLayout gemv_tma_layout(int G, int dw) {
-  GemvTmaLayout L;
-  int off = 0;
-  L.codes = off;  // 1024-aligned slots (the 128-byte swizzle repeats every 1024 bytes)
-  off += kGroupsOfWarps * dw * kSlotBytes;
-  L.img = off;
-  off += G * 256 * MT;
-  L.cs = off;
-  off += G * MT * 8;
-  off = rup(off, 16);
-  L.sstage = off;
-  off += kTmaConsumers * kScaleStageBytes;
-  L.accs = off;
-  off += kCutSlots * kUnitRows * MT * 4;
-  L.cnt = off;
-  off += kCutSlots * 4;
-  off = rup(off, 8);
-  L.bars = off;
-  off += (2 * kGroupsOfWarps * dw + 1) * 8;
-  L.total = off + 1024;  // slack to align the base to 1024
-  return L;
-}
-
-// stream-K unit range [lo, hi) of CTA c
-__host__ __device__ inline void cta_range_of(int c, int grid, int n_tiles, int C, int& lo, int& hi) {
-  const int64_t S = (int64_t)n_tiles * C;
-  lo = (int)(S * c / grid);
-  hi = (int)(S * (c + 1) / grid);
-}
-
-// owner of global unit s when S units are cut into grid ranges [S*i/grid, S*(i+1)/grid)
-__host__ __device__ inline int stage_owner(int64_t s, int64_t S, int grid) {
-  return (int)(((s + 1) * grid - 1) / S);
-}
-
-TB_DEVI void mma16816_acc(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                          uint32_t b0, uint32_t b1) {
-  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-TB_DEVI void decode_word_sigma(uint32_t w, uint32_t (&P)[8]) {
-  const uint32_t w6 = w >> 6;
-  P[0] = lop3_and_or(w, 0x00030003u, kMagic1024);   // codes 0, 8   sigma 1
-  P[1] = lop3_and_or(w, 0x000C000Cu, kMagic1024);   // codes 1, 9   sigma 4
-  P[2] = lop3_and_or(w, 0x00300030u, kMagic1024);   // codes 2, 10  sigma 16
-  P[3] = lop3_and_or(w, 0x00C000C0u, kMagic1024);   // codes 3, 11  sigma 64
-  P[4] = lop3_and_or(w, 0x03000300u, kMagic1024);   // codes 4, 12  sigma 256
-  P[5] = lop3_and_or(w6, 0x00300030u, kMagic1024);  // codes 5, 13  sigma 16
-  P[6] = lop3_and_or(w6, 0x00C000C0u, kMagic1024);  // codes 6, 14  sigma 64
-  P[7] = lop3_and_or(w6, 0x03000300u, kMagic1024);  // codes 7, 15  sigma 256
-}
-
-TB_DEVI float inv_sigma_p(int p) {
-  return p == 0 ? 1.0f : p == 1 ? 0.25f : (p == 2 || p == 5) ? 0.0625f
-       : (p == 3 || p == 6) ? 0.015625f : 0.00390625f;
-}
-
-TB_DEVI void tma2d(uint32_t dst, const CUtensorMap* tm, int x, int y, uint64_t* bar, uint64_t pol) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
-      "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(pol)
-      : "memory");
-}
-
-// One group gi (0..3) of a unit for the warp's two 16-row blocks: decode, 2 x 8 mma (two
-// independent accumulator chains sharing one B fragment), scale epilogue.
-//   box:  the unit's code box; R0, R0 + 16: this lane's A rows of block 0 (block 1 = + 16)
-//   imgt: B-fragment image entry of this lane; csa: (C, S) pairs [G][MT]
-//   ss:   this warp's staged (scale, bias) pairs, fp32 [32 rows][4 groups]
-template <int MT>
-TB_DEVI void unit_group(uint32_t box, int R0, int t, int gi, int grp, uint32_t imgt, uint32_t ss,
-                        int rA, uint32_t csa, int t0, int t1, float (&acc)[2][4]) {
-  const int c = 2 * gi + (t >> 1);  // logical 16-byte chunk of the 128-byte row
-  uint2 w[2][2];
-#pragma unroll
-  for (int j = 0; j < 2; ++j)
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int R = R0 + 16 * j + 8 * h;  // (R & 7) == (rA & 7)
-      w[j][h] = ld_shared_v2(box + R * 128 + ((c ^ (rA & 7)) << 4) + (t & 1) * 8);
-    }
-  const float2 cs0 = ld_shared_f2(csa + (grp * MT + t0) * 8);
-  const float2 cs1 = MT > 1 ? ld_shared_f2(csa + (grp * MT + t1) * 8) : cs0;
-  float d[2][4];
-#pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    d[j][0] = -cs0.x;
-    d[j][1] = -cs1.x;
-    d[j][2] = -cs0.x;
-    d[j][3] = -cs1.x;
-  }
-#pragma unroll
-  for (int half = 0; half < 2; ++half) {
-    const uint4 i0 = ld_shared_v4(imgt + (grp * 4 + 2 * half) * MT * 64);
-    const uint4 i1 = ld_shared_v4(imgt + (grp * 4 + 2 * half + 1) * MT * 64);
-    uint32_t P[2][8], Q[2][8];
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      decode_word_sigma(half ? w[j][0].y : w[j][0].x, P[j]);
-      decode_word_sigma(half ? w[j][1].y : w[j][1].x, Q[j]);
-    }
-#pragma unroll
-    for (int j = 0; j < 2; ++j) mma16816_acc(d[j], P[j][0], Q[j][0], P[j][1], Q[j][1], i0.x, i0.y);
-#pragma unroll
-    for (int j = 0; j < 2; ++j) mma16816_acc(d[j], P[j][2], Q[j][2], P[j][3], Q[j][3], i0.z, i0.w);
-#pragma unroll
-    for (int j = 0; j < 2; ++j) mma16816_acc(d[j], P[j][4], Q[j][4], P[j][5], Q[j][5], i1.x, i1.y);
-#pragma unroll
-    for (int j = 0; j < 2; ++j) mma16816_acc(d[j], P[j][6], Q[j][6], P[j][7], Q[j][7], i1.z, i1.w);
-  }
-#pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    const int ra = 16 * j + rA, rb = ra + 8;  // rows within the warp's 32
-    const float2 A = ld_shared_f2(ss + (ra * kUnitGroups + gi) * 8);  // (s, b) of row ra
-    const float2 B = ld_shared_f2(ss + (rb * kUnitGroups + gi) * 8);
-    acc[j][0] = fmaf(A.x, d[j][0], fmaf(A.y, cs0.y, acc[j][0]));
-    acc[j][2] = fmaf(B.x, d[j][2], fmaf(B.y, cs0.y, acc[j][2]));
-    if (MT > 1) {  // D columns 2t+1 hold a second token only when there is one
-      acc[j][1] = fmaf(A.x, d[j][1], fmaf(A.y, cs1.y, acc[j][1]));
-      acc[j][3] = fmaf(B.x, d[j][3], fmaf(B.y, cs1.y, acc[j][3]));
-    }
-  }
-}
-
-// the unit after (or before) (tile, chunk) in tile-major order
-TB_DEVI void step_unit(int& tile, int& chunk, int C, bool back) {
-  if (back) {
-    if (--chunk < 0) {
-      chunk = C - 1;
-      --tile;
-    }
-  } else if (++chunk == C) {
-    chunk = 0;
-    ++tile;
-  }
 }
 
 template <int MT>
@@ -673,8 +510,9 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// tensor map of one packed matrix's codes, cached by (pointer, shape)
-static int code_map(const uint32_t* w, int64_t N, int64_t K, CUtensorMap* out) {
+// tensor map of one packed matrix's codes (box 32 words x 128 rows, 128-byte swizzle), cached
+// by (pointer, shape)
+int code_map(const uint32_t* w, int64_t N, int64_t K, CUtensorMap* out) {
   struct Key {
     const void* w;
     int64_t N, K;

@@ -125,3 +125,52 @@ def test_multi_refuses_bad_arguments(lib):
     assert f(P, 1, 1024, P, 1024, 2, arr, arr, arr, bad, arr, None, 0, None, None) == -2
     # the prefill path of a multi call needs the x' workspace
     assert f(P, 64, 1024, P, 1024, 2, arr, arr, arr, ns, arr, None, 0, None, None) == -7
+
+
+def test_chain_link_struct_matches_header():
+    import ternary_hadamard_rotated_gb300 as tb
+
+    # int64 K, two int32, five arrays of four 8-byte fields, two pointers: 192 bytes, no padding
+    assert ctypes.sizeof(tb.ChainLink) == 192
+    assert tb.ChainLink.K.offset == 16 and tb.ChainLink.w.offset == 32 and tb.ChainLink.y.offset == 160
+
+
+def test_chain_refuses_bad_arguments(lib):
+    import ternary_hadamard_rotated_gb300 as tb
+
+    assert lib.tb_chain_plan_size(0) == 0
+    assert lib.tb_chain_plan_size(3) >= 3 * (4 * 128 + 176)
+    assert lib.tb_chain_workspace_size() >= 1280
+
+    def link(**kw):
+        lk = tb.ChainLink()
+        lk.x, lk.signs, lk.K, lk.block, lk.n = P, P, 1024, 1024, 1
+        lk.w[0], lk.scales[0], lk.biases[0], lk.N[0], lk.y[0] = P, P, P, 16, P
+        for k, v in kw.items():
+            setattr(lk, k, v)
+        return lk
+
+    def plan(lk, M=1, plan_ptr=0x10000, nbytes=1 << 20):
+        arr = (tb.ChainLink * 1)(lk)
+        return lib.tb_chain_plan(ctypes.cast(arr, ctypes.c_void_p), 1, M, plan_ptr, nbytes, None)
+
+    assert lib.tb_chain_plan(None, 1, 1, 0x10000, 1 << 20, None) == tb.TB_ERR_NULL
+    assert plan(link(), plan_ptr=0) == tb.TB_ERR_NULL
+    assert plan(link(), M=0) == tb.TB_ERR_SHAPE
+    assert plan(link(), M=9) == tb.TB_ERR_TOO_LARGE
+    assert plan(link(), plan_ptr=0x10040) == tb.TB_ERR_ALIGN        # plan not 128-byte aligned
+    assert plan(link(block=512)) == tb.TB_ERR_UNSUPPORTED
+    assert plan(link(K=1536)) == tb.TB_ERR_SHAPE
+    assert plan(link(n=0)) == tb.TB_ERR_SHAPE
+    assert plan(link(n=5)) == tb.TB_ERR_SHAPE
+    assert plan(link(x=None)) == tb.TB_ERR_NULL
+    assert plan(link(x=P + 8)) == tb.TB_ERR_ALIGN
+    assert plan(link(), nbytes=64) == tb.TB_ERR_WORKSPACE
+    r = lib.tb_chain_run
+    assert r(None, 1, 1, 1024, P, 1 << 22, None, None) == tb.TB_ERR_NULL
+    assert r(0x10000, 0, 1, 1024, P, 1 << 22, None, None) == tb.TB_ERR_SHAPE
+    assert r(0x10000, 1, 9, 1024, P, 1 << 22, None, None) == tb.TB_ERR_TOO_LARGE
+    assert r(0x10000, 1, 1, 1000, P, 1 << 22, None, None) == tb.TB_ERR_SHAPE
+    assert r(0x10040, 1, 1, 1024, P, 1 << 22, None, None) == tb.TB_ERR_ALIGN
+    assert r(0x10000, 1, 1, 1024, P, 1024, None, None) == tb.TB_ERR_WORKSPACE
+    assert r(0x10000, 1, 1, 1024, None, 1 << 22, None, None) == tb.TB_ERR_WORKSPACE
