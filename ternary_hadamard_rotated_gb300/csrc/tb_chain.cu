@@ -43,6 +43,9 @@ constexpr uint32_t kChainMagic = 0x54424348u;  // "TBCH"
 constexpr int kChainMaxCtas = 256;                // parts slots of the fixup region
 constexpr int64_t kChainMaxTokens = 8;
 constexpr int64_t kChainMaxK = 1 << 20;
+// Units per unit group that the producer streams into a link before the consumers have
+// loaded that link's activations: the loads of x wait behind the weight copies in flight.
+constexpr int kChainPreIssue = 1;
 
 struct ChainLink {
   const __half* x;                // [Mc, K]
@@ -74,6 +77,7 @@ struct ChainRun {
   const CUtensorMap* maps;
   const ChainHeader* header;
   int n_links, Mc, max_K, dw;
+  int preissue;        // units per group the producer issues into a link before its x is loaded
   int* ws_count;       // [kChainMaxCtas] contributions per shared tile (zero between links)
   uint32_t* sync;      // [0] links completed, summed over CTAs; [1] CTAs finished
   float* ws_partial;   // [kChainMaxCtas][2][128][MT]
@@ -139,6 +143,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) w2_gemv_chain_kernel(const __g
   int* cnt = reinterpret_cast<int*>(smem + L.cnt);         // [kCutSlots]
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* empty = full + kGroupsOfWarps * DW;
+  uint64_t* xready = empty + kGroupsOfWarps * DW;  // one phase per link: its x is loaded
   __shared__ volatile int aborted;
 
   // a plan that does not match the launch: every CTA returns before any wait
@@ -156,6 +161,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) w2_gemv_chain_kernel(const __g
       mbar_init(full + i, 1);
       mbar_init(empty + i, kWarpsPerUnit);
     }
+    mbar_init(xready, kTmaConsumers);
     fence_barrier_init();
   }
   for (int i = threadIdx.x; i < kCutSlots * kUnitRows * MT; i += blockDim.x) accs[i] = 0.f;
@@ -197,6 +203,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) w2_gemv_chain_kernel(const __g
           maxcnt = cntu[u] > maxcnt ? cntu[u] : maxcnt;
         }
         for (int n = 0; n < maxcnt; ++n) {
+          if (n == a.preissue) wait(xready, li & 1);  // this link's x has been read
 #pragma unroll
           for (int u = 0; u < kGroupsOfWarps; ++u) {
             if (n >= cntu[u]) continue;
@@ -213,6 +220,9 @@ __global__ void __launch_bounds__(kTmaThreads, 1) w2_gemv_chain_kernel(const __g
             }
           }
         }
+        // every phase of xready is waited for in order (a parity wait tells apart only the
+        // current phase and the one before it)
+        if (maxcnt <= a.preissue) wait(xready, li & 1);
       }
       // leave no copy in flight: wait (bounded, even after a timeout) for the last fill of
       // every slot that was filled
@@ -248,6 +258,24 @@ __global__ void __launch_bounds__(kTmaThreads, 1) w2_gemv_chain_kernel(const __g
     const int C = lk->C, G = lk->G, K = lk->K;
     const int S = lk->n_tiles * C;
     const LinkRange r = link_range(lk->n_tiles, C);
+    // everything the prologue needs but x itself is read before the wait on the previous link
+    const __half* lx = lk->x;
+    const int8_t* lsg = lk->signs;
+    const int lrot = lk->rotate;
+    int b1, e1, b2, e2;
+    blocks_needed(r.lo, r.hi - r.lo, C, K, b1, e1, b2, e2);
+    if (lsg) {
+      const int nblk = (e1 - b1) + (e2 - b2);
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const int it = warp + q * kTmaConsumers;
+        if (it < Mc * nblk) {
+          const int bi = it % nblk;
+          const int b = bi < e1 - b1 ? b1 + bi : b2 + (bi - (e1 - b1));
+          asm volatile("prefetch.global.L1 [%0];" ::"l"(lsg + b * kBlock + lane * 32));
+        }
+      }
+    }
     int glo, ghi;
     link_group_range(r, ug, glo, ghi);
     const int ncnt = ghi - glo;
@@ -304,12 +332,9 @@ __global__ void __launch_bounds__(kTmaThreads, 1) w2_gemv_chain_kernel(const __g
       }
       asm volatile("bar.sync 1, %0;" ::"n"(kTmaConsumers * 32) : "memory");
     }
-    {
-      int b1, e1, b2, e2;
-      blocks_needed(r.lo, r.hi - r.lo, C, K, b1, e1, b2, e2);
-      prologue_image<MT>(lk->x, lk->signs, K, Mc, lk->rotate, b1, e1, b2, e2, warp, kTmaConsumers,
-                         lane, img, cs);
-    }
+    prologue_image<MT>(lx, lsg, K, Mc, lrot, b1, e1, b2, e2, warp, kTmaConsumers, lane, img, cs);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(xready);  // the producer may stream on into this link
     asm volatile("bar.sync 1, %0;" ::"n"(kTmaConsumers * 32) : "memory");
 
     // Add this warp's sums of tile T (all of the group's units of T) to wherever T is finished.
@@ -651,6 +676,7 @@ extern "C" int tb_chain_run(const void* plan, int n_links, int64_t M, int64_t ma
   a.Mc = (int)M;
   a.max_K = (int)max_K;
   a.dw = dw;
+  a.preissue = kChainPreIssue;
   char* ws = static_cast<char*>(workspace);
   a.ws_count = reinterpret_cast<int*>(ws);
   a.sync = reinterpret_cast<uint32_t*>(ws + kChainCounterBytes);

@@ -252,4 +252,24 @@ TB_DEVI void wht1024_a_shfl(float (&v)[32], int lane) {
   }
 }
 
+// Same transform, register-light: the five lane stages run on eight register indices at a
+// time (each index is an independent chain through the five stages), so a warp keeps eight
+// shuffles in flight with eight extra registers instead of serialising them when registers
+// are scarce.
+TB_DEVI void wht1024_a_shfl_batched(float (&v)[32], int lane) {
+  butterfly32(v);
+#pragma unroll
+  for (int rb = 0; rb < 32; rb += 8) {
+#pragma unroll
+    for (int h = 1; h < 32; h <<= 1) {
+      const float sg = (lane & h) ? -1.0f : 1.0f;
+      float p[8];
+#pragma unroll
+      for (int r = 0; r < 8; ++r) p[r] = __shfl_xor_sync(0xffffffffu, v[rb + r], h);
+#pragma unroll
+      for (int r = 0; r < 8; ++r) v[rb + r] = fmaf(sg, v[rb + r], p[r]);
+    }
+  }
+}
+
 }  // namespace tb

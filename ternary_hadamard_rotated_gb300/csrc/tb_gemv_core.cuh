@@ -254,7 +254,7 @@ TB_DEVI void prologue_image(const __half* x, const int8_t* signs, int K, int Mc,
         if (sg[r] < 0) v[r] = -v[r];
     }
     if (rotate) {
-      wht1024_a_shfl(v, lane);
+      wht1024_a_shfl_batched(v, lane);
 #pragma unroll
       for (int r = 0; r < 32; ++r) v[r] *= kInvSqrtBlock;
     }
