@@ -332,7 +332,14 @@ __global__ void __launch_bounds__(kTmaThreads, 1) w2_gemv_chain_kernel(const __g
       }
       asm volatile("bar.sync 1, %0;" ::"n"(kTmaConsumers * 32) : "memory");
     }
-    prologue_image<MT>(lx, lsg, K, Mc, lrot, b1, e1, b2, e2, warp, kTmaConsumers, lane, img, cs);
+    {
+      // scratch of the transform: the slot after the one that holds this group's first unit
+      // of the link; the producer fills it only after every consumer warp has arrived on
+      // xready for this link
+      const uint32_t scratch = slots_u32 + (ug * DW + (si + 1 == DW ? 0 : si + 1)) * kSlotBytes + wi * 4096;
+      prologue_image<MT>(lx, lsg, K, Mc, lrot, b1, e1, b2, e2, warp, kTmaConsumers, lane, img, cs, scratch);
+    }
+    fence_proxy_async_smem();  // the scratch's generic accesses before the copies that refill it
     __syncwarp();
     if (lane == 0) mbar_arrive(xready);  // the producer may stream on into this link
     asm volatile("bar.sync 1, %0;" ::"n"(kTmaConsumers * 32) : "memory");

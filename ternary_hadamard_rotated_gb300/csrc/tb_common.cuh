@@ -252,6 +252,59 @@ TB_DEVI void wht1024_a_shfl(float (&v)[32], int lane) {
   }
 }
 
+// Same transform through a 4 KB shared scratch owned by the warp: 32 rows of 128 bytes, the
+// 16-byte chunk c of row i stored at position c ^ (i & 7).  Five stages over the register
+// index (element bits 0..4); each lane writes its row as eight 16-byte chunks; each lane reads
+// column `lane` (layout B); five more stages (bits 5..9); the same way back.  Row accesses
+// are conflict-free per 8-lane phase, column accesses over all 32 banks; addresses are eight
+// bases plus immediate offsets, so the transposes need few registers.
+TB_DEVI void wht1024_a_smem(float (&v)[32], uint32_t scratch, int lane) {
+  butterfly32(v);
+  const uint32_t row = scratch + (uint32_t)lane * 128u;
+  const uint32_t sw = (uint32_t)lane & 7u;
+#pragma unroll
+  for (int c = 0; c < 8; ++c)
+    asm volatile("st.shared.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(row + 16u * ((uint32_t)c ^ sw)),
+                 "f"(v[4 * c]), "f"(v[4 * c + 1]), "f"(v[4 * c + 2]), "f"(v[4 * c + 3])
+                 : "memory");
+  __syncwarp();
+  uint32_t col[8];  // word `lane` of row j lies at col[j & 7] + 128 j
+#pragma unroll
+  for (int k = 0; k < 8; ++k) col[k] = scratch + 16u * (((uint32_t)lane >> 2) ^ (uint32_t)k) + 4u * ((uint32_t)lane & 3u);
+#pragma unroll
+  for (int j = 0; j < 32; ++j) v[j] = ld_shared_f(col[j & 7] + 128u * (uint32_t)j);
+  butterfly32(v);
+  __syncwarp();
+#pragma unroll
+  for (int j = 0; j < 32; ++j) st_shared_f(col[j & 7] + 128u * (uint32_t)j, v[j]);
+  __syncwarp();
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    float4 q;
+    asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];"
+                 : "=f"(q.x), "=f"(q.y), "=f"(q.z), "=f"(q.w)
+                 : "r"(row + 16u * ((uint32_t)c ^ sw))
+                 : "memory");
+    v[4 * c] = q.x;
+    v[4 * c + 1] = q.y;
+    v[4 * c + 2] = q.z;
+    v[4 * c + 3] = q.w;
+  }
+  __syncwarp();
+}
+
+// Sum of 32 values as a balanced tree (depth 5 instead of a 32-long dependent chain).
+TB_DEVI float tree_sum32(const float (&v)[32]) {
+  float s[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) s[i] = v[2 * i] + v[2 * i + 1];
+#pragma unroll
+  for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+    for (int i = 0; i < w; ++i) s[i] = s[2 * i] + s[2 * i + 1];
+  return s[0];
+}
+
 // Same transform, register-light: the five lane stages run on eight register indices at a
 // time (each index is an independent chain through the five stages), so a warp keeps eight
 // shuffles in flight with eight extra registers instead of serialising them when registers

@@ -214,11 +214,12 @@ TB_DEVI void blocks_needed(int lo, int nst, int C, int K, int& b1, int& e1, int&
 //   cs:  per group and token (1024 * sum(x'/sigma), sum x')
 // Warp `w` of `nw` takes items (token, block) w, w + nw, ...; the loads of two items are in
 // flight together.  x is read through L2 (ld.global.cg): it may have been written by other
-// SMs earlier in the same launch.
+// SMs earlier in the same launch.  `scratch` is a 4 KB shared buffer of the warp for the
+// transform's transposes.
 template <int MT>
 TB_DEVI void prologue_image(const __half* x, const int8_t* signs, int K, int Mc, int rotate,
                             int b1, int e1, int b2, int e2, int w, int nw, int lane,
-                            __half* img, float2* cs) {
+                            __half* img, float2* cs, uint32_t scratch) {
   const int t = lane & 3;
   const int nblk = (e1 - b1) + (e2 - b2);
   auto block_of = [&](int bi) { return bi < e1 - b1 ? b1 + bi : b2 + (bi - (e1 - b1)); };
@@ -254,34 +255,35 @@ TB_DEVI void prologue_image(const __half* x, const int8_t* signs, int K, int Mc,
         if (sg[r] < 0) v[r] = -v[r];
     }
     if (rotate) {
-      wht1024_a_shfl_batched(v, lane);
+      wht1024_a_smem(v, scratch, lane);
 #pragma unroll
       for (int r = 0; r < 32; ++r) v[r] *= kInvSqrtBlock;
     }
     const int grp = b * (kBlock / kGroup) + (lane >> 2);
-    float ssum = 0.f, csum = 0.f;
 #pragma unroll
-    for (int r = 0; r < 32; ++r) {
-      v[r] = __half2float(__float2half_rn(v[r]));  // x' rounded to fp16
-      ssum += v[r];
-    }
+    for (int r = 0; r < 32; ++r) v[r] = __half2float(__float2half_rn(v[r]));  // x' rounded to fp16
+    float ssum = tree_sum32(v);
     ssum += __shfl_xor_sync(0xffffffffu, ssum, 1);
     ssum += __shfl_xor_sync(0xffffffffu, ssum, 2);
+    float cpart[4];  // C as four partial sums (one per mma k-step) of the fp16 values x'/sigma
 #pragma unroll
     for (int mp = 0; mp < 4; ++mp) {
       uint32_t pk[4];
+      float c2[4];
 #pragma unroll
       for (int e2_ = 0; e2_ < 4; ++e2_) {
         const int p = 4 * (mp & 1) + e2_;
         const int r = (mp >> 1) * 16 + p;
         const float is = inv_sigma_p(p);
         const __half lo_ = __float2half_rn(v[r] * is), hi_ = __float2half_rn(v[r + 8] * is);
-        csum += __half2float(lo_) + __half2float(hi_);
+        c2[e2_] = __half2float(lo_) + __half2float(hi_);
         pk[e2_] = (uint32_t)__half_as_ushort(lo_) | ((uint32_t)__half_as_ushort(hi_) << 16);
       }
+      cpart[mp] = (c2[0] + c2[1]) + (c2[2] + c2[3]);
       *reinterpret_cast<uint4*>(img + ((size_t)(grp * 4 + mp) * MT + tok) * 32 + t * 8) =
           make_uint4(pk[0], pk[1], pk[2], pk[3]);
     }
+    float csum = (cpart[0] + cpart[1]) + (cpart[2] + cpart[3]);
     csum += __shfl_xor_sync(0xffffffffu, csum, 1);
     csum += __shfl_xor_sync(0xffffffffu, csum, 2);
     if (t == 0) cs[grp * MT + tok] = make_float2(1024.f * csum, ssum);
@@ -296,5 +298,4 @@ TB_DEVI void prologue_image(const __half* x, const int8_t* signs, int K, int Mc,
     if (it2 < items) transform_block(it2, xb, sb);
   }
 }
-
 }  // namespace tb
