@@ -17,6 +17,7 @@
 // (one thread), warps 2..9 decode B and afterwards drain TMEM to fp16 y.
 // A 4-stage mbarrier ring couples the three roles; every wait is bounded.
 #include <cuda.h>
+#include <algorithm>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
@@ -28,15 +29,6 @@ namespace tb {
 constexpr int kTcBM = 128, kTcBK = 64;  // token subtile, k per stage
 constexpr int kTcThreads = 320;
 constexpr int kTcABytes = kTcBM * kTcBK * 2;  // 16 KB
-
-struct TcArgs {
-  const uint32_t* w;     // [N, K/16]
-  const __half* scales;  // [N, G]
-  const __half* biases;  // [N, G]
-  __half* y;             // [M, N]
-  int M, N, K, G;
-  int32_t* status;
-};
 
 // K-major operand in the 128-byte swizzle: 8-row core groups 1024 bytes apart.
 TB_DEVI uint64_t umma_desc_sw128(uint32_t saddr) {
@@ -112,18 +104,42 @@ struct TcCfg {
   static constexpr int kBBytes = BN * kTcBK * 2;
   static constexpr int kStageBytes = NSUB * kTcABytes + kBBytes;
   static constexpr int kStages = (192 * 1024) / kStageBytes;
-  static constexpr int kSmem = kStages * kStageBytes + 1024 + 1024;
+  static constexpr int kSmem = kStages * kStageBytes + 1024 + 1024;  // stages, barriers, alignment
   static constexpr int kTmemCols = NSUB * BN;
   // kind::f16 instruction descriptor: fp16 A and B, fp32 D, both K-major, M = 128, N = BN
   static constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(kTcBM >> 4) << 24);
   static constexpr int kThreadsPerRow = 256 / BN;  // decoder threads per B row
 };
 
+// Stream-K schedule: the units (output tile, 64-k block) of all tiles, tile-major, are cut
+// into one equal contiguous range per CTA (one persistent CTA per SM).  A CTA walks its range
+// as segments (runs of k-blocks of one tile); a segment that covers its whole tile is written
+// to y directly, one that covers part of it goes as fp32 to this CTA's workspace slot, and the
+// last of the tile's CTAs to count in adds the parts in CTA order and writes y.  A grid of at
+// most one CTA per tile splits a tile between two CTAs at most; a grid of q CTAs per tile
+// splits every tile into q equal k-ranges; one CTA per tile splits nothing.
+struct TcSkArgs {
+  const uint32_t* w;     // [N, K/16]
+  const __half* scales;  // [N, G]
+  const __half* biases;  // [N, G]
+  __half* y;             // [M, N]
+  int M, N, K, G;
+  int tiles_n, nkb;      // tile t = (t / tiles_n) token tile, (t % tiles_n) row tile
+  int units;             // tiles * nkb
+  float* part;           // [grid][2][NSUB*128][BN] fp32 parts of split tiles (scratch)
+  int* count;            // [tiles] contributions counted (zero before a call and after it)
+  int32_t* status;
+};
+
+TB_DEVI int sk_owner(int u, int units, int grid) { return (int)(((int64_t)(u + 1) * grid - 1) / units); }
+TB_DEVI int sk_lo(int c, int units, int grid) { return (int)((int64_t)units * c / grid); }
+
 template <int NSUB, int BN>
 __global__ void __launch_bounds__(kTcThreads, 1)
-    w2_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const TcArgs a) {
+    w2_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const TcSkArgs a) {
   using Cfg = TcCfg<NSUB, BN>;
   constexpr int S = Cfg::kStages;
+  constexpr int kPartFloats = NSUB * kTcBM * BN;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -132,13 +148,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint64_t* fullA = bars;
   uint64_t* fullB = bars + S;
   uint64_t* empty = bars + 2 * S;
-  uint64_t* accum = bars + 3 * S;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * S + 1);
+  uint64_t* accum = bars + 3 * S;      // one phase per segment: its accumulator is complete
+  uint64_t* tfree = bars + 3 * S + 1;  // one phase per segment: its accumulator has been read
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * S + 2);
   __shared__ volatile int aborted;
+  __shared__ int last_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n0 = blockIdx.x * BN, m0 = blockIdx.y * (NSUB * kTcBM);
-  const int nkb = a.K / kTcBK;
+  const int nkb = a.nkb, units = a.units, grid = gridDim.x;
+  const int lo = sk_lo(blockIdx.x, units, grid), hi = sk_lo(blockIdx.x + 1, units, grid);
 
   if (threadIdx.x == 0) {
     aborted = 0;
@@ -148,6 +166,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(empty + s, 1);
     }
     mbar_init(accum, 1);
+    mbar_init(tfree, 8);  // lane 0 of each of the 8 decoder warps
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -169,39 +188,60 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       set_status(a.status, TB_DEV_TIMEOUT);
     }
   };
+  // segment starting at unit u: tile t, k-blocks [k0, k1)
+  auto segment = [&](int u, int& t, int& k0, int& k1) {
+    t = u / nkb;
+    k0 = u - t * nkb;
+    k1 = min(nkb, k0 + (hi - u));
+  };
 
   if (warp == 0) {
     if (lane == 0) {
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
-      for (int kb = 0; kb < nkb; ++kb) {
-        const int s = kb % S, it = kb / S;
-        if (it > 0) wait(empty + s, (it - 1) & 1);
-        mbar_arrive_expect_tx(fullA + s, NSUB * kTcABytes);
+      int it = 0;
+      for (int u = lo; u < hi;) {
+        int t, k0, k1;
+        segment(u, t, k0, k1);
+        const int m0 = (t / a.tiles_n) * (NSUB * kTcBM);
+        for (int kb = k0; kb < k1; ++kb, ++it) {
+          const int s = it % S, ph = it / S;
+          if (ph > 0) wait(empty + s, (ph - 1) & 1);
+          mbar_arrive_expect_tx(fullA + s, NSUB * kTcABytes);
 #pragma unroll
-        for (int sub = 0; sub < NSUB; ++sub)
-          tma_load_2d(smem + s * Cfg::kStageBytes + sub * kTcABytes, &tmA, kb * kTcBK,
-                      m0 + sub * kTcBM, fullA + s);
+          for (int sub = 0; sub < NSUB; ++sub)
+            tma_load_2d(smem + s * Cfg::kStageBytes + sub * kTcABytes, &tmA, kb * kTcBK,
+                        m0 + sub * kTcBM, fullA + s);
+        }
+        u += k1 - k0;
       }
     }
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) {
-      for (int kb = 0; kb < nkb; ++kb) {
-        const int s = kb % S, it = kb / S;
-        wait(fullA + s, it & 1);
-        wait(fullB + s, it & 1);
+      int it = 0, seg = 0;
+      for (int u = lo; u < hi; ++seg) {
+        int t, k0, k1;
+        segment(u, t, k0, k1);
+        if (seg > 0) wait(tfree, (seg - 1) & 1);  // the previous segment's accumulator is read
         tc_fence_after();
-        const uint32_t sa = smem_u32(smem + s * Cfg::kStageBytes);
-        const uint64_t bd = umma_desc_sw128(sa + NSUB * kTcABytes);
+        for (int kb = k0; kb < k1; ++kb, ++it) {
+          const int s = it % S, ph = it / S;
+          wait(fullA + s, ph & 1);
+          wait(fullB + s, ph & 1);
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + s * Cfg::kStageBytes);
+          const uint64_t bd = umma_desc_sw128(sa + NSUB * kTcABytes);
 #pragma unroll
-        for (int k = 0; k < kTcBK / 16; ++k)
+          for (int k = 0; k < kTcBK / 16; ++k)
 #pragma unroll
-          for (int sub = 0; sub < NSUB; ++sub)
-            tc_mma(tmem_d + sub * BN, umma_desc_sw128(sa + sub * kTcABytes) + 2 * k, bd + 2 * k,
-                   Cfg::kIdesc, (kb | k) != 0);
-        tc_commit(empty + s);
+            for (int sub = 0; sub < NSUB; ++sub)
+              tc_mma(tmem_d + sub * BN, umma_desc_sw128(sa + sub * kTcABytes) + 2 * k, bd + 2 * k,
+                     Cfg::kIdesc, (kb != k0) || (k != 0));
+          tc_commit(empty + s);
+        }
+        tc_commit(accum);
+        u += k1 - k0;
       }
-      tc_commit(accum);
     }
     __syncwarp();
   } else {
@@ -209,88 +249,182 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     constexpr int WPT = 4 / Cfg::kThreadsPerRow;  // packed words per thread per k-block
     const int d = (threadIdx.x - 64) % BN;
     const int wq = ((threadIdx.x - 64) / BN) * WPT;  // first word of this thread
-    const int row = n0 + d;
-    const bool valid = row < a.N;
-    const uint4* wrow = reinterpret_cast<const uint4*>(a.w + (int64_t)(valid ? row : 0) * (a.K / 16));
-    const __half* srow = a.scales + (int64_t)(valid ? row : 0) * a.G;
-    const __half* brow = a.biases + (int64_t)(valid ? row : 0) * a.G;
-    const uint32_t* wrow32 = reinterpret_cast<const uint32_t*>(wrow) + wq;
-    auto load_words = [&](int kb, uint32_t (&wv)[WPT]) {
-      if constexpr (WPT == 4) {
-        const uint4 u = __ldg(wrow + kb);
-        wv[0] = u.x;
-        wv[1] = u.y;
-        wv[2] = u.z;
-        wv[3] = u.w;
-      } else {
-        const uint2 u = __ldg(reinterpret_cast<const uint2*>(wrow32 + kb * 4));
-        wv[0] = u.x; wv[1] = u.y;
-      }
-    };
-    uint32_t cur[WPT];
-    if (valid) load_words(0, cur);
-    else
-#pragma unroll
-      for (int j = 0; j < WPT; ++j) cur[j] = 0;
-    for (int kb = 0; kb < nkb; ++kb) {
-      const int s = kb % S, it = kb / S;
-      uint32_t nxt[WPT];
-#pragma unroll
-      for (int j = 0; j < WPT; ++j) nxt[j] = 0;
-      if (valid && kb + 1 < nkb) load_words(kb + 1, nxt);
-      const __half sv = srow[kb >> 1], bv = brow[kb >> 1];
-      if (it > 0) wait(empty + s, (it - 1) & 1);
-      const uint32_t bt = smem_u32(smem + s * Cfg::kStageBytes + NSUB * kTcABytes) + d * 128;
-      const uint32_t sw = d & 7;
-#pragma unroll
-      for (int jj = 0; jj < WPT; ++jj) {
-        const int j = wq + jj;  // word of the row's 64-k slice: 16-byte chunks 2j, 2j+1
-        uint32_t o[8];
-        if (valid) {
-          decode_word_affine(cur[jj], __half2half2(sv), __half2half2(bv), o);
-        } else {
-#pragma unroll
-          for (int p = 0; p < 8; ++p) o[p] = 0;
-        }
-        sts128(bt + (((2 * j) ^ sw) << 4), o[0], o[1], o[2], o[3]);
-        sts128(bt + (((2 * j + 1) ^ sw) << 4), o[4], o[5], o[6], o[7]);
-      }
-      fence_proxy_async_smem();
-      mbar_arrive(fullB + s);
-#pragma unroll
-      for (int j = 0; j < WPT; ++j) cur[j] = nxt[j];
-    }
-    // ---- epilogue: TMEM -> fp16 y ----
-    wait(accum, 0);
-    tc_fence_after();
     const int q = warp & 3;                 // TMEM lane quarter this warp may read
     const int part = (warp - 2) >> 2;       // which half of the columns / which subtile
     const int sub = NSUB == 2 ? part : 0;
     const int c0 = NSUB == 2 ? 0 : part * (BN / 2);
-    const int tok = m0 + sub * kTcBM + q * 32 + lane;
-    const bool vec = (a.N % 8) == 0;
-#pragma unroll 1
-    for (int c = 0; c < (NSUB == 2 ? BN : BN / 2); c += 32) {
-      uint32_t r[32];
-      tc_ld32(tmem_d + ((uint32_t)(q * 32) << 16) + (uint32_t)(sub * BN + c0 + c), r);
-      const int n = n0 + c0 + c;
-      if (tok < a.M && n < a.N) {
+    const int lrow = sub * kTcBM + q * 32 + lane;  // token row within the tile
+    int it = 0, seg = 0;
+    for (int u = lo; u < hi; ++seg) {
+      int t, k0, k1;
+      segment(u, t, k0, k1);
+      const int n0 = (t % a.tiles_n) * BN, m0 = (t / a.tiles_n) * (NSUB * kTcBM);
+      const int row = n0 + d;
+      const bool valid = row < a.N;
+      const uint4* wrow = reinterpret_cast<const uint4*>(a.w + (int64_t)(valid ? row : 0) * (a.K / 16));
+      const __half* srow = a.scales + (int64_t)(valid ? row : 0) * a.G;
+      const __half* brow = a.biases + (int64_t)(valid ? row : 0) * a.G;
+      const uint32_t* wrow32 = reinterpret_cast<const uint32_t*>(wrow) + wq;
+      auto load_words = [&](int kb, uint32_t (&wv)[WPT]) {
+        if constexpr (WPT == 4) {
+          const uint4 v = __ldg(wrow + kb);
+          wv[0] = v.x;
+          wv[1] = v.y;
+          wv[2] = v.z;
+          wv[3] = v.w;
+        } else {
+          const uint2 v = __ldg(reinterpret_cast<const uint2*>(wrow32 + kb * 4));
+          wv[0] = v.x;
+          wv[1] = v.y;
+        }
+      };
+      // words two k-blocks ahead, scale and bias one group (two k-blocks) ahead: these loads
+      // go to HBM when the weights are read once, and the decode of a k-block must not wait
+      // for them
+      auto load_sb = [&](int grp, __half& sv, __half& bv) {
+        const bool in = valid && 2 * grp < nkb;
+        sv = in ? srow[grp] : __ushort_as_half(0);
+        bv = in ? brow[grp] : __ushort_as_half(0);
+      };
+      uint32_t cur[WPT], nx1[WPT];
+#pragma unroll
+      for (int j = 0; j < WPT; ++j) cur[j] = nx1[j] = 0;
+      if (valid) load_words(k0, cur);
+      if (valid && k0 + 1 < k1) load_words(k0 + 1, nx1);
+      __half s_cur, b_cur, s_nxt, b_nxt;
+      load_sb(k0 >> 1, s_cur, b_cur);
+      load_sb((k0 >> 1) + 1, s_nxt, b_nxt);
+      for (int kb = k0; kb < k1; ++kb, ++it) {
+        const int s = it % S, ph = it / S;
+        uint32_t nx2[WPT];
+#pragma unroll
+        for (int j = 0; j < WPT; ++j) nx2[j] = 0;
+        if (valid && kb + 2 < k1) load_words(kb + 2, nx2);
+        if (ph > 0) wait(empty + s, (ph - 1) & 1);
+        const uint32_t bt = smem_u32(smem + s * Cfg::kStageBytes + NSUB * kTcABytes) + d * 128;
+        const uint32_t sw = d & 7;
+#pragma unroll
+        for (int jj = 0; jj < WPT; ++jj) {
+          const int j = wq + jj;  // word of the row's 64-k slice: 16-byte chunks 2j, 2j+1
+          uint32_t o[8];
+          decode_word_affine(cur[jj], __half2half2(s_cur), __half2half2(b_cur), o);  // a row past N gives 0
+          sts128(bt + (((2 * j) ^ sw) << 4), o[0], o[1], o[2], o[3]);
+          sts128(bt + (((2 * j + 1) ^ sw) << 4), o[4], o[5], o[6], o[7]);
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(fullB + s);
+#pragma unroll
+        for (int j = 0; j < WPT; ++j) {
+          cur[j] = nx1[j];
+          nx1[j] = nx2[j];
+        }
+        if (kb & 1) {  // the next k-block starts a new scale group
+          s_cur = s_nxt;
+          b_cur = b_nxt;
+          load_sb((kb >> 1) + 2, s_nxt, b_nxt);
+        }
+      }
+
+      // ---- epilogue of the segment: TMEM -> fp16 y; a split tile goes through the parts ----
+      wait(accum, seg & 1);
+      tc_fence_after();
+      const bool whole = k0 == 0 && k1 == nkb;
+      const int tok = m0 + lrow;
+      constexpr int CW = NSUB == 2 ? BN : BN / 2;  // columns this thread drains
+      // 32 accumulator columns (from c) to fp16 y
+      auto store_y = [&](int c, const float (&f)[32]) {
+        const int n = n0 + c0 + c;
+        if (tok >= a.M || n >= a.N) return;
         __half* dst = a.y + (int64_t)tok * a.N + n;
-        if (vec && n + 32 <= a.N) {
+        if ((a.N % 8) == 0 && n + 32 <= a.N) {
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
             uint32_t h[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-              h[e] = pack_half2(__uint_as_float(r[8 * v + 2 * e]), __uint_as_float(r[8 * v + 2 * e + 1]));
+            for (int e = 0; e < 4; ++e) h[e] = pack_half2(f[8 * v + 2 * e], f[8 * v + 2 * e + 1]);
             *reinterpret_cast<uint4*>(dst + 8 * v) = make_uint4(h[0], h[1], h[2], h[3]);
           }
         } else {
 #pragma unroll
           for (int e = 0; e < 32; ++e)
-            if (n + e < a.N) dst[e] = __float2half_rn(__uint_as_float(r[e]));
+            if (n + e < a.N) dst[e] = __float2half_rn(f[e]);
+        }
+      };
+      auto tmem_cols = [&](int c, float (&f)[32]) {
+        uint32_t r[32];
+        tc_ld32(tmem_d + ((uint32_t)(q * 32) << 16) + (uint32_t)(sub * BN + c0 + c), r);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) f[e] = __uint_as_float(r[e]);
+      };
+      if (whole) {
+#pragma unroll 1
+        for (int c = 0; c < CW; c += 32) {
+          float f[32];
+          tmem_cols(c, f);
+          store_y(c, f);
+        }
+      } else {
+        // A split tile: each contributor writes its part; the last to count in adds the
+        // parts in CTA order (its own from tensor memory), so the sum does not depend on the
+        // order of arrival, and writes y.
+        float* mine = a.part + ((int64_t)blockIdx.x * 2 + (u == lo ? 0 : 1)) * kPartFloats;
+#pragma unroll 1
+        for (int c = 0; c < CW; c += 32) {
+          float f[32];
+          tmem_cols(c, f);
+          float4* dst = reinterpret_cast<float4*>(mine + (int64_t)lrow * BN + c0 + c);
+#pragma unroll
+          for (int v = 0; v < 8; ++v) __stcg(dst + v, make_float4(f[4 * v], f[4 * v + 1], f[4 * v + 2], f[4 * v + 3]));
+        }
+        asm volatile("bar.sync 2, 256;" ::: "memory");
+        const int first = sk_owner(t * nkb, units, grid);
+        const int lastc = sk_owner(t * nkb + nkb - 1, units, grid);
+        if (threadIdx.x == 64) {
+          fence_acq_rel_gpu();
+          last_flag = atomicAdd(a.count + t, 1) == lastc - first;
+          if (last_flag) {
+            fence_acq_rel_gpu();
+            a.count[t] = 0;
+          }
+        }
+        asm volatile("bar.sync 2, 256;" ::: "memory");
+        if (last_flag) {
+#pragma unroll 1
+          for (int c = 0; c < CW; c += 32) {
+            float f[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) f[e] = 0.f;
+            for (int cc = first; cc <= lastc; ++cc) {
+              if (cc == (int)blockIdx.x) {
+                float m[32];
+                tmem_cols(c, m);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) f[e] += m[e];
+              } else {
+                const int slot = sk_lo(cc, units, grid) / nkb == t ? 0 : 1;
+                const float4* op = reinterpret_cast<const float4*>(
+                    a.part + ((int64_t)cc * 2 + slot) * kPartFloats + (int64_t)lrow * BN + c0 + c);
+                float4 o[8];
+#pragma unroll
+                for (int v = 0; v < 8; ++v) o[v] = __ldcg(op + v);
+#pragma unroll
+                for (int v = 0; v < 8; ++v) {
+                  f[4 * v] += o[v].x;
+                  f[4 * v + 1] += o[v].y;
+                  f[4 * v + 2] += o[v].z;
+                  f[4 * v + 3] += o[v].w;
+                }
+              }
+            }
+            store_y(c, f);
+          }
         }
       }
+      // the accumulator is read: the next segment's first mma may overwrite it
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tfree);
+      u += k1 - k0;
     }
   }
 
@@ -324,12 +458,33 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_tiled_fn() {
   return fn;
 }
 
-size_t gemm_tc_workspace(int64_t M, int64_t K) { return (size_t)M * (size_t)K * 2; }
+// Workspace of the tensor-core path (after the caller's fixup region):
+//   x'      fp16 [M, K], rotated activations;
+//   counts  int32 per output tile of the smallest tile shape (128 x 128), zero before a call
+//           and after it;
+//   parts   fp32 [SMs][2][256 x 256], the stream-K parts of split tiles (scratch).
+static int64_t tc_sms_bound() {
+  DeviceFacts f;
+  return device_facts(&f) == TB_OK ? f.sms : 256;  // no device: the largest SM count supported
+}
+static size_t rup256(size_t v) { return (v + 255) / 256 * 256; }
+static size_t tc_x_bytes(int64_t M, int64_t K) { return rup256((size_t)M * (size_t)K * 2); }
+static size_t tc_count_bytes(int64_t M, int64_t N) {
+  return rup256((size_t)((M + kTcBM - 1) / kTcBM) * (size_t)((N + 127) / 128) * 4);
+}
+static size_t tc_part_bytes() { return (size_t)tc_sms_bound() * 2 * (2 * kTcBM) * 256 * 4; }
 
-// the GEMM alone, on x' already rotated into pair order in xp (fp16 [M, K])
+size_t gemm_tc_x_bytes(int64_t M, int64_t K) { return tc_x_bytes(M, K); }
+
+size_t gemm_tc_workspace(int64_t M, int64_t K, int64_t N) {
+  return tc_x_bytes(M, K) + tc_count_bytes(M, N) + tc_part_bytes();
+}
+
+// the GEMM alone, on x' already rotated into pair order in xp (fp16 [M, K]); `gws` is the
+// workspace after x' (counts, then parts)
 int launch_gemm_tc_rotated(const __half* xp, int64_t M, int64_t K, const uint32_t* w,
                            const __half* scales, const __half* biases, int64_t N, __half* y,
-                           int32_t* status, cudaStream_t s) {
+                           void* gws, int32_t* status, cudaStream_t s) {
   if (M > 0x7fffffffLL || N > 0x7fffffffLL || K > (1 << 24)) return TB_ERR_SHAPE;
 
   CUtensorMap tm;
@@ -345,22 +500,36 @@ int launch_gemm_tc_rotated(const __half* xp, int64_t M, int64_t K, const uint32_
                                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (cr != CUDA_SUCCESS) return TB_ERR_CUDA;
 
-  // Tile choice: two 128-token subtiles per CTA halve the decode work per flop; 256-row
-  // weight tiles halve the activation reads per flop; both only while the grid still fills
-  // the SMs (about one CTA each).
+  // Tile shape and schedule.  Above 128 tokens: 256 x 256 tiles (two 128-token subtiles share
+  // each decoded weight tile, which halves the decode work and the activation reads per flop
+  // of smaller tiles; the per-k-block decode then hides behind the k-block's mma), as stream-K
+  // over the SMs when every SM gets a tile, one CTA per tile when the tiles fill most of the
+  // SMs, else every tile split into q <= 4 k-ranges.  Up to 128 tokens: 128 x 256 tiles the
+  // same way, else 128 x 128 tiles, one CTA each or stream-K when there are more than SMs.
   DeviceFacts f;
   int rcf = device_facts(&f);
   if (rcf != TB_OK) return rcf;
-  auto ctas = [&](int nsub, int bn) { return ((N + bn - 1) / bn) * ((M + nsub * kTcBM - 1) / (nsub * kTcBM)); };
-  const int64_t full = (int64_t)f.sms * 4 / 5;
+  if (f.sms > 256) return TB_ERR_TOO_LARGE;
   const int64_t sms = f.sms;
-  auto ok128 = [&](int64_t c) { return c >= full && (c <= sms || c >= 3 * sms); };  // no near-empty last wave
+  auto tiles = [&](int ns, int b) { return ((M + ns * kTcBM - 1) / (ns * kTcBM)) * ((N + b - 1) / b); };
   int nsub = 1, bn = 256;
-  if (M > kTcBM && ctas(2, 256) >= full) { nsub = 2; bn = 256; }
-  else if (M > kTcBM && ok128(ctas(2, 128))) { nsub = 2; bn = 128; }
-  else if (ctas(1, 256) >= full) { nsub = 1; bn = 256; }
-  else if (ctas(1, 128) <= sms) { nsub = 1; bn = 128; }
-  TcArgs a;
+  int64_t grid64 = 0;  // 0: one CTA per tile
+  const int64_t full = sms * 4 / 5;
+  auto ok128 = [&](int64_t c) { return c >= full && (c <= sms || c >= 3 * sms); };
+  if (M > kTcBM) {
+    nsub = 2;
+    const int64_t T2 = tiles(2, 256);
+    if (T2 >= sms) grid64 = sms;                            // stream-K, two CTAs per tile at most
+    else if (T2 < full) grid64 = T2 * std::min<int64_t>(4, sms / T2);  // q-way split of every tile
+  } else if (tiles(1, 256) >= sms) { grid64 = sms; }
+  else if (tiles(1, 256) >= full) {}
+  else if (ok128(tiles(1, 128)) || tiles(1, 128) < sms) { bn = 128; }
+  else { bn = 128; grid64 = sms; }
+  const int64_t T = tiles(nsub, bn);
+  const int64_t nkb = K / kTcBK;
+  if (T * nkb > 0x7fffffffLL) return TB_ERR_SHAPE;
+  const int grid = (int)(grid64 ? grid64 : T);
+  TcSkArgs a;
   a.w = w;
   a.scales = scales;
   a.biases = biases;
@@ -369,16 +538,18 @@ int launch_gemm_tc_rotated(const __half* xp, int64_t M, int64_t K, const uint32_
   a.N = (int)N;
   a.K = (int)K;
   a.G = (int)(K / kGroup);
+  a.tiles_n = (int)((N + bn - 1) / bn);
+  a.nkb = (int)nkb;
+  a.units = (int)(T * nkb);
+  a.count = static_cast<int*>(gws);
+  a.part = reinterpret_cast<float*>(static_cast<char*>(gws) + tc_count_bytes(M, N));
   a.status = status;
   cudaError_t e = cudaSuccess;
-  const unsigned gm = (unsigned)((M + nsub * kTcBM - 1) / (nsub * kTcBM));
-  const unsigned gn = (unsigned)((N + bn - 1) / bn);
 #define TB_LAUNCH_TC(NS, B)                                                                        \
   do {                                                                                            \
     e = cudaFuncSetAttribute(w2_gemm_tc_kernel<NS, B>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
                              TcCfg<NS, B>::kSmem);                                                 \
-    if (e == cudaSuccess)                                                                         \
-      w2_gemm_tc_kernel<NS, B><<<dim3(gn, gm), kTcThreads, TcCfg<NS, B>::kSmem, s>>>(tm, a);       \
+    if (e == cudaSuccess) w2_gemm_tc_kernel<NS, B><<<grid, kTcThreads, TcCfg<NS, B>::kSmem, s>>>(tm, a); \
   } while (0)
   if (nsub == 2 && bn == 256) TB_LAUNCH_TC(2, 256);
   else if (nsub == 2) TB_LAUNCH_TC(2, 128);
@@ -399,7 +570,8 @@ int launch_gemm_tc(const __half* x, int64_t M, int64_t K, const int8_t* signs, i
   __half* xp = static_cast<__half*>(workspace);
   int rc = launch_rotate_pairorder(x, xp, signs, M, K, block != 0, s);
   if (rc != TB_OK) return rc;
-  return launch_gemm_tc_rotated(xp, M, K, w, scales, biases, N, y, status, s);
+  return launch_gemm_tc_rotated(xp, M, K, w, scales, biases, N, y,
+                                static_cast<char*>(workspace) + tc_x_bytes(M, K), status, s);
 }
 
 }  // namespace tb

@@ -18,7 +18,8 @@ int launch_gemv(const __half* x, int64_t M, int64_t K, const int8_t* signs, int 
 int launch_gemm_tc(const __half* x, int64_t M, int64_t K, const int8_t* signs, int block,
                    const uint32_t* w, const __half* scales, const __half* biases, int64_t N,
                    __half* y, void* workspace, int32_t* status, cudaStream_t s);
-size_t gemm_tc_workspace(int64_t M, int64_t K);
+size_t gemm_tc_workspace(int64_t M, int64_t K, int64_t N);
+size_t gemm_tc_x_bytes(int64_t M, int64_t K);
 int launch_gemv_tma(const __half* x, int64_t M, int64_t K, const int8_t* signs, int block,
                     const uint32_t* w, const __half* scales, const __half* biases, int64_t N,
                     __half* y, void* workspace, size_t ws_bytes, int32_t* status, cudaStream_t s);
@@ -31,7 +32,7 @@ int launch_rotate_pairorder(const __half* x, __half* out, const int8_t* signs, i
                             int64_t K, int rotate, cudaStream_t s);
 int launch_gemm_tc_rotated(const __half* xp, int64_t M, int64_t K, const uint32_t* w,
                            const __half* scales, const __half* biases, int64_t N, __half* y,
-                           int32_t* status, cudaStream_t s);
+                           void* gws, int32_t* status, cudaStream_t s);
 constexpr int kMaxMulti = 4;
 
 // Workspace layout: [fixup region of the GEMV split schedule (zero before the first call,
@@ -59,7 +60,7 @@ extern "C" size_t tb_packed_linear_algo_workspace_size(int64_t M, int64_t K, int
                                                        int algo) {
   using namespace tb;
   if (check_linear_shape(M, K, block, N) != TB_OK) return 0;
-  return fixup_region() + (resolve_algo(M, algo) == TB_ALGO_TC ? gemm_tc_workspace(M, K) : 0);
+  return fixup_region() + (resolve_algo(M, algo) == TB_ALGO_TC ? gemm_tc_workspace(M, K, N) : 0);
 }
 
 extern "C" size_t tb_packed_linear_workspace_size(int64_t M, int64_t K, int64_t N, int block) {
@@ -87,7 +88,7 @@ extern "C" int tb_packed_linear_algo(const uint16_t* x, int64_t M, int64_t K, co
   const __half* bh = reinterpret_cast<const __half*>(biases);
   __half* yh = reinterpret_cast<__half*>(y);
   if (use == TB_ALGO_TC) {
-    const size_t need = fixup_region() + gemm_tc_workspace(M, K);
+    const size_t need = fixup_region() + gemm_tc_workspace(M, K, N);
     if (!workspace || workspace_bytes < need) return TB_ERR_WORKSPACE;
     return launch_gemm_tc(xh, M, K, sg, block, w, sh, bh, N, yh,
                           static_cast<char*>(workspace) + fixup_region(), dev_status, s);
@@ -137,11 +138,14 @@ extern "C" int tb_packed_linear_multi(const uint16_t* x, int64_t M, int64_t K, c
     return launch_gemv_tma_multi(xh, M, K, sg, block, n, w, sh, bh, N, yh, workspace, workspace_bytes,
                                  dev_status, s);
   // prefill: one rotation of x into the workspace, then one GEMM per matrix
-  const size_t need = fixup_region() + gemm_tc_workspace(M, K);
+  int64_t maxN = 0;
+  for (int i = 0; i < n; ++i) maxN = N[i] > maxN ? N[i] : maxN;
+  const size_t need = fixup_region() + gemm_tc_workspace(M, K, maxN);
   if (!workspace || workspace_bytes < need) return TB_ERR_WORKSPACE;
   __half* xp = reinterpret_cast<__half*>(static_cast<char*>(workspace) + fixup_region());
+  void* gws = static_cast<char*>(workspace) + fixup_region() + gemm_tc_x_bytes(M, K);
   int rc = launch_rotate_pairorder(xh, xp, sg, M, K, block != 0, s);
   for (int i = 0; i < n && rc == TB_OK; ++i)
-    rc = launch_gemm_tc_rotated(xp, M, K, w[i], sh[i], bh[i], N[i], yh[i], dev_status, s);
+    rc = launch_gemm_tc_rotated(xp, M, K, w[i], sh[i], bh[i], N[i], yh[i], gws, dev_status, s);
   return rc;
 }

@@ -87,9 +87,21 @@ def test_workspace_size_query(lib):
     fix = ws(1, 5120, 17408, 1024)                  # decode path: the fixup region only
     assert 1024 < fix <= 3 << 20 and fix % 1024 == 0
     assert ws(8, 5120, 17408, 1024) == fix
-    assert ws(512, 5120, 17408, 1024) == fix + 512 * 5120 * 2
+    # tensor-core path: x' (fp16 [M, K]), one counter per 128 x 128 output tile, then two
+    # fp32 256 x 256 parts per SM for the stream-K schedule's split tiles (with no GPU visible
+    # the bound is 256 SMs), each region rounded up to 256 bytes
+    def up(v):
+        return (v + 255) // 256 * 256
+
+    def tc(M, K, N, sms):
+        return up(M * K * 2) + up(-(-M // 128) * -(-N // 128) * 4) + sms * 2 * 256 * 256 * 4
+
+    big = ws(512, 5120, 17408, 1024)
+    sms = (big - fix - up(512 * 5120 * 2) - up(4 * 136 * 4)) // (2 * 256 * 256 * 4)
+    assert 1 <= sms <= 256
+    assert big == fix + tc(512, 5120, 17408, sms)
     assert ws(512, 1000, 17408, 1024) == 0          # invalid shape -> 0
-    assert lib.tb_packed_linear_algo_workspace_size(4, 2048, 64, 1024, 2) == fix + 4 * 2048 * 2
+    assert lib.tb_packed_linear_algo_workspace_size(4, 2048, 64, 1024, 2) == fix + tc(4, 2048, 64, sms)
 
 
 def test_other_entry_points_refuse_bad_arguments(lib):

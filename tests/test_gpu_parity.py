@@ -55,6 +55,12 @@ def run_linear(tb, x16, signs, block, w, s, b, N, algo=0, workspace="zeros", rep
     assert int(st.item()) == 0
     if ws is not None:  # the counters of shared output tiles are left zero for the next call
         assert int(ws[:1024].count_nonzero().item()) == 0
+        if algo == 2 or (algo == 0 and M > 8):
+            # tensor-core path: after the 2 MB fixup region and x' (rounded up to 256 bytes)
+            # come the stream-K tile counters, left zero as well
+            c0 = 2098176 + (M * K * 2 + 255) // 256 * 256
+            nc = -(-M // 128) * -(-N // 128)
+            assert int(ws[c0:c0 + 4 * nc].count_nonzero().item()) == 0
     if repeat > 1:
         return [o.cpu().numpy() for o in outs]
     return outs[0].cpu().numpy()
@@ -239,6 +245,24 @@ def test_linear_tc_tiles(tb, M, K, N):
     ref, bound = linear_reference(x, sg, 1024, L)
     mx, rms = assert_linear_close(y, ref, bound, f"tc {M}x{K}x{N}")
     assert rms < 2e-3, rms
+
+
+@pytest.mark.parametrize("M,K,N", [(100, 2048, 20000), (300, 1024, 19500), (260, 2048, 40000), (40, 1024, 40000)])
+def test_linear_tc_stream_k_split_tiles(tb, M, K, N):
+    # at least one output tile per SM (128 x 128, 256 x 256 and 128 x 256 tiles): the stream-K
+    # schedule cuts tiles between two CTAs and the second one adds the other's part; ragged
+    # token and row tails; the same workspace serves two calls in a row (the tiles' counters
+    # are left zero), and the two results are identical (two addends: the order in which the
+    # CTAs count in does not change the sum)
+    x = ti.activations(M + 7, M, K)
+    sg = ti.rademacher_signs(9, K)
+    L = HostLayer(M + N, N, K)
+    w, s, b = device_layer(M + N, N, K, from_host=L)
+    y1, y2 = run_linear(tb, x, sg, 1024, w, s, b, N, algo=2, repeat=2)
+    ref, bound = linear_reference(x, sg, 1024, L)
+    mx, rms = assert_linear_close(y1, ref, bound, f"stream-K {M}x{K}x{N}")
+    assert rms < 2e-3, rms
+    np.testing.assert_array_equal(y1.view(np.uint16), y2.view(np.uint16))
 
 
 @pytest.mark.parametrize("M,K,N", [(512, 5120, 17408), (512, 17408, 5120), (4096, 5120, 17408),
