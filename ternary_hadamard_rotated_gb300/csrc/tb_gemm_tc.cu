@@ -98,7 +98,8 @@ TB_DEVI void decode_word_affine(uint32_t w, __half2 s2, __half2 b2, uint32_t (&o
 }
 
 // NSUB M-subtiles of 128 tokens share every decoded B tile (NSUB = 2: 256 tokens per CTA,
-// the decode cost per flop halves).  Stage s holds A[sub] (16 KB each) then B (32 KB).
+// the decode cost per flop halves).  Stage s holds A[sub] (16 KB each), then B decoded
+// (BN x 64 fp16).
 template <int NSUB, int BN>
 struct TcCfg {
   static constexpr int kBBytes = BN * kTcBK * 2;
@@ -261,9 +262,34 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int n0 = (t % a.tiles_n) * BN, m0 = (t / a.tiles_n) * (NSUB * kTcBM);
       const int row = n0 + d;
       const bool valid = row < a.N;
-      const uint4* wrow = reinterpret_cast<const uint4*>(a.w + (int64_t)(valid ? row : 0) * (a.K / 16));
       const __half* srow = a.scales + (int64_t)(valid ? row : 0) * a.G;
       const __half* brow = a.biases + (int64_t)(valid ? row : 0) * a.G;
+      // scales and biases of eight groups (16 k-blocks) per load, the next eight loaded while
+      // these are used: the loads go to HBM when the weights are read once
+      const bool vec8 = (a.G % 8) == 0;
+      auto load_sb8 = [&](int gb, uint4& sv, uint4& bv) {
+        if (valid && vec8 && 8 * gb < a.G) {
+          sv = __ldg(reinterpret_cast<const uint4*>(srow) + gb);
+          bv = __ldg(reinterpret_cast<const uint4*>(brow) + gb);
+        } else {
+          uint16_t hs[8], hb[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const bool in = valid && 8 * gb + e < a.G;
+            hs[e] = in ? __half_as_ushort(srow[8 * gb + e]) : 0;
+            hb[e] = in ? __half_as_ushort(brow[8 * gb + e]) : 0;
+          }
+          sv = make_uint4(hs[0] | (uint32_t)hs[1] << 16, hs[2] | (uint32_t)hs[3] << 16,
+                          hs[4] | (uint32_t)hs[5] << 16, hs[6] | (uint32_t)hs[7] << 16);
+          bv = make_uint4(hb[0] | (uint32_t)hb[1] << 16, hb[2] | (uint32_t)hb[3] << 16,
+                          hb[4] | (uint32_t)hb[5] << 16, hb[6] | (uint32_t)hb[7] << 16);
+        }
+      };
+      auto pick = [](const uint4& v, int g) {  // fp16 number g (0..7) of eight
+        const uint32_t w2 = (g >> 2) ? ((g >> 1) & 1 ? v.w : v.z) : ((g >> 1) & 1 ? v.y : v.x);
+        return __ushort_as_half((uint16_t)((g & 1) ? (w2 >> 16) : (w2 & 0xFFFFu)));
+      };
+      const uint4* wrow = reinterpret_cast<const uint4*>(a.w + (int64_t)(valid ? row : 0) * (a.K / 16));
       const uint32_t* wrow32 = reinterpret_cast<const uint32_t*>(wrow) + wq;
       auto load_words = [&](int kb, uint32_t (&wv)[WPT]) {
         if constexpr (WPT == 4) {
@@ -278,22 +304,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           wv[1] = v.y;
         }
       };
-      // words two k-blocks ahead, scale and bias one group (two k-blocks) ahead: these loads
-      // go to HBM when the weights are read once, and the decode of a k-block must not wait
-      // for them
-      auto load_sb = [&](int grp, __half& sv, __half& bv) {
-        const bool in = valid && 2 * grp < nkb;
-        sv = in ? srow[grp] : __ushort_as_half(0);
-        bv = in ? brow[grp] : __ushort_as_half(0);
-      };
+      // packed words two k-blocks ahead (the loads go to HBM when the weights are read once)
       uint32_t cur[WPT], nx1[WPT];
 #pragma unroll
       for (int j = 0; j < WPT; ++j) cur[j] = nx1[j] = 0;
       if (valid) load_words(k0, cur);
       if (valid && k0 + 1 < k1) load_words(k0 + 1, nx1);
-      __half s_cur, b_cur, s_nxt, b_nxt;
-      load_sb(k0 >> 1, s_cur, b_cur);
-      load_sb((k0 >> 1) + 1, s_nxt, b_nxt);
+      uint4 s_cur, b_cur, s_nxt, b_nxt;
+      load_sb8(k0 >> 4, s_cur, b_cur);
+      load_sb8((k0 >> 4) + 1, s_nxt, b_nxt);
       for (int kb = k0; kb < k1; ++kb, ++it) {
         const int s = it % S, ph = it / S;
         uint32_t nx2[WPT];
@@ -301,27 +320,32 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int j = 0; j < WPT; ++j) nx2[j] = 0;
         if (valid && kb + 2 < k1) load_words(kb + 2, nx2);
         if (ph > 0) wait(empty + s, (ph - 1) & 1);
-        const uint32_t bt = smem_u32(smem + s * Cfg::kStageBytes + NSUB * kTcABytes) + d * 128;
+        const uint32_t stage = smem_u32(smem + s * Cfg::kStageBytes);
+        uint32_t wv[WPT];
+#pragma unroll
+        for (int j = 0; j < WPT; ++j) {
+          wv[j] = cur[j];
+          cur[j] = nx1[j];
+          nx1[j] = nx2[j];
+        }
+        const int g = (kb >> 1) & 7;
+        const __half sv = pick(s_cur, g), bv = pick(b_cur, g);
+        const uint32_t bt = stage + NSUB * kTcABytes + d * 128;
         const uint32_t sw = d & 7;
 #pragma unroll
         for (int jj = 0; jj < WPT; ++jj) {
           const int j = wq + jj;  // word of the row's 64-k slice: 16-byte chunks 2j, 2j+1
           uint32_t o[8];
-          decode_word_affine(cur[jj], __half2half2(s_cur), __half2half2(b_cur), o);  // a row past N gives 0
+          decode_word_affine(wv[jj], __half2half2(sv), __half2half2(bv), o);  // a row past N gives 0
           sts128(bt + (((2 * j) ^ sw) << 4), o[0], o[1], o[2], o[3]);
           sts128(bt + (((2 * j + 1) ^ sw) << 4), o[4], o[5], o[6], o[7]);
         }
         fence_proxy_async_smem();
         mbar_arrive(fullB + s);
-#pragma unroll
-        for (int j = 0; j < WPT; ++j) {
-          cur[j] = nx1[j];
-          nx1[j] = nx2[j];
-        }
-        if (kb & 1) {  // the next k-block starts a new scale group
+        if ((kb & 15) == 15) {  // the next k-block starts a new block of eight groups
           s_cur = s_nxt;
           b_cur = b_nxt;
-          load_sb((kb >> 1) + 2, s_nxt, b_nxt);
+          load_sb8((kb >> 4) + 2, s_nxt, b_nxt);
         }
       }
 
