@@ -135,9 +135,6 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
   if (warp == kTmaConsumers) {
     // ---- producer: the packed weights never depend on the previous kernel ----
     if (lane == 0) {
-      // units per group issued before the activations are read: kPreIssue, or none with a
-      // single slot per group (the consumers' transform uses the group's free slot)
-      const int pre = DW >= 2 ? kPreIssue : 0;
       const uint64_t pol = policy_evict_first();
       int tl[kGroupsOfWarps], ch[kGroupsOfWarps], cntu[kGroupsOfWarps];
       int maxcnt = 0;
@@ -152,7 +149,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         maxcnt = cntu[u] > maxcnt ? cntu[u] : maxcnt;
       }
       for (int n = 0, si = 0, k = 0; n < maxcnt; ++n) {  // si = n % DW, k = n / DW
-        if (n == pre) wait(xready, 0);  // the activations have been read
+        if (n == kPreIssue) wait(xready, 0);  // the activations have been read
 #pragma unroll
         for (int u = 0; u < kGroupsOfWarps; ++u) {
           if (n >= cntu[u]) continue;
@@ -225,17 +222,109 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
   asm volatile("griddepcontrol.wait;" ::: "memory");
   {
     // prologue: x' = fwht(signs * x) -> B-fragment image, (C, S) per group and token, for the
-    // 1024-blocks that this CTA's units read.  Scratch of the transform: the second ring slot
-    // of this warp's unit group (the only one with a single slot per group), which the
-    // producer fills only after every consumer warp has arrived on xready.
-    int b1, e1, b2, e2;
-    blocks_needed(lo, nst, C, K, b1, e1, b2, e2);
-    const uint32_t scratch = slots_u32 + (ug * DW + (DW >= 2 ? 1 : 0)) * kSlotBytes + wi * 4096;
-    prologue_image<MT>(a.x, a.signs, K, a.Mc, a.rotate, b1, e1, b2, e2, warp, kTmaConsumers, lane, img,
-                       cs, scratch);
-    fence_proxy_async_smem();  // the scratch's generic accesses before the copies that refill it
-    __syncwarp();
-    if (lane == 0) mbar_arrive(xready);  // the activations are read: the producer may stream on
+    // 1024-blocks that this CTA's units read.  Every consumer warp takes items (token, block)
+    // warp, warp + 12, ...; the loads of two items are issued before either is transformed,
+    // so a warp waits once per pair.
+    const int nb = K / kBlock;
+    int b1 = 0, e1 = nb, b2 = 0, e2 = 0;  // the blocks needed: [b1, e1) and [b2, e2)
+    if (nst > 0 && nst < C) {
+      constexpr int kChunksPerBlock = kBlock / (kUnitGroups * kGroup);
+      const int clo = lo % C, cend = clo + nst;
+      b1 = clo / kChunksPerBlock;
+      if (cend <= C) {
+        e1 = (cend - 1) / kChunksPerBlock + 1;
+      } else {
+        e2 = (cend - C - 1) / kChunksPerBlock + 1;
+        if (e2 >= b1) {
+          b1 = 0;
+          e2 = 0;
+        }
+      }
+    }
+    const int nblk = (e1 - b1) + (e2 - b2);
+    auto load_block = [&](int it, uint4 (&xr)[4], uint4 (&sr)[2]) {
+      const int tok = it / nblk, bi = it - tok * nblk;
+      const int b = bi < e1 - b1 ? b1 + bi : b2 + (bi - (e1 - b1));
+      if (tok < a.Mc) {
+        const uint4* xs = reinterpret_cast<const uint4*>(a.x + (int64_t)tok * K + b * kBlock + lane * 32);
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) xr[q4] = __ldg(xs + q4);
+      } else {
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) xr[q4] = make_uint4(0, 0, 0, 0);
+      }
+      if (a.signs) {
+        const uint4* sp = reinterpret_cast<const uint4*>(a.signs + b * kBlock + lane * 32);
+        sr[0] = __ldg(sp);
+        sr[1] = __ldg(sp + 1);
+      }
+    };
+    auto transform_block = [&](int it, const uint4 (&xr)[4], const uint4 (&sr)[2]) {
+      const int tok = it / nblk, bi = it - tok * nblk;
+      const int b = bi < e1 - b1 ? b1 + bi : b2 + (bi - (e1 - b1));
+      // layout A: v[r] = element b*1024 + lane*32 + r
+      float v[32];
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        const __half* h = reinterpret_cast<const __half*>(&xr[q4]);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[8 * q4 + e] = __half2float(h[e]);
+      }
+      if (a.signs) {
+        const int8_t* sg = reinterpret_cast<const int8_t*>(sr);
+#pragma unroll
+        for (int r = 0; r < 32; ++r)
+          if (sg[r] < 0) v[r] = -v[r];
+      }
+      if (a.rotate) {
+        wht1024_a_shfl(v, lane);  // all ten stages, layout A kept
+#pragma unroll
+        for (int r = 0; r < 32; ++r) v[r] *= kInvSqrtBlock;
+      }
+      const int grp = b * (kBlock / kGroup) + (lane >> 2);
+      float ssum = 0.f, csum = 0.f;
+#pragma unroll
+      for (int r = 0; r < 32; ++r) {
+        v[r] = __half2float(__float2half_rn(v[r]));  // x' rounded to fp16
+        ssum += v[r];
+      }
+      ssum += __shfl_xor_sync(0xffffffffu, ssum, 1);
+      ssum += __shfl_xor_sync(0xffffffffu, ssum, 2);
+#pragma unroll
+      for (int mp = 0; mp < 4; ++mp) {
+        uint32_t pk[4];
+#pragma unroll
+        for (int e2 = 0; e2 < 4; ++e2) {
+          const int p = 4 * (mp & 1) + e2;
+          const int r = (mp >> 1) * 16 + p;
+          const float is = inv_sigma_p(p);
+          const __half lo_ = __float2half_rn(v[r] * is), hi_ = __float2half_rn(v[r + 8] * is);
+          csum += __half2float(lo_) + __half2float(hi_);
+          pk[e2] = (uint32_t)__half_as_ushort(lo_) | ((uint32_t)__half_as_ushort(hi_) << 16);
+        }
+        *reinterpret_cast<uint4*>(img + ((size_t)(grp * 4 + mp) * MT + tok) * 32 + t * 8) =
+            make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      }
+      csum += __shfl_xor_sync(0xffffffffu, csum, 1);
+      csum += __shfl_xor_sync(0xffffffffu, csum, 2);
+      if (t == 0) cs[grp * MT + tok] = make_float2(1024.f * csum, ssum);
+    };
+    const int items = MT * nblk;
+    bool told = false;
+    for (int it = warp; it < items; it += 2 * kTmaConsumers) {
+      const int it2 = it + kTmaConsumers;
+      uint4 xa[4], sa[2], xb[4], sb2[2];
+      load_block(it, xa, sa);
+      if (it2 < items) load_block(it2, xb, sb2);
+      transform_block(it, xa, sa);
+      if (it2 < items) transform_block(it2, xb, sb2);
+      if (!told) {  // this warp's first activations are in: the producer may stream on
+        told = true;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(xready);
+      }
+    }
+    if (!told && lane == 0) mbar_arrive(xready);
     asm volatile("bar.sync 1, %0;" ::"n"(kTmaConsumers * 32) : "memory");
   }
 
