@@ -304,21 +304,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           wv[1] = v.y;
         }
       };
-      // packed words two k-blocks ahead (the loads go to HBM when the weights are read once)
-      uint32_t cur[WPT], nx1[WPT];
+      // packed words four k-blocks ahead (the loads go to HBM when the weights are read once)
+      uint32_t cur[WPT], nx1[WPT], nx2[WPT], nx3[WPT];
 #pragma unroll
-      for (int j = 0; j < WPT; ++j) cur[j] = nx1[j] = 0;
+      for (int j = 0; j < WPT; ++j) cur[j] = nx1[j] = nx2[j] = nx3[j] = 0;
       if (valid) load_words(k0, cur);
       if (valid && k0 + 1 < k1) load_words(k0 + 1, nx1);
+      if (valid && k0 + 2 < k1) load_words(k0 + 2, nx2);
+      if (valid && k0 + 3 < k1) load_words(k0 + 3, nx3);
       uint4 s_cur, b_cur, s_nxt, b_nxt;
       load_sb8(k0 >> 4, s_cur, b_cur);
       load_sb8((k0 >> 4) + 1, s_nxt, b_nxt);
       for (int kb = k0; kb < k1; ++kb, ++it) {
         const int s = it % S, ph = it / S;
-        uint32_t nx2[WPT];
+        uint32_t nx4[WPT];
 #pragma unroll
-        for (int j = 0; j < WPT; ++j) nx2[j] = 0;
-        if (valid && kb + 2 < k1) load_words(kb + 2, nx2);
+        for (int j = 0; j < WPT; ++j) nx4[j] = 0;
+        if (valid && kb + 4 < k1) load_words(kb + 4, nx4);
         if (ph > 0) wait(empty + s, (ph - 1) & 1);
         const uint32_t stage = smem_u32(smem + s * Cfg::kStageBytes);
         uint32_t wv[WPT];
@@ -327,6 +329,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           wv[j] = cur[j];
           cur[j] = nx1[j];
           nx1[j] = nx2[j];
+          nx2[j] = nx3[j];
+          nx3[j] = nx4[j];
         }
         const int g = (kb >> 1) & 7;
         const __half sv = pick(s_cur, g), bv = pick(b_cur, g);

@@ -218,6 +218,20 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
   uint2 sA, bA, sB, bB;
   load_sb(sA, bA);
   load_sb(sB, bB);
+  if (a.signs) {  // the signs never depend on the previous kernel: into L1 before the wait
+    int pb1, pe1, pb2, pe2;
+    blocks_needed(lo, nst, C, K, pb1, pe1, pb2, pe2);
+    const int pnb = (pe1 - pb1) + (pe2 - pb2);
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const int it = warp + q * kTmaConsumers;
+      if (it < a.Mc * pnb) {
+        const int bi = it % pnb;
+        const int b = bi < pe1 - pb1 ? pb1 + bi : pb2 + (bi - (pe1 - pb1));
+        asm volatile("prefetch.global.L1 [%0];" ::"l"(a.signs + b * kBlock + lane * 32));
+      }
+    }
+  }
 
   asm volatile("griddepcontrol.wait;" ::: "memory");
   {
