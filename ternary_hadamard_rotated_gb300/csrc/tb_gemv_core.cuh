@@ -28,7 +28,7 @@ constexpr int kWarpsPerUnit = 4;                        // 32 rows each
 constexpr int kTmaConsumers = kGroupsOfWarps * kWarpsPerUnit;
 constexpr int kTmaThreads = (kTmaConsumers + 1) * 32;
 constexpr int kMaxSlotsPerGroup = 4;
-constexpr int kPreIssue = 1;        // units per group issued before the activations are loaded
+constexpr int kPreIssue = 2;        // units per group issued before the activations are loaded
 constexpr int kCutSlots = 4;        // shared sums of tiles cut by a group or CTA boundary
 constexpr int kScaleStageBytes = 32 * kUnitGroups * 8;  // per warp: 32 rows x 4 groups of fp32 (s, b)
 constexpr uint32_t kMagic1024 = 0x64006400u;

@@ -73,8 +73,13 @@ TB_DEVI int mat_of(const GemvTmaArgs& a, int tile) {
   return i;
 }
 
+// Warp roles: warps 0..11 consume (three unit groups of four), warp 12 produces; warps 13..15
+// only complete the producer's warpgroup so that registers can move between the roles: the
+// launch gives 128 per thread, the producer warpgroup drops to 40 and the consumers rise to 152
+// (12 x 32 x 152 + 4 x 32 x 40 = 63488 of the 65536 the block was launched with).
+constexpr int kWsThreads = 16 * 32;
 template <int MT>
-__global__ void __launch_bounds__(kTmaThreads, 1)
+__global__ void __launch_bounds__(kWsThreads, 1)
     w2_gemv_tma_kernel(const __grid_constant__ CodeMaps maps, const __grid_constant__ GemvTmaArgs a) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -132,7 +137,9 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     ghi = u == 0 ? bnd1 : u == 1 ? bnd2 : hi;
   };
 
-  if (warp == kTmaConsumers) {
+  if (warp >= kTmaConsumers) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 40;" ::: "memory");
+    if (warp != kTmaConsumers) return;
     // ---- producer: the packed weights never depend on the previous kernel ----
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
@@ -178,6 +185,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
   }
 
   // ---- consumers ----
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 152;" ::: "memory");
   const int g = lane >> 2, t = lane & 3;
   const int ug = warp / kWarpsPerUnit, wi = warp % kWarpsPerUnit;
   int glo, ghi;
@@ -605,7 +613,7 @@ static int launch_tma_mt(GemvTmaArgs a, const CodeMaps& maps, int64_t M, int64_t
     a.Mc = (int)((M - m0) < MT ? (M - m0) : MT);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kTmaThreads);
+    cfg.blockDim = dim3(kWsThreads);
     cfg.dynamicSmemBytes = bytes;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
