@@ -503,6 +503,19 @@ def profile_step(args, dist, tb, tdev, torch):
     return {"profile_step": "done", "links": len(links), "status": int(status.item())}
 
 
+def profile_fwht(args, dist, tb, tdev, torch):
+    """Four tb_fwht calls (forward, with signs) on M x K activations, nothing timed."""
+    M, K = args.profile_fwht
+    dev = torch.device("cuda")
+    x = torch.from_numpy(ti.activations(6, M, K)).to(dev)
+    y = torch.empty_like(x)
+    sg = torch.from_numpy(ti.rademacher_signs(6, K)).to(dev)
+    for _ in range(4):
+        tb.tb_fwht(x, y, sg, 1024, False)
+    torch.cuda.synchronize()
+    return {"profile_fwht": [M, K]}
+
+
 def profile_linear(args, dist, tb, tdev, torch):
     """Four calls of one K -> N packed linear on M tokens with algorithm ALGO, nothing timed."""
     K, N, M, algo = args.profile_linear
@@ -630,6 +643,38 @@ def run_batched(args, dist, tb, tdev, torch):
             "rows": rows}
 
 
+def run_fwht(args, dist, tb, tdev, torch):
+    """tb_fwht alone (forward, with signs) on activations larger than L2."""
+    hbm, _, _, peak_kind = peaks()
+    dev = torch.device("cuda")
+    rows = []
+    for M, K in ((4096, 17408), (16384, 5120)):
+        x = torch.from_numpy(ti.activations(6, M, K)).to(dev)
+        y = torch.empty_like(x)
+        sg = torch.from_numpy(ti.rademacher_signs(6, K)).to(dev)
+        flush = torch.empty(256 << 20, dtype=torch.int8, device=dev)
+        for _ in range(3):
+            tb.tb_fwht(x, y, sg, 1024, False)
+        torch.cuda.synchronize()
+        reps = max(3, args.steps)
+        tot = 0.0
+        for _ in range(reps):
+            flush.zero_()  # L2 flush between timed iterations
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            tb.tb_fwht(x, y, sg, 1024, False)
+            b.record()
+            torch.cuda.synchronize()
+            tot += a.elapsed_time(b) / 1e3
+        per = tot / reps
+        byts = 4 * M * K + K  # x read, y written, signs
+        rows.append({"shape": f"M={M} K={K}", "us": round(per * 1e6, 2), "GB/s": round(byts / per / 1e9, 1),
+                     "frac": round(byts / per / 1e9 / hbm, 4)})
+        del x, y, flush
+    return {"metric": "sign * FWHT-1024 (tb_fwht, forward)", "unit": "GB/s", "peak": hbm, "peak_kind": peak_kind,
+            "rows": rows}
+
+
 def run_embed(args, dist, tb, tdev, torch):
     hbm, _, _, peak_kind = peaks()
     dev = torch.device("cuda")
@@ -714,7 +759,7 @@ def main():
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--config", default="sweep", choices=["sweep", "layers", "prefill", "batched", "embed", "all"])
+    ap.add_argument("--config", default="sweep", choices=["sweep", "layers", "prefill", "batched", "embed", "fwht", "all"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-step", action="store_true",
                     help="build the decode stack, run two steps and exit (for an ncu launch list)")
@@ -722,6 +767,8 @@ def main():
                     help="decode step path timed for `value` (the other one is reported in config)")
     ap.add_argument("--per-call", action="store_true",
                     help="with --profile-step: one launch per link instead of the chain launch")
+    ap.add_argument("--profile-fwht", type=int, nargs=2, metavar=("M", "K"),
+                    help="four tb_fwht calls on M x K activations (for ncu)")
     ap.add_argument("--profile-linear", type=int, nargs=4, metavar=("K", "N", "M", "ALGO"),
                     help="one packed K->N matrix, four tb_packed_linear calls on M tokens (for ncu)")
     args = ap.parse_args()
@@ -743,14 +790,17 @@ def main():
     from tb_inputs import device as tdev
 
     tb.load()
-    configs = ["sweep", "layers", "prefill", "batched", "embed"] if args.config == "all" else [args.config]
+    configs = ["sweep", "layers", "prefill", "batched", "embed", "fwht"] if args.config == "all" else [args.config]
     if args.profile_step:
         configs = ["profile"]
     if args.profile_linear:
         configs = ["profile_linear"]
+    if args.profile_fwht:
+        configs = ["profile_fwht"]
     for c in configs:
         fn = {"sweep": run_sweep, "layers": run_layers, "prefill": run_prefill, "batched": run_batched,
-              "embed": run_embed, "profile": profile_step, "profile_linear": profile_linear}[c]
+              "embed": run_embed, "fwht": run_fwht, "profile": profile_step, "profile_linear": profile_linear,
+              "profile_fwht": profile_fwht}[c]
         line = fn(args, dist, tb, tdev, torch)
         if rank == 0:
             print(json.dumps(line), flush=True)
