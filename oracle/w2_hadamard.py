@@ -137,16 +137,25 @@ def decode_w2(words, scales, biases, K: int) -> np.ndarray:
 
     [ARCH] "打包格式的工程": with b = -s the codes {0,1,2} give exactly
     {-s, 0, s}.  The formula is applied as written for any 2-bit code.
+
+    ``biases=None`` is the scale-only reading of the same container: the bias of
+    every group is the pack's -s, so the weight is the ternary value times its
+    scale, W[n, k] = s[n, k//128] * t[n, k] with t = q - 1 (the bias carries no
+    information of its own in that section).
     """
-    q = unpack_w2(words, K).astype(np.float64) + 1.0
+    t = unpack_w2(words, K).astype(np.float64)
     s = np.asarray(scales, dtype=np.float64)
-    b = np.asarray(biases, dtype=np.float64)
     G = K // GROUP
-    if K % GROUP or s.shape != (q.shape[0], G) or b.shape != s.shape:
+    if K % GROUP or s.shape != (t.shape[0], G):
         raise ValueError("scales/biases must be [N, K/128]")
     s_full = np.repeat(s, GROUP, axis=1)
+    if biases is None:
+        return s_full * t
+    b = np.asarray(biases, dtype=np.float64)
+    if b.shape != s.shape:
+        raise ValueError("scales/biases must be [N, K/128]")
     b_full = np.repeat(b, GROUP, axis=1)
-    return s_full * q + b_full
+    return s_full * (t + 1.0) + b_full
 
 
 # ----------------------------------------------------------------------------
@@ -158,7 +167,7 @@ def packed_linear(x, signs, block: int, words, scales, biases) -> np.ndarray:
     [ARCH] "Hadamard 旋转" (``if self.block: x = fwht(x, ...)``, then
     ``quantized_matmul(..., transpose=True, group_size=128, bits=2)``) and
     [PACK] "文本模型加载" (non-embedding path).  x: [M, K]; words [N, K/16];
-    scales, biases [N, K/128]; returns [M, N].
+    scales, biases [N, K/128] (biases None: scale-only, b = -s); returns [M, N].
     """
     x = np.asarray(x, dtype=np.float64)
     K = x.shape[-1]
@@ -193,5 +202,6 @@ def embed_lookup(ids, words, scales, biases, signs, block: int) -> np.ndarray:
     if ids.size and (ids.min() < 0 or ids.max() >= V):
         raise IndexError("token id out of range")
     D = words.shape[1] * CODES_PER_WORD
-    rows = decode_w2(words[ids], np.asarray(scales)[ids], np.asarray(biases)[ids], D)
+    b = None if biases is None else np.asarray(biases)[ids]
+    rows = decode_w2(words[ids], np.asarray(scales)[ids], b, D)
     return fwht(rows, block, signs, inverse=True)

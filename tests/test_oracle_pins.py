@@ -185,6 +185,33 @@ def test_decode_uses_bias_as_stored():
     np.testing.assert_array_equal(oracle.decode_w2(words, s, b, 128)[0], 0.5 * q + 0.25)
 
 
+def test_decode_scale_only_worked_example():
+    # the scale-only reading (no bias read) of the worked group: the page's {-s, 0, s}
+    g = {r[0]: r[1:] for r in read_golden("decode_worked.txt")}
+    s = np.array([[int(g["scale_bits"][0], 16)]], np.uint16).view(np.float16)
+    words = np.full((1, 8), 0x55555555, np.uint32)
+    words[0, 0] = int(g["word"][0], 16)
+    want = np.zeros(128)
+    want[:16] = np.array(g["values_over_s"], float) * float(s[0, 0])
+    np.testing.assert_array_equal(oracle.decode_w2(words, s, None, 128)[0], want)
+
+
+def test_decode_scale_only_equals_the_packed_bias():
+    # for every code the pack writes (and code 3, which it never writes), s*t is exactly
+    # s*q + b with the pack's b = -s
+    N, K = 7, 384
+    t = ti.ternary_codes(4, 0, N, K)
+    s = ti.group_scales(4, 0, N, K // 128)
+    w = oracle.pack_w2(t)
+    W0 = oracle.decode_w2(w, s, None, K)
+    np.testing.assert_array_equal(W0, oracle.decode_w2(w, s, oracle.biases_for(s), K))
+    np.testing.assert_array_equal(W0, t.astype(np.float64) * np.repeat(s.astype(np.float64), 128, axis=1))
+    w3 = np.full((1, 8), 0xFFFFFFFF, np.uint32)
+    s3 = np.array([[0.5]], np.float16)
+    np.testing.assert_array_equal(oracle.decode_w2(w3, s3, None, 128), np.ones((1, 128)))
+    np.testing.assert_array_equal(oracle.decode_w2(w3, s3, oracle.biases_for(s3), 128), np.ones((1, 128)))
+
+
 # ----------------------------------------------------------------------------
 # Packed.__call__: non-embedding and embedding paths
 # ----------------------------------------------------------------------------
@@ -205,8 +232,10 @@ def test_packed_linear_brute_force():
     b = oracle.biases_for(s)
     H = sylvester(block)
     y = np.zeros((M, N))
+    xr_all = []
     for m in range(M):
         xr = []
+        xr_all.append(xr)
         for blk in range(K // block):
             seg = [float(x[m, blk * block + i]) * int(signs[blk * block + i]) for i in range(block)]
             for i in range(block):
@@ -219,6 +248,12 @@ def test_packed_linear_brute_force():
             y[m, n] = acc
     got = oracle.packed_linear(x, signs, block, w, s, b)
     np.testing.assert_allclose(got, y, rtol=1e-12, atol=1e-12)
+    # scale-only (no biases read): the same sums with the ternary codes times their scale
+    y0 = np.zeros((M, N))
+    for m in range(M):
+        for n in range(N):
+            y0[m, n] = sum(xr_all[m][k] * float(s[n, k // 128]) * int(t[n, k]) for k in range(K))
+    np.testing.assert_allclose(oracle.packed_linear(x, signs, block, w, s, None), y0, rtol=1e-12, atol=1e-12)
 
 
 def test_group_sum_identity():
