@@ -229,6 +229,11 @@ class Stack:
     def algo_bytes(self):
         return sum(p.algo_bytes for _, p, _ in self.layers)
 
+    @property
+    def scale_only_bytes(self):
+        """Bytes of the step's matrices without the biases (1/64 byte per weight less)."""
+        return sum(p.algo_bytes - p.N * p.G * 2 for _, p, _ in self.layers)
+
 
 SHARED_INPUT = ({"in_proj_qkv", "in_proj_z"}, {"q_proj", "k_proj", "v_proj"}, {"gate_proj", "up_proj"})
 
@@ -243,8 +248,9 @@ def run_calls(tb, link_args, ws, status):
             tb.tb_packed_linear_multi(x, sg, block, mats, ys, ws, status)
 
 
-def embed(tb, st, ids, e_out, status):
-    tb.tb_embed_lookup(ids, st.emb.w, st.emb.s, st.emb.b, st.signs[ti.HIDDEN], 1024, e_out, status)
+def embed(tb, st, ids, e_out, status, biases=True):
+    tb.tb_embed_lookup(ids, st.emb.w, st.emb.s, st.emb.b if biases else None, st.signs[ti.HIDDEN],
+                       1024, e_out, status)
 
 
 def time_graph(torch, graph, steps, dist):
@@ -332,6 +338,10 @@ def run_sweep(args, dist, tb, tdev, torch):
     step_bytes = st.algo_bytes
     ws = torch.zeros(tb.tb_packed_linear_workspace_size(1, ti.MLP, ti.HIDDEN), dtype=torch.uint8, device=dev)
     call_graph = capture(torch, lambda: (embed(tb, st, ids, e_out, status), run_calls(tb, links, ws, status)))
+    # scale-only form: no biases passed, each taken as -scale by the kernels (same results)
+    links0 = [(x, sg, blk, [(w, s, None) for w, s, _ in mats], ys) for x, sg, blk, mats, ys in links]
+    scale_graph = capture(torch, lambda: (embed(tb, st, ids, e_out, status, biases=False),
+                                          run_calls(tb, links0, ws, status)))
     gemv_graph = capture(torch, lambda: run_calls(tb, links, ws, status))
 
     def chain_step():
@@ -386,6 +396,9 @@ def run_sweep(args, dist, tb, tdev, torch):
     for _ in range(3):
         other()
     osecs = dist.max(time_steps(other, args.steps))
+    for _ in range(3):
+        scale_graph.replay()
+    ssecs = dist.max(time_steps(scale_graph.replay, args.steps))
     torch.cuda.synchronize()
     assert int(status.item()) == 0, f"device status {int(status.item())}"
     assert bool(torch.isfinite(st.logits).all()), "non-finite logits"
@@ -446,6 +459,12 @@ def run_sweep(args, dist, tb, tdev, torch):
             "links_per_step": n_links,
             "shared_input_links": "in_proj_qkv+in_proj_z, q+k+v and gate+up each one link",
             ("tok_s_calls_path" if args.path == "chain" else "tok_s_chain_path"): round(n * args.steps / osecs, 3),
+            "scale_only": {
+                "tok_s": round(n * args.steps / ssecs, 3),
+                "weights_gb_per_step": round((st.scale_only_bytes + ti.HIDDEN // 4 + ti.HIDDEN // 64) / 1e9, 4),
+                "note": "calls path with biases = NULL (each bias is the pack's -scale, not read); "
+                        "outputs bit-identical to the stored-bias step",
+            },
             "parallelism": f"replicas x{n}",
         },
         "roofline": {
@@ -551,19 +570,23 @@ def run_layers(args, dist, tb, tdev, torch):
         y = torch.empty((1, N), dtype=torch.float16, device=dev)
         ws = torch.zeros(tb.tb_packed_linear_workspace_size(1, K, N), dtype=torch.uint8, device=dev)
 
-        def fn():
+        def fn(biases=True):
             for p in ps:
-                tb.tb_packed_linear(x, sg, 1024, p.w, p.s, p.b, y, ws, status)
+                tb.tb_packed_linear(x, sg, 1024, p.w, p.s, p.b if biases else None, y, ws, status)
 
-        g = capture(torch, fn)
-        for _ in range(3):
-            g.replay()
         reps = max(3, args.steps)
-        secs = time_graph(torch, g, reps, dist)
-        per = secs / (reps * copies)
-        gbs = ti.packed_bytes(K, N) / per / 1e9
-        rows.append({"shape": f"{name} {K}->{N}", "us": round(per * 1e6, 2), "GB/s": round(gbs, 1),
-                     "frac": round(gbs / hbm, 4), "copies": copies})
+        per = {}
+        for biases in (True, False):
+            g = capture(torch, lambda: fn(biases))
+            for _ in range(3):
+                g.replay()
+            per[biases] = time_graph(torch, g, reps, dist) / (reps * copies)
+        gbs = ti.packed_bytes(K, N) / per[True] / 1e9
+        gbs0 = (ti.packed_bytes(K, N) - N * (K // 128) * 2) / per[False] / 1e9
+        rows.append({"shape": f"{name} {K}->{N}", "us": round(per[True] * 1e6, 2), "GB/s": round(gbs, 1),
+                     "frac": round(gbs / hbm, 4), "copies": copies,
+                     "scale_only_us": round(per[False] * 1e6, 2),
+                     "scale_only_frac": round(gbs0 / hbm, 4)})
         del ps
     del tmp
     return {"metric": "decode GEMV per layer shape (M=1)", "unit": "GB/s", "peak": hbm,

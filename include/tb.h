@@ -29,6 +29,12 @@
  *    significant first); word j of a row holds the row's codes 16j..16j+15.
  *  - Group size 128 and 2 bits per code are fixed.  Per group: one fp16 scale s
  *    and one fp16 bias b (= -s in the pack); a code decodes to s*q + b.
+ *  - Scale-only form: every call that takes `biases` also accepts NULL there.
+ *    Each bias is then taken as the pack's -s (the fp16 sign bit of s flipped)
+ *    and never read, so a code decodes to s*(q - 1) = s*t and the call reads
+ *    1/64 byte less per weight.  For a pack written by tb_pack_w2 the result is
+ *    bit-identical to passing its stored biases.  ([ARCH] "打包格式的工程": the
+ *    stored bias is always -scale, so it adds bytes but no information.)
  *  - Hadamard block: 1024 (the pack's block_size) or 0 (= module not folded,
  *    no transform).  The transform is the normalised Sylvester-Walsh-Hadamard
  *    matrix in natural order, H[i][j] = (-1)^popcount(i&j), scaled by
@@ -135,7 +141,8 @@ size_t tb_packed_linear_algo_workspace_size(int64_t M, int64_t K, int64_t N, int
  *   y[m, n] = sum_k x'[m, k] * (s[n, k/128] * q[n, k] + b[n, k/128]),
  *   x' = fwht(x, block, signs) rounded to fp16 (x' = x when block = 0);
  *   x fp16 [M, K]; signs int8 [K] (+-1) or NULL (all +1; ignored when block = 0);
- *   w uint32 [N, K/16]; scales, biases fp16 [N, K/128]; y fp16 [M, N] (out).
+ *   w uint32 [N, K/16]; scales fp16 [N, K/128]; biases fp16 [N, K/128] or NULL
+ *   (scale-only, b = -s); y fp16 [M, N] (out).
  * fp32 accumulation, fp16 output (round to nearest even).
  * K: positive multiple of 1024 when block = 1024, of 128 when block = 0.  M, N >= 1.
  * workspace: device memory of at least tb_packed_linear_workspace_size(...) bytes,
@@ -161,7 +168,8 @@ int tb_packed_linear_algo(const uint16_t* x, int64_t M, int64_t K, const int8_t*
  * ([ARCH] "Hadamard 旋转": the folded transform depends only on the input width, so the
  * modules that share x also share x' = fwht(x)).  x' is computed once per launch; matrix i
  * writes y[i] (fp16 [M, N[i]]).  w, scales, biases, N, y are HOST arrays of n entries holding
- * device pointers / row counts; K must be a positive multiple of 1024.  Workspace as for
+ * device pointers / row counts; biases (the array, or any entry) may be NULL (scale-only for
+ * those matrices); K must be a positive multiple of 1024.  Workspace as for
  * tb_packed_linear, sized with tb_packed_linear_workspace_size(M, K, max N, block).
  * M <= 8: one decode GEMV launch for all matrices.  M > 8: one rotation, then one tensor-core
  * GEMM per matrix.
@@ -193,7 +201,7 @@ typedef struct tb_chain_link {
   int32_t n;                  /* matrices reading x: 1..4 */
   const uint32_t* w[4];       /* uint32 [N[i], K/16] packed codes */
   const uint16_t* scales[4];  /* fp16 [N[i], K/128] */
-  const uint16_t* biases[4];  /* fp16 [N[i], K/128] */
+  const uint16_t* biases[4];  /* fp16 [N[i], K/128], or NULL (scale-only, b = -s) */
   int64_t N[4];               /* rows of matrix i, >= 1 */
   uint16_t* y[4];             /* fp16 [M, N[i]] (out) */
 } tb_chain_link;
@@ -238,7 +246,8 @@ int tb_chain_run(const void* plan, int n_links, int64_t M, int64_t max_K, void* 
  * [ARCH] "Hadamard 旋转" (return fwht(out, block, signs, inverse=True)) and
  * [PACK] "文本模型加载" (mx.dequantize of the looked-up rows, then the inverse transform).
  *   out[t, :] = signs * ((H/32) e) per block,  e = s*q + b of row ids[t] of the table.
- *   ids int32 [T]; w uint32 [V, D/16]; scales, biases fp16 [V, D/128];
+ *   ids int32 [T]; w uint32 [V, D/16]; scales fp16 [V, D/128]; biases the same or NULL
+ *   (scale-only, b = -s);
  *   signs int8 [D] (+-1) or NULL (all +1); out fp16 [T, D] (out).
  * An id outside [0, V) writes a row of zeros and sets TB_DEV_BAD_ID in dev_status.
  * block 1024 (D a multiple of 1024) or 0 (D a multiple of 128); T >= 0 (T = 0 is a no-op).

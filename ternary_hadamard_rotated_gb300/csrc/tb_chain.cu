@@ -300,11 +300,13 @@ __global__ void __launch_bounds__(kTmaThreads, 1) w2_gemv_chain_kernel(const __g
           const int row = (ptile - t0m) * kUnitRows + 32 * wi + lane;
           const bool in = row < lk->N[mi];
           psrow = in ? lk->scales[mi] + (int64_t)row * G : nullptr;
-          pbrow = in ? lk->biases[mi] + (int64_t)row * G : nullptr;
+          pbrow = in && lk->biases[mi] ? lk->biases[mi] + (int64_t)row * G : nullptr;
         }
         if (psrow) {
           sv = __ldg(reinterpret_cast<const uint2*>(psrow + pchunk * kUnitGroups));
-          bv = __ldg(reinterpret_cast<const uint2*>(pbrow + pchunk * kUnitGroups));
+          // no biases given: each is the pack's -scale (the fp16 sign bit flipped), not read
+          bv = pbrow ? __ldg(reinterpret_cast<const uint2*>(pbrow + pchunk * kUnitGroups))
+                     : make_uint2(sv.x ^ 0x80008000u, sv.y ^ 0x80008000u);
         }
       }
       ++pn;
@@ -594,9 +596,10 @@ extern "C" int tb_chain_plan(const tb_chain_link* links, int n_links, int64_t M,
     if (!aligned16(l.x) || (l.signs && !aligned16(l.signs))) return TB_ERR_ALIGN;
     int64_t tiles = 0;
     for (int j = 0; j < l.n; ++j) {
-      if (!l.w[j] || !l.scales[j] || !l.biases[j] || !l.y[j]) return TB_ERR_NULL;
+      if (!l.w[j] || !l.scales[j] || !l.y[j]) return TB_ERR_NULL;  // biases may be NULL
       if (l.N[j] < 1 || l.N[j] > (1LL << 30)) return TB_ERR_SHAPE;
-      if (!aligned16(l.w[j]) || !aligned16(l.scales[j]) || !aligned16(l.biases[j]) || !aligned16(l.y[j]))
+      if (!aligned16(l.w[j]) || !aligned16(l.scales[j]) || !aligned16(l.y[j]) ||
+          (l.biases[j] && !aligned16(l.biases[j])))
         return TB_ERR_ALIGN;
       tiles += (l.N[j] + kUnitRows - 1) / kUnitRows;
     }

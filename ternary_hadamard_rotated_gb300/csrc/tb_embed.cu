@@ -40,7 +40,8 @@ __global__ void __launch_bounds__(kEmbWarps * 32) embed_kernel(
     if (ok && in) {
       const uint2 wd = *reinterpret_cast<const uint2*>(w + id * (D / kCodesPerWord) + k0 / kCodesPerWord);
       const int64_t grp = id * G + k0 / kGroup;
-      const float s = __half2float(scales[grp]), bb = __half2float(biases[grp]);
+      // no biases given: each is the pack's -scale
+      const float s = __half2float(scales[grp]), bb = biases ? __half2float(biases[grp]) : -s;
 #pragma unroll
       for (int r = 0; r < 32; ++r) {
         const uint32_t word = r < 16 ? wd.x : wd.y;
@@ -82,8 +83,8 @@ extern "C" int tb_embed_lookup(const int32_t* ids, int64_t T, const uint32_t* w,
   if (block != 0 && block != kBlock) return TB_ERR_UNSUPPORTED;
   if (block == kBlock && D % kBlock) return TB_ERR_SHAPE;
   if (T == 0) return TB_OK;
-  if (!ids || !w || !scales || !biases || !out) return TB_ERR_NULL;
-  if (!aligned16(w) || !aligned16(scales) || !aligned16(biases) || !aligned16(out) ||
+  if (!ids || !w || !scales || !out) return TB_ERR_NULL;  // biases may be NULL
+  if (!aligned16(w) || !aligned16(scales) || (biases && !aligned16(biases)) || !aligned16(out) ||
       (signs && !aligned16(signs)))
     return TB_ERR_ALIGN;
   DeviceFacts f;

@@ -263,21 +263,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int row = n0 + d;
       const bool valid = row < a.N;
       const __half* srow = a.scales + (int64_t)(valid ? row : 0) * a.G;
-      const __half* brow = a.biases + (int64_t)(valid ? row : 0) * a.G;
+      // no biases given: each is the pack's -scale (the fp16 sign bit flipped), not read
+      const bool has_b = a.biases != nullptr;
+      const __half* brow = has_b ? a.biases + (int64_t)(valid ? row : 0) * a.G : nullptr;
       // scales and biases of eight groups (16 k-blocks) per load, the next eight loaded while
       // these are used: the loads go to HBM when the weights are read once
       const bool vec8 = (a.G % 8) == 0;
       auto load_sb8 = [&](int gb, uint4& sv, uint4& bv) {
         if (valid && vec8 && 8 * gb < a.G) {
           sv = __ldg(reinterpret_cast<const uint4*>(srow) + gb);
-          bv = __ldg(reinterpret_cast<const uint4*>(brow) + gb);
+          bv = has_b ? __ldg(reinterpret_cast<const uint4*>(brow) + gb)
+                     : make_uint4(sv.x ^ 0x80008000u, sv.y ^ 0x80008000u, sv.z ^ 0x80008000u,
+                                  sv.w ^ 0x80008000u);
         } else {
           uint16_t hs[8], hb[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             const bool in = valid && 8 * gb + e < a.G;
             hs[e] = in ? __half_as_ushort(srow[8 * gb + e]) : 0;
-            hb[e] = in ? __half_as_ushort(brow[8 * gb + e]) : 0;
+            hb[e] = !in ? 0 : has_b ? __half_as_ushort(brow[8 * gb + e]) : (uint16_t)(hs[e] ^ 0x8000u);
           }
           sv = make_uint4(hs[0] | (uint32_t)hs[1] << 16, hs[2] | (uint32_t)hs[3] << 16,
                           hs[4] | (uint32_t)hs[5] << 16, hs[6] | (uint32_t)hs[7] << 16);

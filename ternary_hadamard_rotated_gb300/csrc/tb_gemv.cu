@@ -158,8 +158,10 @@ TB_DEVI void gemv_groups(const uint8_t* rowg, int gi0, int grp0, const uint4* im
 #pragma unroll
   for (int n = 0; n < NG; ++n) {
     const int grp = grp0 + n;
-    const float sA = __half2float(ss[g * G + grp]), bA = __half2float(sb[g * G + grp]);
-    const float sB = __half2float(ss[(g + 8) * G + grp]), bB = __half2float(sb[(g + 8) * G + grp]);
+    // sb == nullptr: no biases given, each is the pack's -scale
+    const float sA = __half2float(ss[g * G + grp]), bA = sb ? __half2float(sb[g * G + grp]) : -sA;
+    const float sB = __half2float(ss[(g + 8) * G + grp]),
+                bB = sb ? __half2float(sb[(g + 8) * G + grp]) : -sB;
     const float2 c0 = cs[grp * MT + t0], c1 = cs[grp * MT + t1];
     acc[0] += sA * (d[n][0] - c0.x) + bA * c0.y;
     acc[1] += sA * (d[n][1] - c1.x) + bA * c1.y;
@@ -229,14 +231,14 @@ __global__ void __launch_bounds__(kGemvThreads, 1) w2_gemv_kernel(const GemvArgs
     const uint32_t bytes = (uint32_t)(rows * G * 2);
     if ((bytes & 15u) == 0) {
       if (lane == 0) {
-        mbar_arrive_expect_tx(sfull + slot, 2 * bytes);
+        mbar_arrive_expect_tx(sfull + slot, a.biases ? 2 * bytes : bytes);
         bulk_g2s_hint(ds, a.scales + (int64_t)r0 * G, bytes, sfull + slot, pol);
-        bulk_g2s_hint(db, a.biases + (int64_t)r0 * G, bytes, sfull + slot, pol);
+        if (a.biases) bulk_g2s_hint(db, a.biases + (int64_t)r0 * G, bytes, sfull + slot, pol);
       }
     } else {  // ragged last tile: plain copies
       for (int e = lane; e < rows * G; e += 32) {
         ds[e] = a.scales[(int64_t)r0 * G + e];
-        db[e] = a.biases[(int64_t)r0 * G + e];
+        if (a.biases) db[e] = a.biases[(int64_t)r0 * G + e];
       }
       __threadfence_block();
       __syncwarp();
@@ -338,7 +340,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) w2_gemv_kernel(const GemvArgs
         set_status(a.status, TB_DEV_TIMEOUT);
       }
       const __half* ss = scl + sslot * 2 * kTileRows * G;
-      const __half* sb = ss + kTileRows * G;
+      const __half* sb = a.biases ? ss + kTileRows * G : nullptr;
       for (int c = 0; c < spt; ++c, ++i) {
         const int slot = i % D;
         if (!aborted && !mbar_wait(full + warp * D + slot, (i / D) & 1)) {

@@ -213,11 +213,13 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         const int row = (ptile - a.tile0[mi]) * kUnitRows + 32 * wi + lane;
         const bool in = row < a.N[mi];
         psrow = in ? a.scales[mi] + (int64_t)row * G : nullptr;
-        pbrow = in ? a.biases[mi] + (int64_t)row * G : nullptr;
+        pbrow = in && a.biases[mi] ? a.biases[mi] + (int64_t)row * G : nullptr;
       }
       if (psrow) {
         sv = __ldg(reinterpret_cast<const uint2*>(psrow + pchunk * kUnitGroups));
-        bv = __ldg(reinterpret_cast<const uint2*>(pbrow + pchunk * kUnitGroups));
+        // no biases given: each is the pack's -scale (the fp16 sign bit flipped), not read
+        bv = pbrow ? __ldg(reinterpret_cast<const uint2*>(pbrow + pchunk * kUnitGroups))
+                   : make_uint2(sv.x ^ 0x80008000u, sv.y ^ 0x80008000u);
       }
     }
     ++pn;

@@ -73,11 +73,12 @@ extern "C" int tb_packed_linear_algo(const uint16_t* x, int64_t M, int64_t K, co
                                      void* workspace, size_t workspace_bytes, int32_t* dev_status,
                                      int algo, void* stream) {
   using namespace tb;
-  if (!x || !w || !scales || !biases || !y) return TB_ERR_NULL;
+  if (!x || !w || !scales || !y) return TB_ERR_NULL;  // biases may be NULL: each is -scale
   int rc = check_linear_shape(M, K, block, N);
   if (rc != TB_OK) return rc;
   if (algo != TB_ALGO_AUTO && algo != TB_ALGO_GEMV && algo != TB_ALGO_TC) return TB_ERR_UNSUPPORTED;
-  if (!aligned16(x) || !aligned16(w) || !aligned16(scales) || !aligned16(biases) || !aligned16(y) ||
+  if (!aligned16(x) || !aligned16(w) || !aligned16(scales) || (biases && !aligned16(biases)) ||
+      !aligned16(y) ||
       (signs && !aligned16(signs)) || (workspace && !aligned16(workspace)))
     return TB_ERR_ALIGN;
   const int use = resolve_algo(M, algo);
@@ -113,7 +114,7 @@ extern "C" int tb_packed_linear_multi(const uint16_t* x, int64_t M, int64_t K, c
                                       const int64_t* N, uint16_t* const* y, void* workspace,
                                       size_t workspace_bytes, int32_t* dev_status, void* stream) {
   using namespace tb;
-  if (!x || !w || !scales || !biases || !N || !y) return TB_ERR_NULL;
+  if (!x || !w || !scales || !N || !y) return TB_ERR_NULL;  // biases (or an entry) may be NULL
   if (n < 1 || n > kMaxMulti) return TB_ERR_SHAPE;
   if (block != 0 && block != kBlock) return TB_ERR_UNSUPPORTED;
   if (M < 1 || K < kBlock || K % kBlock) return TB_ERR_SHAPE;
@@ -123,12 +124,13 @@ extern "C" int tb_packed_linear_multi(const uint16_t* x, int64_t M, int64_t K, c
   const __half* bh[kMaxMulti];
   __half* yh[kMaxMulti];
   for (int i = 0; i < n; ++i) {
-    if (!w[i] || !scales[i] || !biases[i] || !y[i]) return TB_ERR_NULL;
+    const uint16_t* bi = biases ? biases[i] : nullptr;
+    if (!w[i] || !scales[i] || !y[i]) return TB_ERR_NULL;
     if (N[i] < 1) return TB_ERR_SHAPE;
-    if (!aligned16(w[i]) || !aligned16(scales[i]) || !aligned16(biases[i]) || !aligned16(y[i]))
+    if (!aligned16(w[i]) || !aligned16(scales[i]) || !aligned16(y[i]) || (bi && !aligned16(bi)))
       return TB_ERR_ALIGN;
     sh[i] = reinterpret_cast<const __half*>(scales[i]);
-    bh[i] = reinterpret_cast<const __half*>(biases[i]);
+    bh[i] = reinterpret_cast<const __half*>(bi);
     yh[i] = reinterpret_cast<__half*>(y[i]);
   }
   const int8_t* sg = block ? signs : nullptr;

@@ -68,12 +68,12 @@ extern "C" int tb_packed_linear_gemv_noalloc(const uint16_t* x, int64_t M, int64
                                              int64_t N, uint16_t* y, int32_t* dev_status,
                                              void* stream) {
   using namespace tb;
-  if (!x || !w || !scales || !biases || !y) return TB_ERR_NULL;
+  if (!x || !w || !scales || !y) return TB_ERR_NULL;  // biases may be NULL: each is -scale
   if (block != 0 && block != kBlock) return TB_ERR_UNSUPPORTED;
   if (M < 1 || N < 1 || K < kBlock || K % kBlock) return TB_ERR_SHAPE;
   if (M > kNoallocMaxTokens) return TB_ERR_TOO_LARGE;
-  if (!aligned16(x) || !aligned16(w) || !aligned16(scales) || !aligned16(biases) || !aligned16(y) ||
-      (signs && !aligned16(signs)))
+  if (!aligned16(x) || !aligned16(w) || !aligned16(scales) || (biases && !aligned16(biases)) ||
+      !aligned16(y) || (signs && !aligned16(signs)))
     return TB_ERR_ALIGN;
   DeviceFacts f;
   int rc = device_facts(&f);

@@ -67,12 +67,13 @@ def device_layer(seed: int, N: int, K: int, from_host: HostLayer | None = None, 
     return w, scales, biases
 
 
-def linear_reference(x16, signs, block, layer: HostLayer):
-    """(y_ref, bound) in float64 for the rows held by the host layer."""
+def linear_reference(x16, signs, block, layer: HostLayer, scale_only=False):
+    """(y_ref, bound) in float64 for the rows held by the host layer (scale_only: the
+    oracle's reading without biases, W = s * t)."""
     x = x16.astype(np.float64)
-    y = oracle.packed_linear(x, signs, block, layer.words, layer.scales, layer.biases)
-    bound = LIN_REL * oracle.abs_product_sum(x, signs, block, layer.words, layer.scales,
-                                             layer.biases) + LIN_ABS
+    b = None if scale_only else layer.biases
+    y = oracle.packed_linear(x, signs, block, layer.words, layer.scales, b)
+    bound = LIN_REL * oracle.abs_product_sum(x, signs, block, layer.words, layer.scales, b) + LIN_ABS
     return y, bound
 
 

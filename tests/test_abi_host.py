@@ -74,6 +74,10 @@ def test_packed_linear_refuses_bad_arguments(lib):
     assert call(M=0) == -2
     assert call(N=0) == -2
     assert call(x=P + 2) == -6            # misaligned
+    # biases may be NULL (scale-only: each bias is -scale); the other checks still apply
+    assert call(b=None, K=1000) == -2
+    assert call(b=None, x=None) == -1
+    assert call(b=P + 2) == -6            # given biases must be aligned
     # algorithm choice
     g = lib.tb_packed_linear_algo
     assert g(P, 1, 1024, P, 1024, P, P, P, 16, P, None, 0, None, 7, None) == -3
@@ -118,6 +122,8 @@ def test_other_entry_points_refuse_bad_arguments(lib):
     assert e(P, 4, P, P, P, 0, 1024, None, 1024, P, None, None) == -2
     assert e(P, 0, P, P, P, 100, 1024, None, 1024, P, None, None) == 0   # T = 0: no-op
     assert e(None, 4, P, P, P, 100, 1024, None, 1024, P, None, None) == -1
+    assert e(P, 4, P, P, None, 100, 1000, None, 1024, P, None, None) == -2   # biases NULL: allowed
+    assert e(P, 4, P, P, P + 2, 100, 1024, None, 1024, P, None, None) == -6
 
 
 def test_multi_refuses_bad_arguments(lib):
@@ -178,6 +184,11 @@ def test_chain_refuses_bad_arguments(lib):
     assert plan(link(x=None)) == tb.TB_ERR_NULL
     assert plan(link(x=P + 8)) == tb.TB_ERR_ALIGN
     assert plan(link(), nbytes=64) == tb.TB_ERR_WORKSPACE
+    lk = link()
+    lk.biases[0] = P + 8
+    assert plan(lk) == tb.TB_ERR_ALIGN
+    lk.biases[0] = None                                              # scale-only: allowed
+    assert plan(lk, nbytes=64) == tb.TB_ERR_WORKSPACE
     r = lib.tb_chain_run
     assert r(None, 1, 1, 1024, P, 1 << 22, None, None) == tb.TB_ERR_NULL
     assert r(0x10000, 0, 1, 1024, P, 1 << 22, None, None) == tb.TB_ERR_SHAPE

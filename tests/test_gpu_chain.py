@@ -61,14 +61,14 @@ class SmallChain:
             self.args.append((self.bufs[src], dev(self.signs[K]), 1024, ms, ys))
         self.spec = spec
 
-    def check(self, what=""):
+    def check(self, what="", scale_only=False):
         got = {k: v.cpu().numpy() for k, v in self.bufs.items()}
         for src, mats in self.spec:
             x = got[src]
             assert np.isfinite(x).all(), f"{what}: NaN in input {src}"
             K = mats[0][1]
             for name, _, _ in mats:
-                ref, bound = linear_reference(x, self.signs[K], 1024, self.host[name])
+                ref, bound = linear_reference(x, self.signs[K], 1024, self.host[name], scale_only)
                 assert_linear_close(got[name], ref, bound, f"{what} {name}")
         return got
 

@@ -57,6 +57,30 @@ def test_noalloc_gemv_matches_regular_entry(tb, M, K, N):
         assert (err <= bound).all(), float(err.max())
 
 
+def test_noalloc_gemv_scale_only(tb):
+    # biases = NULL: each bias is the pack's -scale, and the result is the stored-bias one
+    M, K, N = 2, 5120, 1000
+    x = ti.activations(95, M, K)
+    sg = ti.rademacher_signs(95, K)
+    L = HostLayer(95, N, K)
+    w, s, b = device_layer(95, N, K, from_host=L)
+    xd = torch.from_numpy(x).cuda()
+    sd = torch.from_numpy(sg).cuda()
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    outs = []
+    for bb in (b, None):
+        y = torch.full((M, N), float("nan"), dtype=torch.float16, device="cuda")
+        tb.tb_packed_linear_gemv_noalloc(xd, sd, 1024, w, s, bb, y, st)
+        outs.append(y.cpu().numpy())
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    np.testing.assert_array_equal(outs[1].view(np.uint16), outs[0].view(np.uint16))
+    ref = oracle.packed_linear(x.astype(np.float64), sg, 1024, L.words, L.scales, None)
+    bound = LIN_REL * oracle.abs_product_sum(x.astype(np.float64), sg, 1024, L.words, L.scales,
+                                             None) + LIN_ABS
+    assert (np.abs(outs[1].astype(np.float64) - ref) <= bound).all()
+
+
 def test_noalloc_gemv_refuses_too_many_tokens(tb):
     K, N, M = 1024, 16, 9
     x = torch.zeros((M, K), dtype=torch.float16, device="cuda")
