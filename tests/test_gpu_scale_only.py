@@ -3,8 +3,11 @@
 The pack's bias is always -scale (the affine container of the Bonsai article), so a
 caller may pass no biases; the kernels then take each bias as the scale with its fp16
 sign bit flipped and read 1/64 byte less per weight.  Two checks per path:
-  * bit-identical to the same call with the pack's stored biases (same arithmetic on the
-    same values, and every schedule here sums its parts in a fixed order);
+  * the same result as the call with the pack's stored biases: the same arithmetic on the
+    same values, so bit-identical where the path sums in a fixed order (tensor-core GEMM,
+    the K % 1024 GEMV, the embedding) and within two fp16 units in the last place where
+    the decode GEMV's shared-memory sums of a row tile cut between three warp groups may
+    meet in another order;
   * within the linear (or transform) tolerance of the oracle's scale-only reading,
     W = s * t, computed without biases.
 """
@@ -33,6 +36,14 @@ def tb():
 
 def dev(a):
     return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def assert_same(y0, yb, exact):
+    if exact:
+        np.testing.assert_array_equal(y0.view(np.uint16), yb.view(np.uint16))
+    else:
+        ulp = np.spacing(np.abs(yb).astype(np.float16)).astype(np.float64)
+        assert (np.abs(y0.astype(np.float64) - yb.astype(np.float64)) <= 2 * ulp).all()
 
 
 def linear(tb, xd, sd, block, w, s, b, M, N, algo):
@@ -70,7 +81,7 @@ def test_linear_scale_only(tb, M, K, N, algo, block):
     xd, sd = dev(x), (dev(sg) if sg is not None else None)
     y_b = linear(tb, xd, sd, block, w, s, b, M, N, algo)
     y_0 = linear(tb, xd, sd, block, w, s, None, M, N, algo)
-    np.testing.assert_array_equal(y_0.view(np.uint16), y_b.view(np.uint16))
+    assert_same(y_0, y_b, exact=not (algo == 1 and K % 1024 == 0))
     ref, bound = linear_reference(x, sg, block, L, scale_only=True)
     assert_linear_close(y_0, ref, bound, f"scale-only {M}x{K}x{N} algo={algo}")
 
@@ -94,7 +105,7 @@ def test_multi_scale_only_mixed(tb, M):
     torch.cuda.synchronize()
     assert int(st.item()) == 0
     for i, L in enumerate(layers):
-        np.testing.assert_array_equal(outs[1][i].view(np.uint16), outs[0][i].view(np.uint16))
+        assert_same(outs[1][i], outs[0][i], exact=M > 8)
         ref, bound = linear_reference(x, sg, 1024, L, scale_only=True)
         assert_linear_close(outs[1][i], ref, bound, f"multi scale-only M={M} N={L.N}")
 
@@ -124,21 +135,16 @@ def test_embedding_scale_only(tb, block):
 
 
 def test_chain_scale_only(tb):
+    # every link's output against the oracle's scale-only reading of that link's input (the
+    # links feed one another, so last-place differences of cut-tile sums propagate: no
+    # comparison with the stored-bias run beyond that)
     from test_gpu_chain import SPEC, SmallChain
 
     M = 2
     c = SmallChain(tb, SPEC, M, seed=540)
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
-    tb.Chain(c.args, M).run(st)
-    torch.cuda.synchronize()
-    stored = {k: v.cpu().numpy() for k, v in c.bufs.items()}
-    for k, v in c.bufs.items():
-        if k != "x0":
-            v.fill_(float("nan"))
     args0 = [(x, sg, blk, [(w, s, None) for w, s, _ in ms], ys) for x, sg, blk, ms, ys in c.args]
     tb.Chain(args0, M).run(st)
     torch.cuda.synchronize()
     assert int(st.item()) == 0
-    got = c.check("chain scale-only", scale_only=True)
-    for k in stored:
-        np.testing.assert_array_equal(got[k].view(np.uint16), stored[k].view(np.uint16))
+    c.check("chain scale-only", scale_only=True)
