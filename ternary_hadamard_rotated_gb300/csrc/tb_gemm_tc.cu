@@ -421,30 +421,45 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         asm volatile("bar.sync 2, 256;" ::: "memory");
         if (last_flag) {
+          const int me = (int)blockIdx.x;
+          auto load_part = [&](int cc, int c, float4 (&o)[8]) {
+            const int slot = sk_lo(cc, units, grid) / nkb == t ? 0 : 1;
+            const float4* op = reinterpret_cast<const float4*>(
+                a.part + ((int64_t)cc * 2 + slot) * kPartFloats + (int64_t)lrow * BN + c0 + c);
+#pragma unroll
+            for (int v = 0; v < 8; ++v) o[v] = __ldcg(op + v);
+          };
+          auto add_part = [](float (&f)[32], const float4 (&o)[8]) {
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+              f[4 * v] += o[v].x;
+              f[4 * v + 1] += o[v].y;
+              f[4 * v + 2] += o[v].z;
+              f[4 * v + 3] += o[v].w;
+            }
+          };
 #pragma unroll 1
           for (int c = 0; c < CW; c += 32) {
             float f[32];
 #pragma unroll
             for (int e = 0; e < 32; ++e) f[e] = 0.f;
-            for (int cc = first; cc <= lastc; ++cc) {
-              if (cc == (int)blockIdx.x) {
-                float m[32];
-                tmem_cols(c, m);
+            // the parts in CTA order, its own from tensor memory; the other contributors' parts
+            // two at a time, both loads in flight together
+            for (int cc = first; cc <= lastc;) {
+              const int o0 = cc == me ? cc + 1 : cc;
+              const int o1 = o0 + 1 == me ? o0 + 2 : o0 + 1;
+              float4 A[8], B[8];
+              if (o0 <= lastc) load_part(o0, c, A);
+              if (o1 <= lastc) load_part(o1, c, B);
+              const int end = o1 < lastc ? o1 : lastc;
+              for (; cc <= end; ++cc) {
+                if (cc == me) {
+                  float m[32];
+                  tmem_cols(c, m);
 #pragma unroll
-                for (int e = 0; e < 32; ++e) f[e] += m[e];
-              } else {
-                const int slot = sk_lo(cc, units, grid) / nkb == t ? 0 : 1;
-                const float4* op = reinterpret_cast<const float4*>(
-                    a.part + ((int64_t)cc * 2 + slot) * kPartFloats + (int64_t)lrow * BN + c0 + c);
-                float4 o[8];
-#pragma unroll
-                for (int v = 0; v < 8; ++v) o[v] = __ldcg(op + v);
-#pragma unroll
-                for (int v = 0; v < 8; ++v) {
-                  f[4 * v] += o[v].x;
-                  f[4 * v + 1] += o[v].y;
-                  f[4 * v + 2] += o[v].z;
-                  f[4 * v + 3] += o[v].w;
+                  for (int e = 0; e < 32; ++e) f[e] += m[e];
+                } else {
+                  add_part(f, cc == o0 ? A : B);
                 }
               }
             }
