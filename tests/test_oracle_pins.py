@@ -42,7 +42,7 @@ def test_sylvester_natural_order_closed_form():
         assert H[i, j] == (-1) ** bin(i & j).count("1")
 
 
-@pytest.mark.parametrize("n", [1, 2, 4, 8, 32, 128, 1024])
+@pytest.mark.parametrize("n", [1, 2, 4, 8, 32, 128, 512, 1024, 2048])
 def test_fwht_equals_explicit_matrix(n):
     rng = np.random.default_rng(n)
     K = 3 * n
@@ -93,6 +93,31 @@ def test_fwht_closed_forms_block_1024():
     dj[j] = 1.0
     col = np.array([(-1) ** bin(i & j).count("1") for i in range(K)]) / 32
     np.testing.assert_array_equal(oracle.fwht(dj, 1024), col)
+
+
+@pytest.mark.parametrize("n", [512, 2048, 4096])
+def test_fwht_closed_forms_other_blocks(n):
+    # the pack's loader also accepts blocks 512, 2048 and 4096 (scale 1/sqrt(n): 1/(16 sqrt 2),
+    # 1/(32 sqrt 2), 1/64)
+    K = 2 * n
+    delta = np.zeros(K)
+    delta[n] = 1.0  # first element of the second block
+    want = np.zeros(K)
+    want[n:] = 1 / np.sqrt(n)
+    np.testing.assert_allclose(oracle.fwht(delta, n), want, rtol=1e-15, atol=0)
+    ones = np.ones(K)
+    want = np.zeros(K)
+    want[0] = want[n] = np.sqrt(n)
+    np.testing.assert_allclose(oracle.fwht(ones, n), want, rtol=1e-15, atol=1e-12)
+    j = (n // 2) | 5
+    dj = np.zeros(n)
+    dj[j] = 1.0
+    col = np.array([(-1) ** bin(i & j).count("1") for i in range(n)]) / np.sqrt(n)
+    np.testing.assert_allclose(oracle.fwht(dj, n), col, rtol=1e-15, atol=0)
+    # signs on the inverse path come last: s * (H/sqrt n) x
+    s_ = ti.rademacher_signs(n, K)
+    x = np.random.default_rng(n).standard_normal(K)
+    np.testing.assert_allclose(oracle.fwht(oracle.fwht(x, n, s_), n, s_, inverse=True), x, atol=1e-12)
 
 
 def test_fwht_involution_parseval_and_signs():
