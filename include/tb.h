@@ -56,7 +56,8 @@ enum {
   TB_OK = 0,
   TB_ERR_NULL = -1,        /* a required pointer is NULL */
   TB_ERR_SHAPE = -2,       /* M, N, K, T, V or D out of range or not a multiple it must be */
-  TB_ERR_UNSUPPORTED = -3, /* block other than 0 or 1024, or an algorithm not built */
+  TB_ERR_UNSUPPORTED = -3, /* block not 0, 512, 1024, 2048 or 4096 (the chain and the
+                              no-allocation GEMV: not 0 or 1024), or an algorithm not built */
   TB_ERR_VALUE = -4,       /* a host-checked value is invalid */
   TB_ERR_CUDA = -5,        /* a CUDA launch or query failed (see tb_last_cuda_error) */
   TB_ERR_ALIGN = -6,       /* a device pointer is not 16-byte aligned */
@@ -107,15 +108,18 @@ int tb_pack_w2(const int8_t* codes, const uint16_t* scales, int64_t N, int64_t K
 int tb_unpack_w2(const uint32_t* w, int64_t N, int64_t K, int8_t* codes, void* stream);
 
 /*
- * tb_fwht — sign * normalised Walsh-Hadamard transform over blocks of 1024.
+ * tb_fwht — sign * normalised Walsh-Hadamard transform over blocks of `block` elements.
  * [ARCH] "Hadamard 旋转": fwht uses hadamard_transform with scale 1/sqrt(block);
  * forward multiplies by the signs first, the inverse multiplies by them again at the end.
+ * [PACK] "仿射 2-bit 格式与 Prism contract v1": the pack uses block 1024; its loader also
+ * accepts 512, 2048 and 4096.
  *   x  fp16 [M, K];  y fp16 [M, K] (out; y may equal x);
  *   signs int8 [K] of +-1, or NULL for all +1 (not checked on the device);
- *   forward (inverse = 0): y = (H/32) (signs * x) per block;
- *   inverse (inverse = 1): y = signs * ((H/32) x) per block.
- * Computed in fp32, rounded to fp16 (round to nearest even).  block must be 1024,
- * K a positive multiple of 1024, M >= 1.
+ *   forward (inverse = 0): y = (H/sqrt(block)) (signs * x) per block;
+ *   inverse (inverse = 1): y = signs * ((H/sqrt(block)) x) per block.
+ * Computed in fp32 (the scale 1/sqrt(block) rounded to fp32 for 512 and 2048, exact for
+ * 1024 and 4096), rounded to fp16 (round to nearest even).  block: 512, 1024, 2048 or 4096
+ * (else TB_ERR_UNSUPPORTED); K a positive multiple of block, M >= 1.
  */
 int tb_fwht(const uint16_t* x, uint16_t* y, const int8_t* signs, int64_t M, int64_t K,
             int block, int inverse, void* stream);
@@ -124,7 +128,9 @@ int tb_fwht(const uint16_t* x, uint16_t* y, const int8_t* signs, int64_t M, int6
  * Bytes of workspace tb_packed_linear uses for these sizes.  Layout: a fixup region
  * (about 2 MB) for the decode GEMV's split schedule: counters of output tiles shared by
  * several SMs in its first 1024 bytes, then the SMs' fp32 parts of those tiles; then, for
- * the tensor-core path, the rotated activations x' (fp16 [M, K]).  The first 1024 bytes
+ * the tensor-core path, the rotated activations x' (fp16 [M, K]) and the split schedule's
+ * counters and parts; then, for a block other than 0 and 1024, x' in natural order (fp16
+ * [M, K]).  The first 1024 bytes
  * must be zero before the first call that uses the workspace (zero-filling the whole
  * workspace will do); every completed call leaves them zero (a call that reported
  * TB_DEV_TIMEOUT may not: zero them again).  Calls sharing one workspace must be
@@ -144,11 +150,14 @@ size_t tb_packed_linear_algo_workspace_size(int64_t M, int64_t K, int64_t N, int
  *   w uint32 [N, K/16]; scales fp16 [N, K/128]; biases fp16 [N, K/128] or NULL
  *   (scale-only, b = -s); y fp16 [M, N] (out).
  * fp32 accumulation, fp16 output (round to nearest even).
- * K: positive multiple of 1024 when block = 1024, of 128 when block = 0.  M, N >= 1.
+ * block: 1024 (the pack's; the transform is fused into the matmul kernels), 0 (no transform),
+ * or 512, 2048, 4096 (accepted by the pack's loader: x' = tb_fwht(x) into the workspace
+ * first, then the matmul on it; the same x' rounded to fp16, one more launch).
+ * K: positive multiple of 128 and of block.  M, N >= 1.
  * workspace: device memory of at least tb_packed_linear_workspace_size(...) bytes,
- * zero-filled before its first use (see above).  The GEMV path (M <= 8) also runs with
- * workspace = NULL, then with output tiles never split between SMs (slower on shapes
- * whose row-tile count is not a multiple of the SM count).
+ * zero-filled before its first use (see above).  The GEMV path (M <= 8) with block 0 or 1024
+ * also runs with workspace = NULL, then with output tiles never split between SMs (slower on
+ * shapes whose row-tile count is not a multiple of the SM count).
  * dev_status optional (TB_DEV_TIMEOUT).
  */
 int tb_packed_linear(const uint16_t* x, int64_t M, int64_t K, const int8_t* signs, int block,
@@ -169,7 +178,8 @@ int tb_packed_linear_algo(const uint16_t* x, int64_t M, int64_t K, const int8_t*
  * modules that share x also share x' = fwht(x)).  x' is computed once per launch; matrix i
  * writes y[i] (fp16 [M, N[i]]).  w, scales, biases, N, y are HOST arrays of n entries holding
  * device pointers / row counts; biases (the array, or any entry) may be NULL (scale-only for
- * those matrices); K must be a positive multiple of 1024.  Workspace as for
+ * those matrices); K must be a positive multiple of 1024 (and of block); block as for
+ * tb_packed_linear (512, 2048, 4096: x' computed once into the workspace).  Workspace as for
  * tb_packed_linear, sized with tb_packed_linear_workspace_size(M, K, max N, block).
  * M <= 8: one decode GEMV launch for all matrices.  M > 8: one rotation, then one tensor-core
  * GEMM per matrix.
@@ -250,7 +260,10 @@ int tb_chain_run(const void* plan, int n_links, int64_t M, int64_t max_K, void* 
  *   (scale-only, b = -s);
  *   signs int8 [D] (+-1) or NULL (all +1); out fp16 [T, D] (out).
  * An id outside [0, V) writes a row of zeros and sets TB_DEV_BAD_ID in dev_status.
- * block 1024 (D a multiple of 1024) or 0 (D a multiple of 128); T >= 0 (T = 0 is a no-op).
+ * block 1024 (fused), 512, 2048 or 4096 (the rows decoded into out, then the inverse
+ * tb_fwht in place: the same result, since the pack's rows {-s, 0, s} are exact in fp16;
+ * rows of a general affine bias are rounded to fp16 before that transform), or 0; D a
+ * multiple of 128 and of block; T >= 0 (T = 0 is a no-op).
  */
 int tb_embed_lookup(const int32_t* ids, int64_t T, const uint32_t* w, const uint16_t* scales,
                     const uint16_t* biases, int64_t V, int64_t D, const int8_t* signs, int block,

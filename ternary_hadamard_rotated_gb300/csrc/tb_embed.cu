@@ -80,8 +80,8 @@ extern "C" int tb_embed_lookup(const int32_t* ids, int64_t T, const uint32_t* w,
                                int32_t* dev_status, void* stream) {
   using namespace tb;
   if (T < 0 || V < 1 || D < kGroup || D % kGroup) return TB_ERR_SHAPE;
-  if (block != 0 && block != kBlock) return TB_ERR_UNSUPPORTED;
-  if (block == kBlock && D % kBlock) return TB_ERR_SHAPE;
+  if (block != 0 && !supported_block(block)) return TB_ERR_UNSUPPORTED;
+  if (block && D % block) return TB_ERR_SHAPE;
   if (T == 0) return TB_OK;
   if (!ids || !w || !scales || !out) return TB_ERR_NULL;  // biases may be NULL
   if (!aligned16(w) || !aligned16(scales) || (biases && !aligned16(biases)) || !aligned16(out) ||
@@ -94,8 +94,14 @@ extern "C" int tb_embed_lookup(const int32_t* ids, int64_t T, const uint32_t* w,
   int64_t blocks = (items + kEmbWarps - 1) / kEmbWarps;
   const int64_t cap = (int64_t)f.sms * 8;
   if (blocks > cap) blocks = cap;
-  embed_kernel<<<(int)blocks, kEmbWarps * 32, 0, static_cast<cudaStream_t>(stream)>>>(
+  // block 1024 is fused; another block decodes the rows (exact in fp16: {-s, 0, s}) and then
+  // runs the inverse transform in place, which computes the same as the fused kernel
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  embed_kernel<<<(int)blocks, kEmbWarps * 32, 0, s>>>(
       ids, T, w, reinterpret_cast<const __half*>(scales), reinterpret_cast<const __half*>(biases), V,
-      D, signs, block != 0, reinterpret_cast<__half*>(out), dev_status);
-  return check_launch();
+      D, signs, block == kBlock, reinterpret_cast<__half*>(out), dev_status);
+  rc = check_launch();
+  if (rc != TB_OK || block == 0 || block == kBlock) return rc;
+  return launch_fwht(reinterpret_cast<const __half*>(out), reinterpret_cast<__half*>(out), signs, T, D,
+                     block, 1, s);
 }

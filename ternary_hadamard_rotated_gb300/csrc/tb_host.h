@@ -1,6 +1,7 @@
 // Host-side helpers of the C ABI: argument checks, CUDA error capture, device facts.
 #pragma once
 
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -21,6 +22,16 @@ inline int check_launch() {
 }
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Hadamard block sizes the transform accepts (the pack's loader takes 512 .. 4096); 1024 is the
+// pack's own and the one the fused kernels run, the others go through a separate transform
+inline bool supported_block(int block) {
+  return block == 512 || block == 1024 || block == 2048 || block == 4096;
+}
+
+// y = fwht(x) over blocks of `block` (a supported size; K a multiple of it); y may equal x
+int launch_fwht(const __half* x, __half* y, const int8_t* signs, int64_t M, int64_t K, int block,
+                int inverse, cudaStream_t s);
 
 // streaming multiprocessors and opt-in shared memory of the current device
 struct DeviceFacts {

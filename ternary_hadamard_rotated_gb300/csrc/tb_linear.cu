@@ -36,8 +36,15 @@ int launch_gemm_tc_rotated(const __half* xp, int64_t M, int64_t K, const uint32_
 constexpr int kMaxMulti = 4;
 
 // Workspace layout: [fixup region of the GEMV split schedule (zero before the first call,
-// left zero by every completed call)][x' of the tensor-core path], 1 KB aligned.
+// left zero by every completed call)][the tensor-core path's x' in pair order, counters and
+// parts][x' in natural order for a block other than 1024], 1 KB aligned.
 static size_t fixup_region() { return (gemv_fixup_bytes() + 1023) / 1024 * 1024; }
+
+// Blocks 512, 2048 and 4096 are not fused into the matmul kernels: x' = fwht(x) goes through
+// the workspace first, then the matmul runs unrotated on it (the same x', rounded to fp16, that
+// the fused kernels compute for block 1024).
+static bool separate_block(int block) { return block != 0 && block != kBlock; }
+static size_t natural_x_bytes(int64_t M, int64_t K) { return (size_t)((M * K * 2 + 1023) / 1024 * 1024); }
 
 // decode (GEMV) up to this many tokens; the tensor-core GEMM above
 constexpr int64_t kGemvMaxTokens = 8;
@@ -48,10 +55,25 @@ static int resolve_algo(int64_t M, int algo) {
 }
 
 static int check_linear_shape(int64_t M, int64_t K, int block, int64_t N) {
-  if (block != 0 && block != kBlock) return TB_ERR_UNSUPPORTED;
+  if (block != 0 && !supported_block(block)) return TB_ERR_UNSUPPORTED;
   if (M < 1 || N < 1 || K < kGroup || K % kGroup) return TB_ERR_SHAPE;
-  if (block == kBlock && K % kBlock) return TB_ERR_SHAPE;
+  if (block && K % block) return TB_ERR_SHAPE;
   return TB_OK;
+}
+
+// bytes of workspace one call needs: the GEMV's fixup region, the tensor-core path's x' and
+// schedule state, and x' in natural order for a block that is not fused
+static size_t linear_workspace(int64_t M, int64_t K, int64_t N, int block, int use) {
+  size_t b = fixup_region();
+  if (use == TB_ALGO_TC) b += gemm_tc_workspace(M, K, N);
+  if (separate_block(block)) b += natural_x_bytes(M, K);
+  return b;
+}
+
+// where x' in natural order goes: after everything the matmul path itself uses
+static __half* natural_x(void* workspace, int64_t M, int64_t K, int64_t N, int use) {
+  return reinterpret_cast<__half*>(static_cast<char*>(workspace) + fixup_region() +
+                                   (use == TB_ALGO_TC ? gemm_tc_workspace(M, K, N) : 0));
 }
 
 }  // namespace tb
@@ -60,7 +82,7 @@ extern "C" size_t tb_packed_linear_algo_workspace_size(int64_t M, int64_t K, int
                                                        int algo) {
   using namespace tb;
   if (check_linear_shape(M, K, block, N) != TB_OK) return 0;
-  return fixup_region() + (resolve_algo(M, algo) == TB_ALGO_TC ? gemm_tc_workspace(M, K, N) : 0);
+  return linear_workspace(M, K, N, block, resolve_algo(M, algo));
 }
 
 extern "C" size_t tb_packed_linear_workspace_size(int64_t M, int64_t K, int64_t N, int block) {
@@ -88,6 +110,15 @@ extern "C" int tb_packed_linear_algo(const uint16_t* x, int64_t M, int64_t K, co
   const __half* sh = reinterpret_cast<const __half*>(scales);
   const __half* bh = reinterpret_cast<const __half*>(biases);
   __half* yh = reinterpret_cast<__half*>(y);
+  if (separate_block(block)) {  // x' = fwht(x) into the workspace, then the unrotated matmul
+    if (!workspace || workspace_bytes < linear_workspace(M, K, N, block, use)) return TB_ERR_WORKSPACE;
+    __half* xn = natural_x(workspace, M, K, N, use);
+    int rc2 = launch_fwht(xh, xn, sg, M, K, block, 0, s);
+    if (rc2 != TB_OK) return rc2;
+    xh = xn;
+    sg = nullptr;
+    block = 0;
+  }
   if (use == TB_ALGO_TC) {
     const size_t need = fixup_region() + gemm_tc_workspace(M, K, N);
     if (!workspace || workspace_bytes < need) return TB_ERR_WORKSPACE;
@@ -116,8 +147,8 @@ extern "C" int tb_packed_linear_multi(const uint16_t* x, int64_t M, int64_t K, c
   using namespace tb;
   if (!x || !w || !scales || !N || !y) return TB_ERR_NULL;  // biases (or an entry) may be NULL
   if (n < 1 || n > kMaxMulti) return TB_ERR_SHAPE;
-  if (block != 0 && block != kBlock) return TB_ERR_UNSUPPORTED;
-  if (M < 1 || K < kBlock || K % kBlock) return TB_ERR_SHAPE;
+  if (block != 0 && !supported_block(block)) return TB_ERR_UNSUPPORTED;
+  if (M < 1 || K < kBlock || K % kBlock || (block && K % block)) return TB_ERR_SHAPE;
   if (!aligned16(x) || (signs && !aligned16(signs)) || (workspace && !aligned16(workspace)))
     return TB_ERR_ALIGN;
   const __half* sh[kMaxMulti];
@@ -136,6 +167,18 @@ extern "C" int tb_packed_linear_multi(const uint16_t* x, int64_t M, int64_t K, c
   const int8_t* sg = block ? signs : nullptr;
   const __half* xh = reinterpret_cast<const __half*>(x);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (separate_block(block)) {  // x' once into the workspace, then the unrotated matrices
+    int64_t maxN = 0;
+    for (int i = 0; i < n; ++i) maxN = N[i] > maxN ? N[i] : maxN;
+    const int use = M <= kGemvMaxTokens ? TB_ALGO_GEMV : TB_ALGO_TC;
+    if (!workspace || workspace_bytes < linear_workspace(M, K, maxN, block, use)) return TB_ERR_WORKSPACE;
+    __half* xn = natural_x(workspace, M, K, maxN, use);
+    int rc2 = launch_fwht(xh, xn, sg, M, K, block, 0, s);
+    if (rc2 != TB_OK) return rc2;
+    xh = xn;
+    sg = nullptr;
+    block = 0;
+  }
   if (M <= kGemvMaxTokens)
     return launch_gemv_tma_multi(xh, M, K, sg, block, n, w, sh, bh, N, yh, workspace, workspace_bytes,
                                  dev_status, s);

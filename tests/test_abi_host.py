@@ -67,8 +67,11 @@ def test_packed_linear_refuses_bad_arguments(lib):
     assert call(x=None) == -1
     assert call(w=None) == -1
     assert call(y=None) == -1
-    assert call(block=512) == -3          # only 1024 (and 0 = not folded) are built
-    assert call(block=2048) == -3
+    assert call(block=256) == -3          # 512, 1024, 2048, 4096 (and 0 = not folded) only
+    assert call(block=8192) == -3
+    assert call(block=2048) == -2         # K = 1024 is not a multiple of the block
+    assert call(block=4096, K=2048) == -2
+    assert call(block=2048, K=2048) == -7  # x' of an unfused block goes through the workspace
     assert call(K=1000) == -2             # not a multiple of 128
     assert call(K=1152) == -2             # a multiple of 128 but not of the 1024 block
     assert call(M=0) == -2
@@ -113,12 +116,16 @@ def test_other_entry_points_refuse_bad_arguments(lib):
     assert lib.tb_pack_w2(P, P, 4, 100, P, P, None, None) == -2
     assert lib.tb_pack_w2(P, P, 0, 128, P, P, None, None) == -2
     assert lib.tb_unpack_w2(P, 4, 20, P, None) == -2
-    assert lib.tb_fwht(P, P, None, 2, 1024, 512, 0, None) == -3
+    assert lib.tb_fwht(P, P, None, 2, 1024, 256, 0, None) == -3
+    assert lib.tb_fwht(P, P, None, 2, 1024, 768, 0, None) == -3
     assert lib.tb_fwht(P, P, None, 2, 1536, 1024, 0, None) == -2
+    assert lib.tb_fwht(P, P, None, 2, 2048, 4096, 0, None) == -2
+    assert lib.tb_fwht(P, P, None, 2, 6144, 4096, 0, None) == -2
     assert lib.tb_fwht(P + 8, P, None, 2, 1024, 1024, 0, None) == -6
     e = lib.tb_embed_lookup
     assert e(P, 4, P, P, P, 100, 1000, None, 1024, P, None, None) == -2
-    assert e(P, 4, P, P, P, 100, 1024, None, 4096, P, None, None) == -3
+    assert e(P, 4, P, P, P, 100, 1024, None, 4096, P, None, None) == -2   # D not a multiple of block
+    assert e(P, 4, P, P, P, 100, 1024, None, 256, P, None, None) == -3
     assert e(P, 4, P, P, P, 0, 1024, None, 1024, P, None, None) == -2
     assert e(P, 0, P, P, P, 100, 1024, None, 1024, P, None, None) == 0   # T = 0: no-op
     assert e(None, 4, P, P, P, 100, 1024, None, 1024, P, None, None) == -1
@@ -135,7 +142,10 @@ def test_multi_refuses_bad_arguments(lib):
     assert f(P, 1, 1024, P, 1024, 5, arr, arr, arr, ns, arr, None, 0, None, None) == -2   # n > 4
     assert f(P, 1, 1024, P, 1024, 0, arr, arr, arr, ns, arr, None, 0, None, None) == -2   # n < 1
     assert f(P, 1, 1536, P, 1024, 2, arr, arr, arr, ns, arr, None, 0, None, None) == -2   # K % 1024
-    assert f(P, 1, 1024, P, 512, 2, arr, arr, arr, ns, arr, None, 0, None, None) == -3
+    assert f(P, 1, 1024, P, 256, 2, arr, arr, arr, ns, arr, None, 0, None, None) == -3
+    assert f(P, 1, 1024, P, 2048, 2, arr, arr, arr, ns, arr, None, 0, None, None) == -2
+    # a block other than 1024 needs the workspace for x' even on the decode path
+    assert f(P, 1, 2048, P, 2048, 2, arr, arr, arr, ns, arr, None, 0, None, None) == -7
     assert f(None, 1, 1024, P, 1024, 2, arr, arr, arr, ns, arr, None, 0, None, None) == -1
     nul = (ctypes.c_void_p * 2)(P, None)
     assert f(P, 1, 1024, P, 1024, 2, nul, arr, arr, ns, arr, None, 0, None, None) == -1
