@@ -374,3 +374,78 @@ def test_generators_distribution_and_row_independence():
     assert set(np.unique(sg).tolist()) == {-1, 1}
     assert len(ti.sweep_layers()) == 401
     assert ti.sweep_weight_count() == 25_095_045_120
+
+
+# ----------------------------------------------------------------------------
+# GGUF block formats (PQ2_0, PTQ1_0) and their transcoding into the W2 container
+# ----------------------------------------------------------------------------
+def _golden_blocks():
+    out = []
+    for r in read_golden("gguf_blocks.txt"):
+        fmt, sbits, fill, nlead = r[0], int(r[1], 16), int(r[2]), int(r[3])
+        lead = [int(v) for v in r[4:4 + nlead]]
+        byts = np.array([int(v, 16) for v in r[4 + nlead:]], dtype=np.uint8)
+        t = np.full((1, 128), fill, dtype=np.int8)
+        t[0, :nlead] = lead
+        d = np.array([[sbits]], np.uint16).view(np.float16)
+        out.append((fmt, t, d, byts))
+    return out
+
+
+def test_gguf_blocks_golden():
+    rows = _golden_blocks()
+    assert len(rows) == 8
+    for fmt, t, d, byts in rows:
+        enc = oracle.pq2_0_encode if fmt == "PQ2_0" else oracle.ptq1_0_encode
+        dec = oracle.pq2_0_decode if fmt == "PQ2_0" else oracle.ptq1_0_decode
+        got = enc(t, d)
+        assert got.shape == (1, 1, oracle.PQ2_0_BYTES if fmt == "PQ2_0" else oracle.PTQ1_0_BYTES)
+        np.testing.assert_array_equal(got[0, 0], byts, err_msg=fmt)
+        t2, d2 = dec(byts.reshape(1, 1, -1), 128)
+        np.testing.assert_array_equal(t2, t)
+        np.testing.assert_array_equal(d2.view(np.uint16), d.view(np.uint16))
+
+
+def test_gguf_pq2_0_slots_are_the_w2_words():
+    # with the same slot order, a PQ2_0 block's 32 code bytes are the little-endian bytes of
+    # the group's eight W2 words (both put code i at bits 2 (i % 16) of its word)
+    t = ti.ternary_codes(21, 0, 3, 384)
+    d = ti.group_scales(21, 0, 3, 3)
+    blocks = oracle.pq2_0_encode(t, d)
+    words = oracle.pack_w2(t).reshape(3, 3, 8)
+    np.testing.assert_array_equal(blocks[:, :, 2:], words.view(np.uint8).reshape(3, 3, 32))
+
+
+@pytest.mark.parametrize("fmt", ["PQ2_0", "PTQ1_0"])
+def test_gguf_round_trip_and_transcode(fmt):
+    N, K = 5, 640
+    t = ti.ternary_codes(22, 0, N, K)
+    d = ti.group_scales(22, 0, N, K // 128)
+    enc = oracle.pq2_0_encode if fmt == "PQ2_0" else oracle.ptq1_0_encode
+    blocks = enc(t, d)
+    w, s, b = oracle.transcode_to_w2(blocks, fmt, K)
+    # lossless: the container holds exactly the trits and scales the blocks held
+    np.testing.assert_array_equal(oracle.unpack_w2(w, K), t)
+    np.testing.assert_array_equal(s.view(np.uint16), d.view(np.uint16))
+    np.testing.assert_array_equal(b.view(np.uint16), (d.view(np.uint16) ^ 0x8000))
+    W = oracle.decode_w2(w, s, b, K)
+    np.testing.assert_array_equal(W, t * np.repeat(d.astype(np.float64), 128, axis=1))
+
+
+def test_gguf_invalid_blocks_refused():
+    t = np.zeros((1, 128), np.int8)
+    d = np.ones((1, 1), np.float16)
+    pq = oracle.pq2_0_encode(t, d)
+    pq[0, 0, 7] = 0xFF  # slot value 3
+    with pytest.raises(ValueError):
+        oracle.pq2_0_decode(pq, 128)
+    pt = oracle.ptq1_0_encode(t, d)
+    pt[0, 0, 5] = 243  # not five base-3 digits
+    with pytest.raises(ValueError):
+        oracle.ptq1_0_decode(pt, 128)
+    pt = oracle.ptq1_0_encode(t, d)
+    pt[0, 0, 27] = 13 + 81  # a digit past trit 127
+    with pytest.raises(ValueError):
+        oracle.ptq1_0_decode(pt, 128)
+    with pytest.raises(ValueError):
+        oracle.transcode_to_w2(pq, "Q4_0", 128)
