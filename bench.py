@@ -700,6 +700,57 @@ def run_fwht(args, dist, tb, tdev, torch):
             "rows": rows}
 
 
+def run_transcode(args, dist, tb, tdev, torch):
+    """tb_transcode_gguf on the lm_head-sized table (248320 x 5120), both GGUF formats.
+
+    The blocks are random valid blocks built on the device: fp16 scales in [0.005, 0.02];
+    PQ2_0 code bytes drawn from the 81 bytes whose four 2-bit slots are all trits, PTQ1_0 bytes
+    uniform in [0, 243) (the last byte of a block in [0, 27)).  Bytes moved: the blocks read,
+    the words, scales and biases written."""
+    hbm, _, _, peak_kind = peaks()
+    dev = torch.device("cuda")
+    V, D = ti.VOCAB, ti.HIDDEN
+    nb = V * (D // 128)
+    g = torch.Generator(device=dev)
+    g.manual_seed(ti.config_seed(5, 700))
+    sc = (torch.rand(nb, generator=g, device=dev) * 0.015 + 0.005).half()
+    valid_pq = torch.tensor([v for v in range(256) if all(((v >> (2 * i)) & 3) < 3 for i in range(4))],
+                            dtype=torch.uint8, device=dev)
+    rows = []
+    for name, fmt, nbytes in (("PQ2_0", 1, 34), ("PTQ1_0", 2, 28)):
+        blocks = torch.empty((nb, nbytes), dtype=torch.uint8, device=dev)
+        blocks[:, 0:2] = sc.view(torch.uint8).view(nb, 2)
+        if fmt == 1:
+            idx = torch.randint(0, 81, (nb, 32), generator=g, device=dev)
+            blocks[:, 2:] = valid_pq[idx]
+        else:
+            blocks[:, 2:27] = torch.randint(0, 243, (nb, 25), generator=g, device=dev, dtype=torch.int32).to(torch.uint8)
+            blocks[:, 27] = torch.randint(0, 27, (nb,), generator=g, device=dev, dtype=torch.int32).to(torch.uint8)
+        w = torch.empty((V, D // 16), dtype=torch.int32, device=dev)
+        s_ = torch.empty((V, D // 128), dtype=torch.float16, device=dev)
+        b_ = torch.empty((V, D // 128), dtype=torch.float16, device=dev)
+        st = torch.zeros(1, dtype=torch.int32, device=dev)
+        for _ in range(3):
+            tb.tb_transcode_gguf(blocks, fmt, V, D, w, s_, b_, st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        reps = max(3, args.steps)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            tb.tb_transcode_gguf(blocks, fmt, V, D, w, s_, b_, st)
+        b.record()
+        torch.cuda.synchronize()
+        per = a.elapsed_time(b) / 1e3 / reps
+        byts = nb * (nbytes + 32 + 4)
+        rows.append({"format": name, "us": round(per * 1e6, 1), "GB/s": round(byts / per / 1e9, 1),
+                     "frac": round(byts / per / 1e9 / hbm, 4), "bytes": byts})
+        del blocks, w, s_, b_
+    return {"metric": "GGUF -> W2 transcode (tb_transcode_gguf), 248320 x 5120 table", "unit": "GB/s",
+            "peak": hbm, "peak_kind": peak_kind, "l2": "inputs and outputs of 0.6-0.7 GB, far larger than L2",
+            "rows": rows}
+
+
 def run_embed(args, dist, tb, tdev, torch):
     hbm, _, _, peak_kind = peaks()
     dev = torch.device("cuda")
@@ -784,7 +835,7 @@ def main():
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--config", default="sweep", choices=["sweep", "layers", "prefill", "batched", "embed", "fwht", "all"])
+    ap.add_argument("--config", default="sweep", choices=["sweep", "layers", "prefill", "batched", "embed", "fwht", "transcode", "all"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-step", action="store_true",
                     help="build the decode stack, run two steps and exit (for an ncu launch list)")
@@ -824,7 +875,8 @@ def main():
         configs = ["profile_fwht"]
     for c in configs:
         fn = {"sweep": run_sweep, "layers": run_layers, "prefill": run_prefill, "batched": run_batched,
-              "embed": run_embed, "fwht": run_fwht, "profile": profile_step, "profile_linear": profile_linear,
+              "embed": run_embed, "fwht": run_fwht, "transcode": run_transcode, "profile": profile_step,
+              "profile_linear": profile_linear,
               "profile_fwht": profile_fwht}[c]
         line = fn(args, dist, tb, tdev, torch)
         if rank == 0:

@@ -66,7 +66,8 @@ enum {
 };
 
 /* bits OR-ed into *dev_status by kernels */
-#define TB_DEV_BAD_CODE 1  /* tb_pack_w2: a code outside {-1,0,1} */
+#define TB_DEV_BAD_CODE 1  /* tb_pack_w2: a code outside {-1,0,1}; tb_transcode_gguf: a block
+                              slot or digit that is not a trit */
 #define TB_DEV_BAD_ID 2    /* tb_embed_lookup: an id outside [0, V) (its row is written as zeros) */
 #define TB_DEV_TIMEOUT 4   /* a bounded wait inside a kernel gave up; outputs are not valid */
 #define TB_DEV_BAD_PLAN 8  /* tb_chain_run: the plan does not match the launch (nothing computed) */
@@ -106,6 +107,31 @@ int tb_pack_w2(const int8_t* codes, const uint16_t* scales, int64_t N, int64_t K
  * K must be a positive multiple of 16, N >= 1.
  */
 int tb_unpack_w2(const uint32_t* w, int64_t N, int64_t K, int8_t* codes, void* stream);
+
+/* GGUF block formats of the same trits (tb_transcode_gguf) */
+#define TB_FMT_PQ2_0 1  /* 34 bytes per 128 weights: fp16 scale, 128 2-bit slots */
+#define TB_FMT_PTQ1_0 2 /* 28 bytes per 128 weights: fp16 scale, 128 trits five per byte */
+
+/*
+ * tb_transcode_gguf — lossless transcoding of GGUF blocks into the W2-g128 container.
+ * [ARCH] "打包格式的工程": PQ2_0 (34 bytes per 128 weights, each trit in a 2-bit slot) and
+ * PTQ1_0 (28 bytes, dense trits) carry the same trits and group scales; the transcoder takes
+ * the scale from the block header, sets the bias to its negation and rearranges the codes
+ * into uint32 words.  The page gives the block sizes, not the byte layout inside a block;
+ * the layout read here: bytes 0-1 the fp16 scale; PQ2_0: slot i at bits 2(i%4) of byte
+ * 2 + i/4, slot value t + 1; PTQ1_0: byte 2 + j = sum_i (t[5j+i] + 1) * 3^i over the trits
+ * 5j .. 5j+4 below 128 (first trit least significant; byte 27 holds trits 125..127).
+ *   blocks  uint8, N * (K/128) blocks back to back, row by row (row n, group g at block
+ *           n*K/128 + g); 2-byte aligned for PQ2_0, 4-byte aligned for PTQ1_0;
+ *   format  TB_FMT_PQ2_0 or TB_FMT_PTQ1_0 (else TB_ERR_UNSUPPORTED);
+ *   w       uint32 [N, K/16] (out), as tb_pack_w2 writes it; 16-byte aligned;
+ *   scales  fp16 [N, K/128] (out); biases fp16 [N, K/128] (out, = -scales) or NULL.
+ * K a positive multiple of 128, N >= 1.  dev_status optional: TB_DEV_BAD_CODE when a PQ2_0
+ * slot holds 3, a PTQ1_0 byte is 243 or more, or a digit past trit 127 is not zero (the
+ * outputs of such a block are then not valid).
+ */
+int tb_transcode_gguf(const uint8_t* blocks, int format, int64_t N, int64_t K, uint32_t* w,
+                      uint16_t* scales, uint16_t* biases, int32_t* dev_status, void* stream);
 
 /*
  * tb_fwht — sign * normalised Walsh-Hadamard transform over blocks of `block` elements.

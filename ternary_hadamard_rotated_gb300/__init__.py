@@ -37,6 +37,9 @@ TB_ALGO_AUTO = 0
 TB_ALGO_GEMV = 1
 TB_ALGO_TC = 2
 
+TB_FMT_PQ2_0 = 1
+TB_FMT_PTQ1_0 = 2
+
 _lib = None
 
 _P = ctypes.c_void_p
@@ -64,6 +67,7 @@ _SIGNATURES = {
     "tb_chain_workspace_size": (_SZ, []),
     "tb_chain_plan": (_INT, [_P, _INT, _I64, _P, _SZ, _P]),
     "tb_chain_run": (_INT, [_P, _INT, _I64, _I64, _P, _SZ, _P, _P]),
+    "tb_transcode_gguf": (_INT, [_P, _INT, _I64, _I64, _P, _P, _P, _P, _P]),
 }
 
 EXPORTED = tuple(_SIGNATURES)
@@ -121,6 +125,13 @@ def tb_pack_w2(codes, scales, w, biases, dev_status=None, stream=None):
     N, K = codes.shape
     _check("tb_pack_w2", load().tb_pack_w2(_ptr(codes), _ptr(scales), N, K, _ptr(w), _ptr(biases),
                                            _ptr(dev_status), _stream(stream)))
+
+
+def tb_transcode_gguf(blocks, fmt, N, K, w, scales, biases=None, dev_status=None, stream=None):
+    """GGUF blocks (uint8, N * K/128 blocks of 34 (PQ2_0) or 28 (PTQ1_0) bytes) -> the W2
+    container: w uint32 [N, K/16] (as int32), scales fp16 [N, K/128], biases = -scales (or None)."""
+    _check("tb_transcode_gguf", load().tb_transcode_gguf(_ptr(blocks), fmt, N, K, _ptr(w), _ptr(scales),
+                                                         _ptr(biases), _ptr(dev_status), _stream(stream)))
 
 
 def tb_unpack_w2(w, codes, stream=None):

@@ -133,6 +133,20 @@ def test_other_entry_points_refuse_bad_arguments(lib):
     assert e(P, 4, P, P, P + 2, 100, 1024, None, 1024, P, None, None) == -6
 
 
+def test_transcode_refuses_bad_arguments(lib):
+    import ternary_hadamard_rotated_gb300 as tb
+
+    f = lib.tb_transcode_gguf
+    assert f(None, 1, 4, 128, P, P, P, None, None) == tb.TB_ERR_NULL
+    assert f(P, 1, 4, 128, None, P, P, None, None) == tb.TB_ERR_NULL
+    assert f(P, 3, 4, 128, P, P, P, None, None) == tb.TB_ERR_UNSUPPORTED
+    assert f(P, 1, 0, 128, P, P, P, None, None) == tb.TB_ERR_SHAPE
+    assert f(P, 2, 4, 100, P, P, P, None, None) == tb.TB_ERR_SHAPE
+    assert f(P + 1, 1, 4, 128, P, P, P, None, None) == tb.TB_ERR_ALIGN   # PQ2_0: 2-byte blocks
+    assert f(P + 2, 2, 4, 128, P, P, P, None, None) == tb.TB_ERR_ALIGN   # PTQ1_0: 4-byte blocks
+    assert f(P, 1, 4, 128, P + 4, P, P, None, None) == tb.TB_ERR_ALIGN   # words 16-byte aligned
+
+
 def test_multi_refuses_bad_arguments(lib):
     import ctypes
 
