@@ -570,6 +570,10 @@ int launch_gemm_tc_rotated(const __half* xp, int64_t M, int64_t K, const uint32_
     else if (T2 < full) grid64 = T2 * std::min<int64_t>(4, sms / T2);  // q-way split of every tile
   } else if (tiles(1, 256) >= sms) { grid64 = sms; }
   else if (tiles(1, 256) >= full) {}
+  else if (tiles(1, 128) < full) {  // few tiles: every tile split into q <= 4 k-ranges
+    bn = 128;
+    grid64 = tiles(1, 128) * std::min<int64_t>(4, sms / tiles(1, 128));
+  }
   else if (ok128(tiles(1, 128)) || tiles(1, 128) < sms) { bn = 128; }
   else { bn = 128; grid64 = sms; }
   const int64_t T = tiles(nsub, bn);
