@@ -552,7 +552,8 @@ int launch_gemm_tc_rotated(const __half* xp, int64_t M, int64_t K, const uint32_
   // of smaller tiles; the per-k-block decode then hides behind the k-block's mma), as stream-K
   // over the SMs when every SM gets a tile, one CTA per tile when the tiles fill most of the
   // SMs, else every tile split into q <= 4 k-ranges.  Up to 128 tokens: 128 x 256 tiles the
-  // same way, else 128 x 128 tiles, one CTA each or stream-K when there are more than SMs.
+  // same way, or 128 x 128 tiles when those keep more SMs busy (the cost of a k-block grows with
+  // the tile's rows, so the count of SMs in use sets the time when tokens are few).
   DeviceFacts f;
   int rcf = device_facts(&f);
   if (rcf != TB_OK) return rcf;
@@ -562,20 +563,27 @@ int launch_gemm_tc_rotated(const __half* xp, int64_t M, int64_t K, const uint32_
   int nsub = 1, bn = 256;
   int64_t grid64 = 0;  // 0: one CTA per tile
   const int64_t full = sms * 4 / 5;
-  auto ok128 = [&](int64_t c) { return c >= full && (c <= sms || c >= 3 * sms); };
+  const int64_t nkb0 = K / kTcBK;  // a split never leaves a CTA without a k-block
   if (M > kTcBM) {
     nsub = 2;
     const int64_t T2 = tiles(2, 256);
     if (T2 >= sms) grid64 = sms;                            // stream-K, two CTAs per tile at most
-    else if (T2 < full) grid64 = T2 * std::min<int64_t>(4, sms / T2);  // q-way split of every tile
+    else if (T2 < full) grid64 = T2 * std::min<int64_t>(std::min<int64_t>(4, nkb0), sms / T2);
   } else if (tiles(1, 256) >= sms) { grid64 = sms; }
   else if (tiles(1, 256) >= full) {}
-  else if (tiles(1, 128) < full) {  // few tiles: every tile split into q <= 4 k-ranges
-    bn = 128;
-    grid64 = tiles(1, 128) * std::min<int64_t>(4, sms / tiles(1, 128));
+  else {  // few tiles: the tile width (256 or 128 rows, split into q <= 4 k-ranges, or one CTA
+          // per tile when they fill most of the SMs) that keeps the most SMs busy, 256 on a tie
+    const int64_t T256 = tiles(1, 256), T128 = tiles(1, 128);
+    const int64_t g256 = T256 * std::min<int64_t>(std::min<int64_t>(4, nkb0), sms / T256);
+    const int64_t g128 = T128 >= full ? std::min<int64_t>(T128, sms)
+                                      : T128 * std::min<int64_t>(std::min<int64_t>(4, nkb0), sms / T128);
+    if (g128 > g256) {
+      bn = 128;
+      grid64 = T128 >= sms ? sms : T128 >= full ? 0 : g128;
+    } else {
+      grid64 = g256;
+    }
   }
-  else if (ok128(tiles(1, 128)) || tiles(1, 128) < sms) { bn = 128; }
-  else { bn = 128; grid64 = sms; }
   const int64_t T = tiles(nsub, bn);
   const int64_t nkb = K / kTcBK;
   if (T * nkb > 0x7fffffffLL) return TB_ERR_SHAPE;

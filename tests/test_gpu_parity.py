@@ -265,6 +265,18 @@ def test_linear_tc_stream_k_split_tiles(tb, M, K, N):
     np.testing.assert_array_equal(y1.view(np.uint16), y2.view(np.uint16))
 
 
+@pytest.mark.parametrize("M,K,N", [(3, 128, 40), (100, 128, 300), (200, 128, 64), (130, 256, 520)])
+def test_linear_tc_short_k(tb, M, K, N):
+    # fewer 64-k blocks than the k split would want: no CTA may be left without one (its
+    # tile would never be finished), and the tile counters are left zero
+    x = ti.activations(M + K, M, K)
+    L = HostLayer(M + 3, N, K)
+    w, s, b = device_layer(M + 3, N, K, from_host=L)
+    y = run_linear(tb, x, None, 0, w, s, b, N, algo=2)
+    ref, bound = linear_reference(x, None, 0, L)
+    assert_linear_close(y, ref, bound, f"tc short k {M}x{K}x{N}")
+
+
 @pytest.mark.parametrize("M,K,N", [(512, 5120, 17408), (512, 17408, 5120), (4096, 5120, 17408),
                                    (4096, 17408, 5120)])
 def test_prefill_configs_sampled(tb, M, K, N):
