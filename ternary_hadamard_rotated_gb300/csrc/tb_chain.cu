@@ -499,12 +499,11 @@ __global__ void __launch_bounds__(kTmaThreads, 1) w2_gemv_chain_kernel(const __g
       if (n + 1 < ncnt) body(n + 1, sB, bB);
     }
 
-    // every output of this link from this CTA is written: count the link complete
+    // every output of this link from this CTA is written: count the link complete (a release
+    // reduction: the CTA's writes, ordered before it by the barrier, become visible first; the
+    // thread does not wait for a returned value)
     asm volatile("bar.sync 1, %0;" ::"n"(kTmaConsumers * 32) : "memory");
-    if (threadIdx.x == 0) {
-      fence_acq_rel_gpu();
-      atomicAdd(a.sync, 1u);
-    }
+    if (threadIdx.x == 0) asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(a.sync) : "memory");
   }
 
   // the last CTA to finish returns both counters to zero for the next launch (every CTA has
