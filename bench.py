@@ -9,7 +9,7 @@ scales and biases stream from HBM per token; the step is replayed as one CUDA
 graph.  Weights are far larger than L2, so no flush is needed between steps.
 
 Prints ONE JSON line (rank 0).  ``--config`` picks other workloads for profiling
-(layers, prefill, batched, embed, all); they print one JSON line each.
+(layers, prefill, batched, embed, fwht, transcode, all); they print one JSON line each.
 ``--impl reference`` times the float64 CPU oracle on a bounded sample instead.
 """
 from __future__ import annotations
@@ -866,7 +866,8 @@ def main():
     from tb_inputs import device as tdev
 
     tb.load()
-    configs = ["sweep", "layers", "prefill", "batched", "embed", "fwht"] if args.config == "all" else [args.config]
+    configs = (["sweep", "layers", "prefill", "batched", "embed", "fwht", "transcode"] if args.config == "all"
+               else [args.config])
     if args.profile_step:
         configs = ["profile"]
     if args.profile_linear:
