@@ -463,7 +463,7 @@ def run_sweep(args, dist, tb, tdev, torch):
                 "tok_s": round(n * args.steps / ssecs, 3),
                 "weights_gb_per_step": round((st.scale_only_bytes + ti.HIDDEN // 4 + ti.HIDDEN // 64) / 1e9, 4),
                 "note": "calls path with biases = NULL (each bias is the pack's -scale, not read); "
-                        "outputs bit-identical to the stored-bias step",
+                        "the same arithmetic on the same values as the stored-bias step",
             },
             "parallelism": f"replicas x{n}",
         },
