@@ -31,6 +31,13 @@ __global__ void __launch_bounds__(kEmbWarps * 32) embed_kernel(
   for (int64_t it = blockIdx.x * (int64_t)kEmbWarps + warp; it < T * nchunk;
        it += (int64_t)gridDim.x * kEmbWarps) {
     const int64_t t = it / nchunk, b = it - t * nchunk;
+    // the signs of this lane's 32 elements (layout A) do not depend on the id: loaded first
+    int4 sg[2] = {make_int4(0, 0, 0, 0), make_int4(0, 0, 0, 0)};
+    if (rotate && signs) {
+      const int4* sp = reinterpret_cast<const int4*>(signs + b * kBlock + lane * 32);
+      sg[0] = __ldg(sp);
+      sg[1] = __ldg(sp + 1);
+    }
     const int64_t id = ids[t];
     const bool ok = id >= 0 && id < V;
     if (!ok && b == 0 && lane == 0) set_status(status, TB_DEV_BAD_ID);
@@ -54,15 +61,16 @@ __global__ void __launch_bounds__(kEmbWarps * 32) embed_kernel(
     }
     __half* orow = out + t * D + b * kBlock;
     if (rotate) {
-      wht1024_a_to_b(v, scratch[warp], lane);  // v[j] = element j*32 + lane
-      const int8_t* sb = signs ? signs + b * kBlock : nullptr;
+      wht1024_a_to_b(v, scratch[warp], lane);     // v[j] = element j*32 + lane
+      transpose_b_to_a(v, scratch[warp], lane);   // back to v[r] = element lane*32 + r
+      const int8_t* sp = reinterpret_cast<const int8_t*>(sg);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        float f = v[j] * kInvSqrtBlock;
-        if (sb && sb[j * 32 + lane] < 0) f = -f;
-        orow[j * 32 + lane] = __float2half_rn(f);
+      for (int r = 0; r < 32; ++r) {
+        const float f = v[r] * kInvSqrtBlock;
+        v[r] = sp[r] < 0 ? -f : f;
       }
-    } else if (in) {
+    }
+    if (in) {
       uint4* dst = reinterpret_cast<uint4*>(orow + lane * 32);
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4)
