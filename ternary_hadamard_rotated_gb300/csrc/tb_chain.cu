@@ -128,8 +128,14 @@ TB_DEVI void link_group_range(const LinkRange& r, int u, int& glo, int& ghi) {
   ghi = u == 0 ? r.bnd1 : u == 1 ? r.bnd2 : r.hi;
 }
 
+// Warp roles: warps 0..11 consume (three unit groups of four), warp 12 produces; warps 13..15
+// only complete the producer's warpgroup so that registers can move between the roles: the
+// launch gives 128 per thread, the producer warpgroup drops to 56 and the consumers rise to 152
+// (12 x 32 x 152 + 4 x 32 x 56 = 65536, the block's whole launch allocation).  At 128 registers
+// for every warp the consumers spilled and a decode step took 6 % longer.
+constexpr int kChainThreads = 16 * 32;
 template <int MT>
-__global__ void __launch_bounds__(kTmaThreads, 1) w2_gemv_chain_kernel(const __grid_constant__ ChainRun a) {
+__global__ void __launch_bounds__(kChainThreads, 1) w2_gemv_chain_kernel(const __grid_constant__ ChainRun a) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -176,7 +182,9 @@ __global__ void __launch_bounds__(kTmaThreads, 1) w2_gemv_chain_kernel(const __g
     }
   };
 
-  if (warp == kTmaConsumers) {
+  if (warp >= kTmaConsumers) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 56;" ::: "memory");
+    if (warp != kTmaConsumers) return;
     // ---- producer: streams the codes of every link in order; never waits for a link's input
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
@@ -238,6 +246,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) w2_gemv_chain_kernel(const __g
   }
 
   // ---- consumers ----
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 152;" ::: "memory");
   const int g = lane >> 2, t = lane & 3;
   const int ug = warp / kWarpsPerUnit, wi = warp % kWarpsPerUnit;
   const bool back = ug == kGroupsOfWarps - 1;
@@ -551,7 +560,7 @@ static int launch_chain_mt(const ChainRun& a, int grid, cudaStream_t s) {
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kTmaThreads);
+  cfg.blockDim = dim3(kChainThreads);
   cfg.dynamicSmemBytes = bytes;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
