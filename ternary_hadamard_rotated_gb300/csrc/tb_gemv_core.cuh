@@ -26,7 +26,6 @@ constexpr int kSlotBytes = kUnitRows * 128;             // 16 KB box of packed c
 constexpr int kGroupsOfWarps = 3;                       // unit groups
 constexpr int kWarpsPerUnit = 4;                        // 32 rows each
 constexpr int kTmaConsumers = kGroupsOfWarps * kWarpsPerUnit;
-constexpr int kTmaThreads = (kTmaConsumers + 1) * 32;
 constexpr int kMaxSlotsPerGroup = 2;  // a deeper ring measured slower: it takes the L1 that the scale and activation loads hit
 constexpr int kPreIssue = 2;        // units per group issued before the activations are loaded
 constexpr int kCutSlots = 4;        // shared sums of tiles cut by a group or CTA boundary
