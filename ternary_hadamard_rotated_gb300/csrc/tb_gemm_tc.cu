@@ -491,23 +491,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 int launch_rotate_pairorder(const __half* x, __half* out, const int8_t* signs, int64_t M,
                             int64_t K, int rotate, cudaStream_t s);
 
-// cuTensorMapEncodeTiled from the driver, resolved once through the runtime (the library
-// does not link libcuda directly, so it loads on machines without a driver too)
-static PFN_cuTensorMapEncodeTiled_v12000 encode_tiled_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
-  return fn;
-}
-
 // Workspace of the tensor-core path (after the caller's fixup region):
 //   x'      fp16 [M, K], rotated activations;
 //   counts  int32 per output tile of the smallest tile shape (128 x 128), zero before a call
@@ -542,7 +525,7 @@ int launch_gemm_tc_rotated(const __half* xp, int64_t M, int64_t K, const uint32_
   const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
   const cuuint32_t box[2] = {(cuuint32_t)kTcBK, (cuuint32_t)kTcBM};
   const cuuint32_t estr[2] = {1, 1};
-  PFN_cuTensorMapEncodeTiled_v12000 encode = encode_tiled_fn();
+  PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
   if (!encode) return TB_ERR_CUDA;
   CUresult cr = encode(&tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<__half*>(xp), dims, strides,
                                        box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,

@@ -520,7 +520,9 @@ __global__ void __launch_bounds__(kWsThreads, 1)
 }
 
 // ------------------------------------------------------------------ host side
-static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+// cuTensorMapEncodeTiled from the driver, resolved once through the runtime (the library does not
+// link libcuda directly, so it loads on machines without a driver too); null if unavailable
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
   std::call_once(once, [] {
@@ -558,7 +560,7 @@ int code_map(const uint32_t* w, int64_t N, int64_t K, CUtensorMap* out) {
       return TB_OK;
     }
   }
-  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (!enc) return TB_ERR_CUDA;
   CUtensorMap m;
   const cuuint64_t dims[2] = {(cuuint64_t)(K / 16), (cuuint64_t)N};

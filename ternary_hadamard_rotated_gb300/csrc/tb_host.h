@@ -1,6 +1,7 @@
 // Host-side helpers of the C ABI: argument checks, CUDA error capture, device facts.
 #pragma once
 
+#include <cudaTypedefs.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -32,6 +33,9 @@ inline bool supported_block(int block) {
 // y = fwht(x) over blocks of `block` (a supported size; K a multiple of it); y may equal x
 int launch_fwht(const __half* x, __half* y, const int8_t* signs, int64_t M, int64_t K, int block,
                 int inverse, cudaStream_t s);
+
+// cuTensorMapEncodeTiled, looked up once (thread-safe); null when the driver lacks it
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 
 // streaming multiprocessors and opt-in shared memory of the current device
 struct DeviceFacts {
