@@ -252,6 +252,32 @@ TB_DEVI void wht1024_a_shfl(float (&v)[32], int lane) {
   }
 }
 
+// Unnormalised Walsh-Hadamard transform of 512 elements held by a warp as v[e] = element
+// lane*16 + e: four butterfly stages over the register index (element bits 0..3), then five
+// over the lane index (bits 4..8) with xor-shuffles; the layout is kept.
+TB_DEVI void wht512_a_shfl(float (&v)[16], int lane) {
+#pragma unroll
+  for (int h = 1; h < 16; h <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      if ((i & h) == 0) {
+        const float a = v[i], b = v[i + h];
+        v[i] = a + b;
+        v[i + h] = a - b;
+      }
+    }
+  }
+#pragma unroll
+  for (int h = 1; h < 32; h <<= 1) {
+    const float sg = (lane & h) ? -1.0f : 1.0f;  // upper partner keeps a - b
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+      const float p = __shfl_xor_sync(0xffffffffu, v[r], h);
+      v[r] = fmaf(sg, v[r], p);
+    }
+  }
+}
+
 // Same transform through a 4 KB shared scratch owned by the warp: 32 rows of 128 bytes, the
 // 16-byte chunk c of row i stored at position c ^ (i & 7).  Five stages over the register
 // index (element bits 0..4); each lane writes its row as eight 16-byte chunks; each lane reads

@@ -266,74 +266,97 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       }
     }
     const int nblk = (e1 - b1) + (e2 - b2);
+    // An item is one half of a (token, block) pair: since H1024 = [[H512, H512], [H512, -H512]],
+    // outputs 0..511 of the block are H512 (x_lo + x_hi) and outputs 512..1023 are
+    // H512 (x_lo - x_hi), two independent 512-point transforms on two warps.  Lane l holds
+    // elements 16 l .. 16 l + 15 of both input halves and of its output half.
+    auto item_block = [&](int it, int& tok, int& b, int& hh) {
+      hh = it & 1;
+      const int rest = it >> 1;
+      tok = rest / nblk;
+      const int bi = rest - tok * nblk;
+      b = bi < e1 - b1 ? b1 + bi : b2 + (bi - (e1 - b1));
+    };
     auto load_block = [&](int it, uint4 (&xr)[4], uint4 (&sr)[2]) {
-      const int tok = it / nblk, bi = it - tok * nblk;
-      const int b = bi < e1 - b1 ? b1 + bi : b2 + (bi - (e1 - b1));
+      int tok, b, hh;
+      item_block(it, tok, b, hh);
       if (tok < a.Mc) {
-        const uint4* xs = reinterpret_cast<const uint4*>(a.x + (int64_t)tok * K + b * kBlock + lane * 32);
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) xr[q4] = __ldg(xs + q4);
+        const uint4* xs = reinterpret_cast<const uint4*>(a.x + (int64_t)tok * K + b * kBlock + lane * 16);
+        xr[0] = __ldg(xs);
+        xr[1] = __ldg(xs + 1);
+        xr[2] = __ldg(xs + kBlock / 16);  // the same elements of the upper half
+        xr[3] = __ldg(xs + kBlock / 16 + 1);
       } else {
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) xr[q4] = make_uint4(0, 0, 0, 0);
       }
       if (a.signs) {
-        const uint4* sp = reinterpret_cast<const uint4*>(a.signs + b * kBlock + lane * 32);
+        const uint4* sp = reinterpret_cast<const uint4*>(a.signs + b * kBlock + lane * 16);
         sr[0] = __ldg(sp);
-        sr[1] = __ldg(sp + 1);
+        sr[1] = __ldg(sp + kBlock / 32);
       }
     };
     auto transform_block = [&](int it, const uint4 (&xr)[4], const uint4 (&sr)[2]) {
-      const int tok = it / nblk, bi = it - tok * nblk;
-      const int b = bi < e1 - b1 ? b1 + bi : b2 + (bi - (e1 - b1));
-      // layout A: v[r] = element b*1024 + lane*32 + r
-      float v[32];
+      int tok, b, hh;
+      item_block(it, tok, b, hh);
+      // v[e] = output element b*1024 + 512*hh + lane*16 + e
+      float v[16];
+      {
+        const __half* xl = reinterpret_cast<const __half*>(&xr[0]);
+        const __half* xh = reinterpret_cast<const __half*>(&xr[2]);
+        const int8_t* sl = reinterpret_cast<const int8_t*>(&sr[0]);
+        const int8_t* sh = reinterpret_cast<const int8_t*>(&sr[1]);
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        const __half* h = reinterpret_cast<const __half*>(&xr[q4]);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) v[8 * q4 + e] = __half2float(h[e]);
-      }
-      if (a.signs) {
-        const int8_t* sg = reinterpret_cast<const int8_t*>(sr);
-#pragma unroll
-        for (int r = 0; r < 32; ++r)
-          if (sg[r] < 0) v[r] = -v[r];
+        for (int e = 0; e < 16; ++e) {
+          float lo_ = __half2float(xl[e]), hi_ = __half2float(xh[e]);
+          if (a.signs) {
+            if (sl[e] < 0) lo_ = -lo_;
+            if (sh[e] < 0) hi_ = -hi_;
+          }
+          v[e] = a.rotate ? (hh ? lo_ - hi_ : lo_ + hi_) : (hh ? hi_ : lo_);
+        }
       }
       if (a.rotate) {
-        wht1024_a_shfl(v, lane);  // all ten stages, layout A kept
+        wht512_a_shfl(v, lane);  // the other nine stages, layout kept
 #pragma unroll
-        for (int r = 0; r < 32; ++r) v[r] *= kInvSqrtBlock;
+        for (int e = 0; e < 16; ++e) v[e] *= kInvSqrtBlock;
       }
-      const int grp = b * (kBlock / kGroup) + (lane >> 2);
+      // group of 128 of this output: eight lanes (q = lane & 7) of 16 elements each
+      const int grp = b * (kBlock / kGroup) + 4 * hh + (lane >> 3);
+      const int q = lane & 7;
       float ssum = 0.f, csum = 0.f;
 #pragma unroll
-      for (int r = 0; r < 32; ++r) {
-        v[r] = __half2float(__float2half_rn(v[r]));  // x' rounded to fp16
-        ssum += v[r];
+      for (int e = 0; e < 16; ++e) {
+        v[e] = __half2float(__float2half_rn(v[e]));  // x' rounded to fp16
+        ssum += v[e];
       }
       ssum += __shfl_xor_sync(0xffffffffu, ssum, 1);
       ssum += __shfl_xor_sync(0xffffffffu, ssum, 2);
+      ssum += __shfl_xor_sync(0xffffffffu, ssum, 4);
+      // B-fragment image: entry (grp, mp) holds, for each fragment lane t, group elements
+      // 32 t + 16 (mp >> 1) + 4 (mp & 1) + {0..3} and the same + 8, divided by sigma of their
+      // position; this lane's 16 elements are those of t = q >> 1 and mp = 2 (q & 1) + {0, 1}
 #pragma unroll
-      for (int mp = 0; mp < 4; ++mp) {
+      for (int m1 = 0; m1 < 2; ++m1) {
+        const int mp = 2 * (q & 1) + m1;
         uint32_t pk[4];
 #pragma unroll
         for (int e2 = 0; e2 < 4; ++e2) {
-          const int p = 4 * (mp & 1) + e2;
-          const int r = (mp >> 1) * 16 + p;
+          const int p = 4 * m1 + e2;
           const float is = inv_sigma_p(p);
-          const __half lo_ = __float2half_rn(v[r] * is), hi_ = __float2half_rn(v[r + 8] * is);
+          const __half lo_ = __float2half_rn(v[p] * is), hi_ = __float2half_rn(v[p + 8] * is);
           csum += __half2float(lo_) + __half2float(hi_);
           pk[e2] = (uint32_t)__half_as_ushort(lo_) | ((uint32_t)__half_as_ushort(hi_) << 16);
         }
-        *reinterpret_cast<uint4*>(img + ((size_t)(grp * 4 + mp) * MT + tok) * 32 + t * 8) =
+        *reinterpret_cast<uint4*>(img + ((size_t)(grp * 4 + mp) * MT + tok) * 32 + (q >> 1) * 8) =
             make_uint4(pk[0], pk[1], pk[2], pk[3]);
       }
       csum += __shfl_xor_sync(0xffffffffu, csum, 1);
       csum += __shfl_xor_sync(0xffffffffu, csum, 2);
-      if (t == 0) cs[grp * MT + tok] = make_float2(1024.f * csum, ssum);
+      csum += __shfl_xor_sync(0xffffffffu, csum, 4);
+      if (q == 0) cs[grp * MT + tok] = make_float2(1024.f * csum, ssum);
     };
-    const int items = MT * nblk;
+    const int items = 2 * MT * nblk;
     bool told = false;
     for (int it = warp; it < items; it += 2 * kTmaConsumers) {
       const int it2 = it + kTmaConsumers;
