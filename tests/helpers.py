@@ -102,3 +102,27 @@ def assert_transform_close(out_gpu, ref, block=1024, what=""):
     if bad.any():
         idx = np.argwhere(bad)[:5]
         raise AssertionError(f"{what}: {bad.sum()} of {bad.size} outside tolerance; first {idx.tolist()}")
+
+
+def compare_chain_runs(first, second, spec, ulps=8):
+    """Two runs of one chain on the same inputs: a link whose input is bit-identical in both runs
+    gives outputs within `ulps` fp16 ulps (+1e-6).  The only run-to-run freedom inside a link is
+    the order of the shared-memory fp32 sums of tiles cut between unit groups.  A link whose input
+    already differs is not compared: a last-place difference in its input moves every output by
+    an amount set by the input's scale, not by that output's own ulp.  Each run is held to the
+    oracle on its own inputs elsewhere.  `first` and `second` map buffer names to fp16 arrays;
+    `spec` is [(input name, [(output name, K, N), ...]), ...].  Returns the links compared."""
+    compared = []
+    for src, mats in spec:
+        if not np.array_equal(np.asarray(first[src]).view(np.uint16), np.asarray(second[src]).view(np.uint16)):
+            continue
+        for name, _, _ in mats:
+            a = np.asarray(first[name]).astype(np.float64)
+            b = np.asarray(second[name]).astype(np.float64)
+            ulp = np.spacing(np.abs(a).astype(np.float16)).astype(np.float64)
+            bad = ~(np.abs(a - b) <= ulps * ulp + 1e-6)
+            if bad.any():
+                raise AssertionError(f"{name}: {int(bad.sum())} outputs differ by more than {ulps} ulp "
+                                     f"between two runs on the same input {src}")
+        compared.append(src)
+    return compared
