@@ -246,9 +246,9 @@ __global__ void __launch_bounds__(kWsThreads, 1)
   asm volatile("griddepcontrol.wait;" ::: "memory");
   {
     // prologue: x' = fwht(signs * x) -> B-fragment image, (C, S) per group and token, for the
-    // 1024-blocks that this CTA's units read.  Every consumer warp takes items (token, block)
-    // warp, warp + 12, ...; the loads of two items are issued before either is transformed,
-    // so a warp waits once per pair.
+    // 1024-blocks that this CTA's units read.  Every consumer warp takes items (token, block,
+    // half) warp, warp + 12, ...; the loads of two items are issued before either is
+    // transformed, so a warp waits once per pair.
     const int nb = K / kBlock;
     int b1 = 0, e1 = nb, b2 = 0, e2 = 0;  // the blocks needed: [b1, e1) and [b2, e2)
     if (nst > 0 && nst < C) {
