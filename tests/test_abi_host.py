@@ -221,3 +221,25 @@ def test_chain_refuses_bad_arguments(lib):
     assert r(0x10040, 1, 1, 1024, P, 1 << 22, None, None) == tb.TB_ERR_ALIGN
     assert r(0x10000, 1, 1, 1024, P, 1024, None, None) == tb.TB_ERR_WORKSPACE
     assert r(0x10000, 1, 1, 1024, None, 1 << 22, None, None) == tb.TB_ERR_WORKSPACE
+
+
+def declared_prototypes():
+    """name -> number of parameters, from the prototypes in include/tb.h."""
+    src = open(os.path.join(ROOT, "include", "tb.h"), encoding="utf-8").read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", "", src)
+    out = {}
+    for m in re.finditer(r"\b(tb_[a-z0-9_]+)\s*\(([^()]*)\)\s*;", src):
+        params = m.group(2).strip()
+        out[m.group(1)] = 0 if params in ("", "void") else params.count(",") + 1
+    return out
+
+
+def test_binding_signatures_match_the_header():
+    import ternary_hadamard_rotated_gb300 as tb
+
+    protos = declared_prototypes()
+    assert set(protos) == set(declared_functions())
+    for name, n in protos.items():
+        assert name in tb._SIGNATURES, name
+        assert len(tb._SIGNATURES[name][1]) == n, (name, n, len(tb._SIGNATURES[name][1]))
