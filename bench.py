@@ -91,8 +91,89 @@ class Dist:
 
 
 # ---------------------------------------------------------------------------- clocks
+class NvmlSampler:
+    """Read-only NVML sampling (ctypes into the driver's libnvidia-ml) in a background thread:
+    SM clock, its maximum, power and the clock-event reasons every `period` seconds.  Short timed
+    regions (tens of ms) still get samples, which nvidia-smi's 100 ms loop would miss."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, torch_dev: int, period: float = 0.002):
+        import ctypes
+        import threading
+
+        self.ok = False
+        self.samples = []
+        self.period = period
+        self.stop_ev = threading.Event()
+        self.thread = None
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                return
+            h = ctypes.c_void_p()
+            bus = None
+            try:
+                import torch
+                pr = torch.cuda.get_device_properties(torch_dev)
+                bus = f"{pr.pci_domain_id:08x}:{pr.pci_bus_id:02x}:{pr.pci_device_id:02x}.0"
+            except Exception:
+                bus = None
+            if bus is None or lib.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(h)) != 0:
+                if lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(torch_dev), ctypes.byref(h)) != 0:
+                    return
+            self.lib, self.h = lib, h
+            mx = ctypes.c_uint()
+            self.max_mhz = float(mx.value) if lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0 else None
+            self.reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+            self.ok = True
+        except (OSError, AttributeError):
+            self.ok = False
+
+    def _one(self):
+        import ctypes
+        c, p, r = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        if self.lib.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(c)) != 0:
+            return None
+        self.lib.nvmlDeviceGetPowerUsage(self.h, ctypes.byref(p))
+        self.reasons_fn(self.h, ctypes.byref(r))
+        return time.time(), float(c.value), p.value / 1000.0, int(r.value)
+
+    def _run(self):
+        while not self.stop_ev.is_set():
+            v = self._one()
+            if v is not None:
+                self.samples.append(v)
+            time.sleep(self.period)
+
+    def start(self):
+        if self.ok:
+            import threading
+            self.thread = threading.Thread(target=self._run, daemon=True)
+            self.thread.start()
+
+    def stop(self, window):
+        if self.thread is not None:
+            self.stop_ev.set()
+            self.thread.join(timeout=5)
+        sel = [v for v in self.samples if window[0] <= v[0] <= window[1]]
+        if not sel:
+            return None
+        reasons = set()
+        for _, _, _, r in sel:
+            for bit, name in self.REASONS.items():
+                if r & bit:
+                    reasons.add(name)
+        return {"sm_mhz": float(np.median([v[1] for v in sel])), "sm_max_mhz": self.max_mhz,
+                "power_w_max": round(max(v[2] for v in sel), 1), "reasons": sorted(reasons),
+                "samples": len(sel), "source": f"NVML every {self.period * 1e3:.0f} ms in the timed region"}
+
+
 class Clocks:
-    """nvidia-smi sampling during the timed region."""
+    """Clock samples during the timed region: NVML at 2 ms (read-only), with nvidia-smi's
+    100 ms loop as the fallback where NVML cannot be loaded."""
 
     FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -102,12 +183,14 @@ class Clocks:
         self.index = index
         self.proc = None
         self.window = None
+        self.nvml = NvmlSampler(index)
 
     def mark(self, t0: float, t1: float):
         """Keep only samples taken between these wall-clock times (the timed region)."""
         self.window = (t0, t1)
 
     def start(self):
+        self.nvml.start()
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
@@ -117,8 +200,16 @@ class Clocks:
             self.proc = None
 
     def stop(self):
+        fast = self.nvml.stop(self.window or (0.0, float("inf")))
+        slow = self._stop_smi()
+        if fast is not None:
+            fast["nvidia_smi_samples"] = slow.get("samples", 0)
+            return fast
+        return slow
+
+    def _stop_smi(self):
         if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
         self.proc.terminate()
         out, _ = self.proc.communicate(timeout=10)
         sm, mx, reasons = [], None, set()
@@ -143,7 +234,7 @@ class Clocks:
                 if v.lower() == "active":
                     reasons.add(n)
         return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": mx,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm), "source": "nvidia-smi every 100 ms"}
 
 
 # ---------------------------------------------------------------------------- GPU workloads
@@ -282,6 +373,135 @@ def capture(torch, fn):
         fn()
     torch.cuda.synchronize()
     return g
+
+
+def sub_results(tb, st, torch, status, reps: int = 5):
+    """Compact per-kernel numbers on the resident stack (no new weights): every distinct link of
+    the decode step as its own CUDA graph over all its copies (GEMV GB/s), batched decode on the
+    64 gate_proj matrices, prefill on gate_proj and down_proj with the L2 flushed, and the
+    embedding of 256 ids."""
+    hbm, tf, _, _ = peaks()
+    dev = torch.device("cuda")
+    links = st.link_args()
+    ws = torch.zeros(tb.tb_packed_linear_workspace_size(64, ti.MLP, ti.HIDDEN), dtype=torch.uint8, device=dev)
+    out = {}
+
+    def timed_graph(fn, n_calls):
+        g = capture(torch, fn)
+        for _ in range(2):
+            g.replay()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record()
+        for _ in range(reps):
+            g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / 1e3 / (reps * n_calls)
+
+    # the decode step's links, grouped by kind (M = 1)
+    kinds = {}
+    for (x, K, mats), la in zip(st.links, links):
+        kinds.setdefault("+".join(m[0] for m in mats), []).append((la, sum(p.algo_bytes for _, p, _, _ in mats)))
+    rows = []
+    for name, lst in kinds.items():
+        sec = timed_graph(lambda lst=lst: run_calls(tb, [la for la, _ in lst], ws, status), len(lst))
+        byts = lst[0][1]
+        rows.append({"link": name, "count": len(lst), "us": round(sec * 1e6, 2),
+                     "GB/s": round(byts / sec / 1e9, 1), "frac": round(byts / sec / 1e9 / hbm, 4)})
+    out["decode_links_m1"] = rows
+
+    # batched decode on the 64 gate_proj matrices (5120 -> 17408; far more than L2 per pass)
+    gates = [p for n, p, _ in st.layers if n == "gate_proj"]
+    sg = st.signs[ti.HIDDEN]
+    rows = []
+    for M in (1, 2, 4, 8, 16, 32, 64):
+        x = torch.from_numpy(ti.activations(ti.config_seed(5, M), M, ti.HIDDEN)).to(dev)
+        y = torch.empty((M, ti.MLP), dtype=torch.float16, device=dev)
+
+        def fn(x=x, y=y):
+            for p in gates:
+                tb.tb_packed_linear(x, sg, 1024, p.w, p.s, p.b, y, ws, status)
+
+        sec = timed_graph(fn, len(gates))
+        byts = gates[0].algo_bytes
+        rows.append({"M": M, "us": round(sec * 1e6, 2), "frac_hbm": round(byts / sec / 1e9 / hbm, 4),
+                     "TFLOP/s": round(2 * M * ti.MLP * ti.HIDDEN / sec / 1e12, 1)})
+    out["batched_5120x17408"] = rows
+
+    # prefill on one gate_proj and one down_proj matrix, L2 flushed before every call
+    flush = torch.empty(256 << 20, dtype=torch.int8, device=dev)
+    down = next(p for n, p, _ in st.layers if n == "down_proj")
+    rows = []
+    for M in (512, 4096):
+        for p in (gates[0], down):
+            x = torch.from_numpy(ti.activations(ti.config_seed(4, p.K), M, p.K)).to(dev)
+            y = torch.empty((M, p.N), dtype=torch.float16, device=dev)
+            wsp = torch.zeros(tb.tb_packed_linear_workspace_size(M, p.K, p.N), dtype=torch.uint8, device=dev)
+            sgp = st.signs[p.K]
+            for _ in range(2):
+                tb.tb_packed_linear(x, sgp, 1024, p.w, p.s, p.b, y, wsp, status)
+            tot = 0.0
+            for _ in range(3):
+                flush.zero_()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                tb.tb_packed_linear(x, sgp, 1024, p.w, p.s, p.b, y, wsp, status)
+                b.record()
+                torch.cuda.synchronize()
+                tot += a.elapsed_time(b) / 1e3
+            sec = tot / 3
+            tfl = 2.0 * M * p.N * p.K / sec / 1e12
+            rows.append({"shape": f"M={M} {p.K}->{p.N}", "ms": round(sec * 1e3, 3), "TFLOP/s": round(tfl, 1),
+                         "frac": round(tfl / tf, 4)})
+            del x, y, wsp
+    out["prefill"] = rows
+
+    # embedding: 256 uniform ids from the 248320-row table, L2 flushed
+    T = 256
+    ids = torch.from_numpy(ti.token_ids(ti.config_seed(5, 99), T, ti.VOCAB)).to(dev)
+    e = torch.empty((T, ti.HIDDEN), dtype=torch.float16, device=dev)
+    tot = []
+    for r in range(4):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        tb.tb_embed_lookup(ids, st.emb.w, st.emb.s, st.emb.b, sg, 1024, e, status)
+        b.record()
+        torch.cuda.synchronize()
+        tot.append(a.elapsed_time(b) / 1e3)
+    sec = float(np.median(tot[1:]))
+    byts = T * (ti.HIDDEN // 4 + ti.HIDDEN // 32) + T * ti.HIDDEN * 2
+    out["embedding_256_ids"] = {"us": round(sec * 1e6, 2), "GB/s": round(byts / sec / 1e9, 1),
+                                "frac_hbm": round(byts / sec / 1e9 / hbm, 4)}
+    del flush
+    out["note"] = ("builder-side sub-results measured in this run: per-link CUDA graphs over every copy of a "
+                   "link (M = 1), batched decode over the 64 gate_proj copies, prefill and embedding with "
+                   "the L2 flushed before each call")
+    return out
+
+
+def stack_parity(st, x, y, rows: int = 256):
+    """The oracle on `rows` sampled rows of lm_head, on the input h of the last timed step (x),
+    against that step's logits (y): max and RMS error over RMS(y) (the float64 oracle runs in
+    the CPU-baseline leg only)."""
+    import oracle
+
+    _, K, mats = st.links[-1]
+    _, p, layer, _ = mats[0]
+    rng = np.random.default_rng(17)
+    sel = np.sort(rng.choice(p.N, size=rows, replace=False))
+    seed = ti.config_seed(3, layer)
+    codes = np.concatenate([ti.ternary_codes(seed, r, r + 1, K) for r in sel])
+    scales = np.concatenate([ti.group_scales(seed, r, r + 1, K // 128) for r in sel])
+    words = oracle.pack_w2(codes)
+    xf = x.cpu().numpy().astype(np.float64)
+    ref = oracle.packed_linear(xf, st.signs[K].cpu().numpy(), 1024, words, scales, oracle.biases_for(scales))
+    got = y[:, : p.N].cpu().numpy()[:, sel].astype(np.float64)
+    rms = float(np.sqrt(np.mean(ref ** 2))) or 1.0
+    err = np.abs(got - ref)
+    return {"link": "lm_head 5120->248320", "rows": rows, "max_err_over_rms_y": round(float(err.max()) / rms, 6),
+            "rms_err_over_rms_y": round(float(np.sqrt(np.mean(err ** 2))) / rms, 6)}
 
 
 def cpu_baseline_sample(budget_s: float = 12.0):
@@ -494,12 +714,18 @@ def run_sweep(args, dist, tb, tdev, torch):
         "gpu_launches": per_step * args.steps,
         "clocks": clk,
     }
+    # the last step's lm_head input and output, kept for the parity diagnostic below
+    h_last, logits_last = st.h.clone(), st.logits.clone()
+    if not args.no_sub_results:
+        line["sub_results"] = sub_results(tb, st, torch, status)
     if dist.rank == 0 and n == 1 and not args.no_cpu_baseline:
         v, desc = cpu_baseline_sample()
         line["cpu_baseline"] = {"value": round(v, 6), "unit": "tok/s",
                                 "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
                                 "sample": "float64 NumPy oracle, M=1, sampled rows of every distinct "
                                           "sweep shape, extrapolated to the 401 linears + embedding: " + desc}
+        # the same leg's oracle on sampled lm_head rows of the last step, against its logits
+        line["parity"] = stack_parity(st, h_last, logits_last)
     return line
 
 
@@ -818,19 +1044,25 @@ def run_reference(args):
 
     for _ in range(args.warmup):
         one_step()
+    w0 = time.perf_counter()
     t = [one_step() for _ in range(args.steps)]
+    wall = (time.perf_counter() - w0) / args.steps
     sec = float(np.mean(t))
     v = 1.0 / sec
     return {"impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": "tok/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sec * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic",
+            "data": "synthetic", "extrapolated": True,
             "config": {"workload": "decode step, M=1: embedding of 1 id + 401 W2-g128 linears of the "
                                    "64-layer 27B stack (float64 CPU oracle, linears extrapolated from "
-                                   "sampled rows)"},
+                                   "sampled rows)",
+                       "ms_per_step": "extrapolated: the oracle runs on sampled rows of each distinct "
+                                      "shape and its time is scaled by rows and by the shape's count; "
+                                      "the wall time of one sampled step is in sample_wall_s"},
             "cpu_baseline": {"value": round(v, 6), "unit": "tok/s", "cores": len(os.sched_getaffinity(0)),
                              "kind": "oracle",
                              "sample": f"{rows} rows of each distinct shape per step, extrapolated"},
+            "sample_wall_s": round(wall, 3),
             "e2e": {"value": round(v, 6), "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
@@ -842,6 +1074,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="sweep", choices=["sweep", "layers", "prefill", "batched", "embed", "fwht", "transcode", "all"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sub-results", action="store_true",
+                    help="skip the per-link, batched, prefill and embedding numbers of the default line")
     ap.add_argument("--profile-step", action="store_true",
                     help="build the decode stack, run two steps and exit (for an ncu launch list)")
     ap.add_argument("--path", default="calls", choices=["chain", "calls"],

@@ -167,8 +167,8 @@ size_t tb_packed_linear_algo_workspace_size(int64_t M, int64_t K, int64_t N, int
 
 /*
  * tb_packed_linear — Packed.__call__ on the non-embedding path.
- * [ARCH] "Hadamard 旋转" (if block: x = fwht(x, block, signs); then
- * quantized_matmul(x, weight, scales, biases, transpose=True, group_size=128, bits=2))
+ * [ARCH] "Hadamard 旋转" (a folded module rotates its input, then multiplies it by the
+ * transposed 2-bit, group-128 affine matrix)
  * and [PACK] "文本模型加载" (packed weights consumed directly, never expanded).
  *   y[m, n] = sum_k x'[m, k] * (s[n, k/128] * q[n, k] + b[n, k/128]),
  *   x' = fwht(x, block, signs) rounded to fp16 (x' = x when block = 0);
@@ -266,6 +266,19 @@ int tb_chain_plan(const tb_chain_link* links, int n_links, int64_t M, void* plan
 size_t tb_chain_workspace_size(void);
 
 /*
+ * tb_chain_set_wait — the bound of a plan's waits on the previous link.
+ * Before its prologue, every CTA waits until all CTAs have counted the previous link complete;
+ * that wait gives up after wait_ns nanoseconds (0 = the library default, 2 s), sets
+ * TB_DEV_TIMEOUT and lets the run wind down (its outputs are then not valid; zero the
+ * workspace's counters before the next run).  extra_count raises the count each link waits for
+ * by that many, so that the wait cannot complete: it exists to test the timeout path without a
+ * fault or a hang, and must be 0 for a run whose results are used.  Writes the two fields of the
+ * plan on `stream` and waits for that copy.  Errors: TB_ERR_NULL, TB_ERR_ALIGN, TB_ERR_VALUE
+ * (a negative value), TB_ERR_CUDA.  A new plan starts with wait_ns = 0 and extra_count = 0.
+ */
+int tb_chain_set_wait(void* plan, int64_t wait_ns, int32_t extra_count, void* stream);
+
+/*
  * tb_chain_run — run a plan: one launch on `stream`, asynchronous.  n_links, M and max_K
  * (the largest K of the links) must be the values the plan was made with; a mismatch that
  * the device can see sets TB_DEV_BAD_PLAN and computes nothing.  Runs that share one
@@ -279,7 +292,7 @@ int tb_chain_run(const void* plan, int n_links, int64_t M, int64_t max_K, void* 
 
 /*
  * tb_embed_lookup — Packed.__call__ on the embedding path.
- * [ARCH] "Hadamard 旋转" (return fwht(out, block, signs, inverse=True)) and
+ * [ARCH] "Hadamard 旋转" (the looked-up rows are dequantised, then inverse-transformed) and
  * [PACK] "文本模型加载" (mx.dequantize of the looked-up rows, then the inverse transform).
  *   out[t, :] = signs * ((H/32) e) per block,  e = s*q + b of row ids[t] of the table.
  *   ids int32 [T]; w uint32 [V, D/16]; scales fp16 [V, D/128]; biases the same or NULL

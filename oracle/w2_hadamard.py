@@ -164,8 +164,8 @@ def decode_w2(words, scales, biases, K: int) -> np.ndarray:
 def packed_linear(x, signs, block: int, words, scales, biases) -> np.ndarray:
     """Non-embedding path: y = fwht(x, block, signs) @ W^T, float64.
 
-    [ARCH] "Hadamard 旋转" (``if self.block: x = fwht(x, ...)``, then
-    ``quantized_matmul(..., transpose=True, group_size=128, bits=2)``) and
+    [ARCH] "Hadamard 旋转" (a folded module rotates its input first, then
+    multiplies by the transposed 2-bit, group-128 affine matrix) and
     [PACK] "文本模型加载" (non-embedding path).  x: [M, K]; words [N, K/16];
     scales, biases [N, K/128] (biases None: scale-only, b = -s); returns [M, N].
     """
@@ -191,8 +191,8 @@ def abs_product_sum(x, signs, block: int, words, scales, biases) -> np.ndarray:
 def embed_lookup(ids, words, scales, biases, signs, block: int) -> np.ndarray:
     """Embedding path: dequantise the looked-up rows, then the inverse fwht.
 
-    [ARCH] "Hadamard 旋转" (``return fwht(out, block, signs, inverse=True)``)
-    and [PACK] "文本模型加载" (``mx.dequantize`` of the looked-up rows, then
+    [ARCH] "Hadamard 旋转" (the embedding path ends with the inverse
+    transform of the dequantised rows) and [PACK] "文本模型加载" (``mx.dequantize`` of the looked-up rows, then
     the inverse Hadamard transform).  ids: [T]; returns [T, D] float64.
     Raises on an id outside [0, V).
     """

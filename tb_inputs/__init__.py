@@ -104,6 +104,20 @@ def group_scales(seed: int, n0: int, n1: int, G: int) -> np.ndarray:
     return f.astype(np.float16)
 
 
+def raw_words(seed: int, N: int, K: int) -> np.ndarray:
+    """Uniformly random uint32 words [N, K/16]: every 2-bit field equally likely to hold
+    0, 1, 2 or 3.  Inputs for the general affine container (a field of 3, which the
+    packer never writes, included); no packing is done here, the bits are drawn as words."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    return rng.integers(0, 1 << 32, size=(N, K // 16), dtype=np.uint64).astype(np.uint32)
+
+
+def free_biases(seed: int, N: int, G: int) -> np.ndarray:
+    """fp16 biases ~ U[-0.03, 0.01] [N, G], drawn independently of any scale (so b != -s)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    return (rng.random((N, G)) * 0.04 - 0.03).astype(np.float16)
+
+
 def activations(seed: int, M: int, K: int) -> np.ndarray:
     """x ~ N(0,1) rounded to fp16, shape [M, K]."""
     rng = np.random.Generator(np.random.PCG64(seed))

@@ -66,6 +66,7 @@ _SIGNATURES = {
     "tb_chain_plan_size": (_SZ, [_INT]),
     "tb_chain_workspace_size": (_SZ, []),
     "tb_chain_plan": (_INT, [_P, _INT, _I64, _P, _SZ, _P]),
+    "tb_chain_set_wait": (_INT, [_P, _I64, ctypes.c_int32, _P]),
     "tb_chain_run": (_INT, [_P, _INT, _I64, _I64, _P, _SZ, _P, _P]),
     "tb_transcode_gguf": (_INT, [_P, _INT, _I64, _I64, _P, _P, _P, _P, _P]),
 }
@@ -252,6 +253,13 @@ def tb_chain_plan(links, M, plan, stream=None):
     nbytes = plan.numel() * plan.element_size()
     _check("tb_chain_plan", load().tb_chain_plan(ctypes.cast(arr, ctypes.c_void_p), n, M, _ptr(plan), nbytes,
                                                  _stream(stream)))
+
+
+def tb_chain_set_wait(plan, wait_ns, extra_count=0, stream=None):
+    """Bound of the plan's waits on the previous link (ns, 0 = default); extra_count > 0 only to
+    test the timeout path (the awaited count can then not be reached)."""
+    _check("tb_chain_set_wait", load().tb_chain_set_wait(_ptr(plan), int(wait_ns), int(extra_count),
+                                                         _stream(stream)))
 
 
 def tb_chain_run(plan, n_links, M, max_K, workspace, dev_status=None, stream=None):

@@ -1,7 +1,7 @@
 // Chained decode: a sequence of Packed linears (M <= 8 tokens) in one persistent launch.
 //
 // [ARCH] kwkr.cn/news/564617, section "Hadamard 旋转把量化误差抹平的免费午餐": every linear of
-// the stack is Packed.__call__ = fwht(x, block, signs) followed by the W2-g128 matmul; a decode
+// the stack is the module's forward pass (rotate the input, then the W2-g128 matmul); a decode
 // step runs them one after another, each reading what the ones before it wrote.  [PACK]
 // lpnh.cn/news/2438023, section "文本模型加载artifact.load_model 与 Packed 模块": the modules
 // and their packed tensors.
@@ -25,6 +25,7 @@
 // The plan (tb_chain_plan) holds, in device memory written once by the host: a header, one
 // CUtensorMap per matrix (the TMA descriptor of its codes, read by the copies straight from
 // global memory) and one ChainLink per link.
+#include <cstddef>
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <string.h>
@@ -62,7 +63,10 @@ struct ChainHeader {
   uint32_t magic;
   int32_t n_links, M, max_K;
   int64_t maps_off, links_off, bytes;
-  int64_t pad[3];
+  int64_t wait_ns;      // limit of each wait on the previous link, ns of %globaltimer (0: TB_WAIT_NS)
+  int32_t extra_count;  // added to the count each link waits for (0; > 0 only to test the timeout)
+  int32_t pad0;
+  int64_t pad1;
 };
 static_assert(sizeof(ChainHeader) == 64, "header size");
 
@@ -329,11 +333,12 @@ __global__ void __launch_bounds__(kChainThreads, 1) w2_gemv_chain_kernel(const _
     // counted that link complete
     if (li > 0) {
       if (threadIdx.x == 0 && !aborted) {
-        const uint32_t target = (uint32_t)li * gridDim.x;
+        const uint32_t target = (uint32_t)li * gridDim.x + (uint32_t)hdr->extra_count;
+        const uint64_t limit = hdr->wait_ns > 0 ? (uint64_t)hdr->wait_ns : TB_WAIT_NS;
         if (ld_acquire_gpu(a.sync) < target) {
           const uint64_t t_0 = globaltimer_ns();
           while (ld_acquire_gpu(a.sync) < target) {
-            if (globaltimer_ns() - t_0 > TB_WAIT_NS) {
+            if (globaltimer_ns() - t_0 > limit) {
               aborted = 1;
               set_status(a.status, TB_DEV_TIMEOUT);
               break;
@@ -664,6 +669,26 @@ extern "C" int tb_chain_plan(const tb_chain_link* links, int n_links, int64_t M,
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaMemcpyAsync(plan, host.data(), need, cudaMemcpyHostToDevice, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);  // the host image is freed on return
+  if (e != cudaSuccess) {
+    record_cuda_error(e);
+    return TB_ERR_CUDA;
+  }
+  return TB_OK;
+}
+
+extern "C" int tb_chain_set_wait(void* plan, int64_t wait_ns, int32_t extra_count, void* stream) {
+  if (!plan) return TB_ERR_NULL;
+  if (reinterpret_cast<uintptr_t>(plan) & 127u) return TB_ERR_ALIGN;
+  if (wait_ns < 0 || extra_count < 0) return TB_ERR_VALUE;
+  struct {
+    int64_t wait_ns;
+    int32_t extra_count;
+  } f = {wait_ns, extra_count};
+  static_assert(offsetof(ChainHeader, extra_count) == offsetof(ChainHeader, wait_ns) + 8, "header fields");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(static_cast<uint8_t*>(plan) + offsetof(ChainHeader, wait_ns), &f, 12,
+                                  cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);  // `f` lives on this stack frame
   if (e != cudaSuccess) {
     record_cuda_error(e);
     return TB_ERR_CUDA;

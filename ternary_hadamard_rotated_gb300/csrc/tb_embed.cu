@@ -1,7 +1,8 @@
 // Embedding path of the Packed layer: gather a packed row, dequantise, inverse FWHT.
 //
 // [ARCH] kwkr.cn/news/564617, section "Hadamard 旋转把量化误差抹平的免费午餐":
-//   if self.embedding: ... return fwht(out, self.block, self.signs, inverse=True)
+//   an embedding module looks its rows up, dequantises them and returns the inverse
+//   transform of the result (the Hadamard transform first, the signs last).
 // [PACK] lpnh.cn/news/2438023, section "文本模型加载artifact.load_model 与 Packed 模块":
 //   embed_tokens rows are restored with mx.dequantize, then the inverse Hadamard
 //   transform is applied (transform first, signs last).

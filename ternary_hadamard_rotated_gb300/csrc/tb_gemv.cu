@@ -1,9 +1,9 @@
 // Decode path of the Packed layer: fused sign*FWHT prologue + W2-g128 GEMV.
 //
 // [ARCH] kwkr.cn/news/564617, section "Hadamard 旋转把量化误差抹平的免费午餐":
-//   if self.block: x = fwht(x, block, signs); y = quantized_matmul(x, weight, scales,
-//   biases, transpose=True, group_size=128, bits=2) -- the packed 2-bit words are
-//   consumed directly and never expanded to fp16.
+//   a folded module first rotates its input (sign flip, then the normalised block Hadamard
+//   transform) and then multiplies it by the 2-bit, group-128 affine weights, which stay
+//   packed: they are consumed as words and never expanded to an fp16 matrix.
 // [PACK] lpnh.cn/news/2438023, section "文本模型加载artifact.load_model 与 Packed 模块".
 //
 // Design (one GB300 SM = one persistent CTA of 8 warps):

@@ -2,8 +2,9 @@
 // the per-call kernel (tb_gemv_tma.cu) and the chained persistent kernel (tb_chain.cu).
 //
 // [ARCH] kwkr.cn/news/564617, section "Hadamard 旋转把量化误差抹平的免费午餐": the layer is
-// x' = fwht(x, block, signs) followed by quantized_matmul with the packed 2-bit codes, fp16
-// scales and biases (group 128), consumed directly and never expanded to a dense matrix.
+// the rotated input (signs, then the block Hadamard transform) times the packed 2-bit codes
+// with their fp16 scales and biases (group 128), consumed directly and never expanded to a
+// dense matrix.
 //
 // Work unit: 128 output rows x 512 k (4 groups of 128) = one 16 KB TMA box of packed codes
 // (128 rows x 128 B, 128-byte swizzle).  Arithmetic per group of 128 and token: LOP3 puts each

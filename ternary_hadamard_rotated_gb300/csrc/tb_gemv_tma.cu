@@ -1,9 +1,9 @@
 // Decode path of the Packed layer, TMA-streamed: fused sign*FWHT prologue + W2-g128 GEMV.
 //
 // [ARCH] kwkr.cn/news/564617, section "Hadamard 旋转把量化误差抹平的免费午餐":
-//   if self.block: x = fwht(x, block, signs); y = quantized_matmul(x, weight, scales,
-//   biases, transpose=True, group_size=128, bits=2): the packed 2-bit words are consumed
-//   directly and never expanded to fp16.
+//   a folded module rotates its input by the signed block Hadamard transform, then multiplies
+//   it by the packed 2-bit, group-128 affine weights; the words are consumed as they are and
+//   never expanded to an fp16 matrix.
 // [PACK] lpnh.cn/news/2438023, section "文本模型加载artifact.load_model 与 Packed 模块".
 //
 // Work unit: 128 output rows x 512 k (4 groups of 128) = one 16 KB TMA box of packed codes

@@ -2,9 +2,9 @@
 // streaming GEMV (decode, M <= 8 tokens) and the tensor-core GEMM (prefill).
 //
 // [ARCH] kwkr.cn/news/564617, section "Hadamard 旋转把量化误差抹平的免费午餐":
-//   Packed.__call__: if self.block: x = fwht(x, self.block, self.signs), then
-//   mx.quantized_matmul(x, self.weight, self.scales, self.biases, transpose=True,
-//   group_size=128, bits=2).
+//   the module's forward pass rotates the input (signs, then the normalised block Hadamard
+//   transform) when the module is folded, and then multiplies the result by the transposed
+//   2-bit, group-128 affine weight matrix with its scales and biases.
 #include <cuda_runtime.h>
 
 #include "tb_common.cuh"

@@ -9,6 +9,7 @@
 // several SMs) kept in a fixed array compiled into this library instead of a caller's
 // workspace.  Every GPU that loads the library holds that array (about 2 MiB) until the
 // process exits.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -36,27 +37,57 @@ static __device__ __align__(256) unsigned char g_tb_gemv_scratch[tb::kStaticScra
 
 namespace tb {
 
-// Device address of g_tb_gemv_scratch on the current device, looked up once per device.
+// The driver's cuCtxGetCurrent, resolved once through the runtime (the library does not link
+// libcuda itself); null if the driver does not offer it.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+static CtxGetCurrentFn ctx_get_current() {
+  static CtxGetCurrentFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(p);
+  });
+  return fn;
+}
+
+// Device address of g_tb_gemv_scratch on the current device.  It is looked up once per device
+// and context: a context created after a reset (cudaDeviceReset, or the primary context torn
+// down and made again) loads the module anew, so the address is looked up again when the
+// current context is not the one it was found under.  (Without the driver's cuCtxGetCurrent
+// it is looked up on every call.)
 static int static_scratch(void** out) {
   static std::mutex mu;
   static void* addr[64] = {nullptr};
+  static CUcontext under[64] = {nullptr};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess || dev < 0 || dev >= 64) {
     if (e != cudaSuccess) record_cuda_error(e);
     return TB_ERR_CUDA;
   }
+  CtxGetCurrentFn get = ctx_get_current();
+  CUcontext ctx = nullptr;
+  if (get && get(&ctx) != CUDA_SUCCESS) ctx = nullptr;
   std::lock_guard<std::mutex> lock(mu);
-  if (!addr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_tb_gemv_scratch);
-    if (e != cudaSuccess || !p) {
-      if (e != cudaSuccess) record_cuda_error(e);
-      return TB_ERR_CUDA;
-    }
-    addr[dev] = p;
+  if (ctx && addr[dev] && under[dev] == ctx) {
+    *out = addr[dev];
+    return TB_OK;
   }
-  *out = addr[dev];
+  void* p = nullptr;
+  e = cudaGetSymbolAddress(&p, g_tb_gemv_scratch);  // binds the device's context if none is
+  if (e != cudaSuccess || !p) {
+    if (e != cudaSuccess) record_cuda_error(e);
+    return TB_ERR_CUDA;
+  }
+  if (get && get(&ctx) == CUDA_SUCCESS && ctx) {
+    addr[dev] = p;
+    under[dev] = ctx;
+  }
+  *out = p;
   return TB_OK;
 }
 

@@ -166,13 +166,73 @@ def test_chain_host_refusals(tb):
     assert e.value.status == tb.TB_ERR_TOO_LARGE
 
 
-def test_decode_stack_chain_sampled(tb):
-    """The bench's decode step at full size (257 links, 7.06 GB of weights, one chain launch):
-    sampled rows of sampled links against the oracle, on the inputs those links read."""
+@pytest.fixture(scope="module")
+def stack(tb):
+    """The bench's synthetic 64-layer stack (257 links, 7.06 GB of packed weights)."""
     import bench
     from tb_inputs import device as tdev
 
-    st = bench.Stack(tb, tdev, torch)
+    return bench.Stack(tb, tdev, torch)
+
+
+def check_stack_link(st, li, rng, what, rows_per_matrix=96):
+    """Sampled rows of every matrix of link li against the oracle, on the input the link read
+    (still in its buffer); the rows' codes and scales are regenerated on the host."""
+    x, K, mats = st.links[li]
+    xs = x.cpu().numpy()
+    assert np.isfinite(xs).all(), f"{what}: non-finite input of link {li}"
+    sg = st.signs[K].cpu().numpy()
+    xf = xs.astype(np.float64)
+    for name, p, layer, y in mats:
+        rows = np.sort(rng.choice(p.N, size=min(p.N, rows_per_matrix), replace=False))
+        seed = ti.config_seed(3, layer)
+        codes = np.concatenate([ti.ternary_codes(seed, r, r + 1, K) for r in rows])
+        scales = np.concatenate([ti.group_scales(seed, r, r + 1, K // 128) for r in rows])
+        words = oracle.pack_w2(codes)
+        biases = oracle.biases_for(scales)
+        ref = oracle.packed_linear(xf, sg, 1024, words, scales, biases)
+        bound = 2e-3 * oracle.abs_product_sum(xf, sg, 1024, words, scales, biases) + 1e-5
+        got = y[:, : p.N].cpu().numpy()[:, rows]
+        assert_linear_close(got, ref, bound, f"{what} link {li} {name}")
+
+
+def test_decode_stack_calls_sampled(tb, stack):
+    """The bench's timed path at full size: the 257 links as one tb_packed_linear(_multi) call
+    each, in order.  Checked on sampled rows: the last in_proj_qkv + in_proj_z link (one call
+    over 10240 + 6144 rows) right after it ran, then, after the rest of the step, lm_head
+    (5120 -> 248320 in one call: 1940 row tiles, the longest split schedule) and the last
+    down_proj."""
+    import bench
+
+    st = stack
+    links = st.link_args()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = torch.zeros(tb.tb_packed_linear_workspace_size(1, ti.MLP, ti.HIDDEN), dtype=torch.uint8,
+                     device="cuda")
+    for b in (st.h, st.qkv, st.z, st.q, st.k, st.v, st.gate, st.up, st.logits):
+        b.fill_(float("nan"))
+    j = max(i for i, (_, _, mats) in enumerate(st.links) if mats[0][0] == "in_proj_qkv")
+    assert [m[0] for m in st.links[j][2]] == ["in_proj_qkv", "in_proj_z"]
+    bench.run_calls(tb, links[: j + 1], ws, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    rng = np.random.default_rng(5)
+    check_stack_link(st, j, rng, "calls")
+    bench.run_calls(tb, links[j + 1:], ws, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert bool(torch.isfinite(st.logits).all())
+    n = len(st.links)
+    assert st.links[n - 1][2][0][0] == "lm_head"
+    for li in (n - 1, n - 2):
+        check_stack_link(st, li, rng, "calls", rows_per_matrix=256 if li == n - 1 else 96)
+    assert int(ws[:1024].count_nonzero().item()) == 0
+
+
+def test_decode_stack_chain_sampled(tb, stack):
+    """The bench's decode step at full size (257 links, 7.06 GB of weights, one chain launch):
+    sampled rows of sampled links against the oracle, on the inputs those links read."""
+    st = stack
     links = st.link_args()
     chain = tb.Chain(links, 1)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
@@ -185,21 +245,42 @@ def test_decode_stack_chain_sampled(tb):
     # lm_head (reads h, writes the logits) and the last down_proj (reads the gate output,
     # writes h): links whose input and output are both still in their buffers after the run
     rng = np.random.default_rng(3)
-    sg = {K: v.cpu().numpy() for K, v in st.signs.items()}
     for li in (len(st.links) - 1, len(st.links) - 2):
-        x, K, mats = st.links[li]
-        xs = x.cpu().numpy()
-        assert np.isfinite(xs).all()
-        for name, p, layer, y in mats:
-            rows = np.sort(rng.choice(p.N, size=min(p.N, 96), replace=False))
-            seed = ti.config_seed(3, layer)
-            codes = np.concatenate([ti.ternary_codes(seed, r, r + 1, K) for r in rows])
-            scales = np.concatenate([ti.group_scales(seed, r, r + 1, K // 128) for r in rows])
-            words = oracle.pack_w2(codes)
-            biases = oracle.biases_for(scales)
-            xf = xs.astype(np.float64)
-            ref = oracle.packed_linear(xf, sg[K], 1024, words, scales, biases)
-            bound = 2e-3 * oracle.abs_product_sum(xf, sg[K], 1024, words, scales, biases) + 1e-5
-            got = y[:, : p.N].cpu().numpy()[:, rows]
-            assert_linear_close(got, ref, bound, f"stack link {li} {name}")
+        check_stack_link(st, li, rng, "chain")
+    assert int(chain.workspace[:1280].count_nonzero().item()) == 0
+
+
+def test_chain_wait_timeout_winds_down(tb):
+    """The bounded wait on the previous link: with the awaited count raised past what the CTAs
+    can reach, every CTA gives up after the plan's limit (1 ms), the run reports TB_DEV_TIMEOUT
+    and ends (no hang, no fault); the same plan with the count restored runs correctly."""
+    import time
+
+    M = 1
+    spec = SPEC[:4]
+    c = SmallChain(tb, spec, M, seed=490)
+    chain = tb.Chain(c.args, M)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    tb.tb_chain_set_wait(chain.plan, 1_000_000, 1)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    chain.run(st)
+    torch.cuda.synchronize()
+    took = time.perf_counter() - t0
+    assert int(st.item()) & tb.TB_DEV_TIMEOUT
+    assert took < 10.0, took  # one 1 ms limit per CTA, far below the default 2 s per wait
+    with pytest.raises(tb.TBError) as e:
+        tb.tb_chain_set_wait(chain.plan, -1, 0)
+    assert e.value.status == tb.TB_ERR_VALUE
+    # after a timed-out run the workspace's counters are zeroed again, as the header asks
+    chain.workspace.zero_()
+    tb.tb_chain_set_wait(chain.plan, 0, 0)
+    for v in c.bufs.values():
+        if v is not c.bufs["x0"]:
+            v.fill_(float("nan"))
+    st.zero_()
+    chain.run(st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    c.check("after a timed-out run")
     assert int(chain.workspace[:1280].count_nonzero().item()) == 0

@@ -281,6 +281,49 @@ def test_packed_linear_brute_force():
     np.testing.assert_allclose(oracle.packed_linear(x, signs, block, w, s, None), y0, rtol=1e-12, atol=1e-12)
 
 
+def test_abs_product_sum_brute_force():
+    # the scale of every linear tolerance, sum_k |x'_k| * |s q + b|, by explicit loops on the
+    # tiny configuration's block: x' from the Sylvester matrix (not the butterfly), each weight
+    # read bit by bit off its word, a stored bias that is not -s and a field holding 3
+    M, K, N, block = 2, 1024, 3, 1024
+    x = ti.activations(0, M, K)
+    signs = ti.rademacher_signs(0, K)
+    w = ti.raw_words(17, N, K)
+    w[0, 0] = 0xFFFFFFFF  # sixteen fields of 3
+    s = ti.group_scales(17, 0, N, K // 128)
+    b = ti.free_biases(17, N, K // 128)
+    assert (b.astype(np.float64) != -s.astype(np.float64)).all()
+    H = sylvester(block)
+    want = np.zeros((M, N))
+    want0 = np.zeros((M, N))
+    xr = np.zeros((M, K))
+    for m in range(M):
+        seg = x[m].astype(np.float64) * signs
+        xr[m] = (H @ seg) / 32.0
+        for n in range(N):
+            acc = acc0 = 0.0
+            for k in range(K):
+                q = _bits_of_word(w[n, k // 16])[k % 16]
+                sc, bi = float(s[n, k // 128]), float(b[n, k // 128])
+                acc += abs(xr[m, k]) * abs(sc * q + bi)
+                acc0 += abs(xr[m, k]) * abs(sc * (q - 1))
+            want[m, n] = acc
+            want0[m, n] = acc0
+    got = oracle.abs_product_sum(x, signs, block, w, s, b)
+    np.testing.assert_allclose(got, want, rtol=1e-12, atol=0)
+    np.testing.assert_allclose(oracle.abs_product_sum(x, signs, block, w, s, None), want0, rtol=1e-12)
+    # the slips this pin exists for would each move the sum well away from the loops' value
+    Wabs = np.abs(oracle.decode_w2(w, s, b, K))
+    slips = {
+        "|x| for |x'|": np.abs(x.astype(np.float64)) @ Wabs.T,
+        "|s| dropped": np.abs(xr) @ np.abs(oracle.decode_w2(w, np.ones_like(s), b, K)).T,
+        "bias dropped": np.abs(xr) @ np.abs(oracle.decode_w2(w, s, np.zeros_like(b), K)).T,
+        "|x' w| summed signed": np.abs(xr @ oracle.decode_w2(w, s, b, K).T),
+    }
+    for what, v in slips.items():
+        assert np.abs(v - want).max() > 1e-3 * np.abs(want).max(), what
+
+
 def test_group_sum_identity():
     # y = sum_g s_g * sum_{k in g} q_k x'_k + b_g * sum_{k in g} x'_k
     M, K, N = 3, 2048, 17

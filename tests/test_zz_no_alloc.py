@@ -4,8 +4,9 @@ tb_packed_linear_gemv_noalloc serves callers that cannot allocate device memory 
 under CUDA graph capture, plugins inside a runtime that owns all device memory, services
 with a fixed memory budget).  Its split-schedule state lives in a fixed array inside the
 library; this test calls it twice in a row through the C ABI and checks both results
-against tb_packed_linear's on the same inputs, within the linear-path tolerance.
-The file is named to run last, so a failure here leaves every other result in place.
+against tb_packed_linear's on the same inputs and against the float64 oracle, each within
+the linear-path tolerance.  The file is named to run last, so a failure here leaves every
+other result in place.
 """
 import numpy as np
 import pytest
@@ -29,12 +30,28 @@ def tb():
     return tbm
 
 
-@pytest.mark.parametrize("M,K,N", [(1, 17408, 5120), (3, 5120, 1000), (1, 2048, 77)])
-def test_noalloc_gemv_matches_regular_entry(tb, M, K, N):
+class _AffineLayer:
+    """Random words (every 2-bit field 0..3) and biases drawn apart from the scales."""
+
+    def __init__(self, seed, N, K):
+        self.words = ti.raw_words(seed, N, K)
+        self.scales = ti.group_scales(seed, 0, N, K // 128)
+        self.biases = ti.free_biases(seed, N, K // 128)
+
+
+@pytest.mark.parametrize("M,K,N,affine", [(1, 17408, 5120, False), (3, 5120, 1000, False),
+                                          (1, 2048, 77, False), (2, 5120, 300, True)])
+def test_noalloc_gemv_matches_regular_entry(tb, M, K, N, affine):
     x = ti.activations(90 + M, M, K)
     sg = ti.rademacher_signs(90, K)
-    L = HostLayer(90, N, K)
-    w, s, b = device_layer(90, N, K, from_host=L)
+    if affine:
+        L = _AffineLayer(91, N, K)
+        w = torch.from_numpy(L.words.view(np.int32)).cuda()
+        s = torch.from_numpy(L.scales).cuda()
+        b = torch.from_numpy(L.biases).cuda()
+    else:
+        L = HostLayer(90, N, K)
+        w, s, b = device_layer(90, N, K, from_host=L)
     xd = torch.from_numpy(x).cuda()
     sd = torch.from_numpy(sg).cuda()
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
@@ -49,12 +66,16 @@ def test_noalloc_gemv_matches_regular_entry(tb, M, K, N):
         outs.append(y)
     torch.cuda.synchronize()
     assert int(st.item()) == 0
-    ref = y_reg.cpu().numpy().astype(np.float64)
-    bound = LIN_REL * oracle.abs_product_sum(x.astype(np.float64), sg, 1024, L.words, L.scales,
-                                             L.biases) + LIN_ABS
+    xf = x.astype(np.float64)
+    bound = LIN_REL * oracle.abs_product_sum(xf, sg, 1024, L.words, L.scales, L.biases) + LIN_ABS
+    y_or = oracle.packed_linear(xf, sg, 1024, L.words, L.scales, L.biases)
+    y_rg = y_reg.cpu().numpy().astype(np.float64)
+    assert (np.abs(y_rg - y_or) <= bound).all()
     for y in outs:
-        err = np.abs(y.cpu().numpy().astype(np.float64) - ref)
-        assert (err <= bound).all(), float(err.max())
+        yn = y.cpu().numpy().astype(np.float64)
+        for ref, what in ((y_rg, "regular entry"), (y_or, "oracle")):
+            err = np.abs(yn - ref)
+            assert (err <= bound).all(), (what, float(err.max()))
 
 
 def test_noalloc_gemv_scale_only(tb):
