@@ -33,12 +33,11 @@ METRIC = "decode tok/s at 27B shapes (M=1) + fused W2 GEMV HBM GB/s as % of GB30
 # DRAM bytes (read + write) of one chain launch from an ncu capture, or None until taken
 CHAIN_TRAFFIC = None
 # DRAM bytes per launch of the per-call decode GEMV over its algorithmic bytes, from an ncu
-# capture (dram__bytes_read.sum + dram__bytes_write.sum) of the kernel as it is now, or None.
-# The last capture (25.18 MB read, 0 written, 25.07 MB algorithmic for 5120 -> 17408;
-# profiles/w2_gemv_tma_lm_head.md) predates the two-warp prologue transform, so it is not used.
-GEMV_TRAFFIC_RATIO = None
-GEMV_TRAFFIC_NOTE = ("not captured for the kernel as it is now (the last capture, 1.004x the algorithmic "
-                     "bytes, predates the two-warp prologue transform)")
+# capture (dram__bytes_read.sum + dram__bytes_write.sum) of the kernel as it is now:
+# 25,166,080 B read, 0 written, for 25,067,520 B of 5120 -> 17408 weights
+# (profiles/w2_gemv_tma_5120x17408_traffic.md).
+GEMV_TRAFFIC_RATIO = 25166080 / 25067520
+GEMV_TRAFFIC_NOTE = "not captured"
 CHAIN_TRAFFIC_NOTE = "not captured yet for this kernel"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
@@ -785,6 +784,22 @@ def profile_linear(args, dist, tb, tdev, torch):
     return {"profile_linear": [K, N, M, algo], "status": int(status.item())}
 
 
+def profile_embed(args, dist, tb, tdev, torch):
+    """Four tb_embed_lookup calls of 256 uniform ids on the 248320 x 5120 table, nothing timed."""
+    dev = torch.device("cuda")
+    tmp = torch.empty(1 << 30, dtype=torch.int8, device=dev)
+    p = Packed(tb, tdev, torch, ti.config_seed(5, 99), ti.VOCAB, ti.HIDDEN, tmp)
+    del tmp
+    sg = torch.from_numpy(ti.rademacher_signs(5, ti.HIDDEN)).to(dev)
+    ids = torch.from_numpy(ti.token_ids(ti.config_seed(5, 99), 256, ti.VOCAB)).to(dev)
+    out = torch.empty((256, ti.HIDDEN), dtype=torch.float16, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    for _ in range(4):
+        tb.tb_embed_lookup(ids, p.w, p.s, p.b, sg, 1024, out, status)
+    torch.cuda.synchronize()
+    return {"profile_embed": 256, "status": int(status.item())}
+
+
 def run_layers(args, dist, tb, tdev, torch):
     """Per-shape decode GEMV at the 27B layer shapes (M = 1)."""
     hbm, _, _, peak_kind = peaks()
@@ -1084,6 +1099,8 @@ def main():
                     help="with --profile-step: one launch per link instead of the chain launch")
     ap.add_argument("--profile-fwht", type=int, nargs=2, metavar=("M", "K"),
                     help="four tb_fwht calls on M x K activations (for ncu)")
+    ap.add_argument("--profile-embed", action="store_true",
+                    help="four embedding lookups of 256 ids on the 248320 x 5120 table (for ncu)")
     ap.add_argument("--profile-linear", type=int, nargs=4, metavar=("K", "N", "M", "ALGO"),
                     help="one packed K->N matrix, four tb_packed_linear calls on M tokens (for ncu)")
     args = ap.parse_args()
@@ -1113,10 +1130,12 @@ def main():
         configs = ["profile_linear"]
     if args.profile_fwht:
         configs = ["profile_fwht"]
+    if args.profile_embed:
+        configs = ["profile_embed"]
     for c in configs:
         fn = {"sweep": run_sweep, "layers": run_layers, "prefill": run_prefill, "batched": run_batched,
               "embed": run_embed, "fwht": run_fwht, "transcode": run_transcode, "profile": profile_step,
-              "profile_linear": profile_linear,
+              "profile_linear": profile_linear, "profile_embed": profile_embed,
               "profile_fwht": profile_fwht}[c]
         line = fn(args, dist, tb, tdev, torch)
         if rank == 0:
