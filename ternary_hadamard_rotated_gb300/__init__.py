@@ -36,6 +36,8 @@ TB_DEV_BAD_PLAN = 8
 TB_ALGO_AUTO = 0
 TB_ALGO_GEMV = 1
 TB_ALGO_TC = 2
+TB_ALGO_GEMV_SYNC = 3
+TB_ALGO_GEMV_TMEM = 4
 
 TB_FMT_PQ2_0 = 1
 TB_FMT_PTQ1_0 = 2

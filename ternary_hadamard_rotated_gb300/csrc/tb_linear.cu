@@ -33,6 +33,10 @@ int launch_rotate_pairorder(const __half* x, __half* out, const int8_t* signs, i
 int launch_gemm_tc_rotated(const __half* xp, int64_t M, int64_t K, const uint32_t* w,
                            const __half* scales, const __half* biases, int64_t N, __half* y,
                            void* gws, int32_t* status, cudaStream_t s);
+int launch_gemv_f8_multi(const __half* x, int64_t M, int64_t K, const int8_t* signs, int block,
+                         int nmat, const uint32_t* const* w, const __half* const* scales,
+                         const __half* const* biases, const int64_t* N, __half* const* y,
+                         void* workspace, size_t ws_bytes, int32_t* status, cudaStream_t s);
 constexpr int kMaxMulti = 4;
 
 // Workspace layout: [fixup region of the GEMV split schedule (zero before the first call,
@@ -52,6 +56,28 @@ constexpr int64_t kGemvMaxTokens = 8;
 static int resolve_algo(int64_t M, int algo) {
   if (algo == TB_ALGO_AUTO) return M <= kGemvMaxTokens ? TB_ALGO_GEMV : TB_ALGO_TC;
   return algo;
+}
+
+// The streaming GEMV (decode): the tensor-memory kernel where it applies (M <= 2, K a multiple
+// of 1024) unless the warp-level one is asked for, else the warp-level TMA kernel, else (K not a
+// multiple of 1024) the row-streaming one.  `which` is TB_ALGO_GEMV, _GEMV_SYNC or _GEMV_TMEM.
+static int launch_streaming_gemv(int which, const __half* x, int64_t M, int64_t K, const int8_t* sg,
+                                 int block, int n, const uint32_t* const* w, const __half* const* sh,
+                                 const __half* const* bh, const int64_t* N, __half* const* yh,
+                                 void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                 cudaStream_t s) {
+  if (which != TB_ALGO_GEMV_SYNC && K % kBlock == 0) {
+    const int rc = launch_gemv_f8_multi(x, M, K, sg, block, n, w, sh, bh, N, yh, workspace,
+                                        workspace_bytes, dev_status, s);
+    if (rc != TB_ERR_UNSUPPORTED || which == TB_ALGO_GEMV_TMEM) return rc;
+  } else if (which == TB_ALGO_GEMV_TMEM) {
+    return TB_ERR_UNSUPPORTED;
+  }
+  if (K % kBlock == 0)  // TMA-streamed GEMV; without a workspace its ranges stay on tile bounds
+    return launch_gemv_tma_multi(x, M, K, sg, block, n, w, sh, bh, N, yh, workspace, workspace_bytes,
+                                 dev_status, s);
+  if (n != 1) return TB_ERR_SHAPE;
+  return launch_gemv(x, M, K, sg, block, w[0], sh[0], bh[0], N[0], yh[0], dev_status, s);
 }
 
 static int check_linear_shape(int64_t M, int64_t K, int block, int64_t N) {
@@ -98,7 +124,7 @@ extern "C" int tb_packed_linear_algo(const uint16_t* x, int64_t M, int64_t K, co
   if (!x || !w || !scales || !y) return TB_ERR_NULL;  // biases may be NULL: each is -scale
   int rc = check_linear_shape(M, K, block, N);
   if (rc != TB_OK) return rc;
-  if (algo != TB_ALGO_AUTO && algo != TB_ALGO_GEMV && algo != TB_ALGO_TC) return TB_ERR_UNSUPPORTED;
+  if (algo < TB_ALGO_AUTO || algo > TB_ALGO_GEMV_TMEM) return TB_ERR_UNSUPPORTED;
   if (!aligned16(x) || !aligned16(w) || !aligned16(scales) || (biases && !aligned16(biases)) ||
       !aligned16(y) ||
       (signs && !aligned16(signs)) || (workspace && !aligned16(workspace)))
@@ -125,10 +151,8 @@ extern "C" int tb_packed_linear_algo(const uint16_t* x, int64_t M, int64_t K, co
     return launch_gemm_tc(xh, M, K, sg, block, w, sh, bh, N, yh,
                           static_cast<char*>(workspace) + fixup_region(), dev_status, s);
   }
-  if (K % kBlock == 0)  // TMA-streamed GEMV; without a workspace its ranges stay on tile bounds
-    return launch_gemv_tma(xh, M, K, sg, block, w, sh, bh, N, yh, workspace, workspace_bytes,
-                           dev_status, s);
-  return launch_gemv(xh, M, K, sg, block, w, sh, bh, N, yh, dev_status, s);
+  return launch_streaming_gemv(use, xh, M, K, sg, block, 1, &w, &sh, &bh, &N, &yh, workspace,
+                               workspace_bytes, dev_status, s);
 }
 
 extern "C" int tb_packed_linear(const uint16_t* x, int64_t M, int64_t K, const int8_t* signs,
@@ -180,8 +204,8 @@ extern "C" int tb_packed_linear_multi(const uint16_t* x, int64_t M, int64_t K, c
     block = 0;
   }
   if (M <= kGemvMaxTokens)
-    return launch_gemv_tma_multi(xh, M, K, sg, block, n, w, sh, bh, N, yh, workspace, workspace_bytes,
-                                 dev_status, s);
+    return launch_streaming_gemv(TB_ALGO_GEMV, xh, M, K, sg, block, n, w, sh, bh, N, yh, workspace,
+                                 workspace_bytes, dev_status, s);
   // prefill: one rotation of x into the workspace, then one GEMM per matrix
   int64_t maxN = 0;
   for (int i = 0; i < n; ++i) maxN = N[i] > maxN ? N[i] : maxN;
