@@ -26,15 +26,14 @@
 //    sum_k q x' = 2^E (D[3t] + D[3t+1]/16 + D[3t+2]/256), then y += s * that + b * S with
 //    S = sum x' over the group.  Rows 8..15 of B read the next atom: those D columns are unused.
 //
-// Roles: two warpgroups each walk a contiguous half of the CTA's stream-K unit range (the second
-// one backwards, so that the tiles shared with both neighbouring CTAs are finished first).  Per
-// group of 128 k a warpgroup loads its rows' 8 words per thread from the TMA box, decodes them,
-// stores 32 columns of A (two buffers), and one thread issues the group's four MMAs into the
-// group's accumulator and commits them to the buffer's mbarrier.  The epilogue of a unit runs
-// while the next unit's first MMAs are in flight.  A producer warp streams 16 KB boxes of packed
-// codes (128 rows x 512 k) into a ring shared by both warpgroups.  About 100 KB of shared memory
-// and 256 tensor-memory columns per CTA leave room for a second CTA on the SM: with programmatic
-// dependent launch, the next call's CTAs start streaming their weights while this call finishes.
+// Roles (one CTA of ten warps per SM): warp 0 streams 16 KB boxes of packed codes (128 rows x
+// 512 k) into a six-slot TMA ring; warps 2..9 form two decoder warpgroups, each walking a
+// contiguous half of the CTA's stream-K unit range (the second one backwards, so that the tiles
+// shared with both neighbouring CTAs are finished first).  Per group of 128 k a warpgroup loads
+// its rows' 8 words per thread from the box, decodes them, stores 32 columns of A into one of six
+// tensor-memory slots and signals an mbarrier; warp 1 issues the group's four MMAs into one of
+// four accumulators and commits them to the slot's and the accumulator's mbarriers; the
+// warpgroup reads the accumulator three groups later.  No step waits on a CTA-wide barrier.
 #include <cuda.h>
 #include <cuda_fp8.h>
 #include <cudaTypedefs.h>
@@ -52,13 +51,18 @@ namespace tb {
 int code_map(const uint32_t* w, int64_t N, int64_t K, CUtensorMap* out);
 size_t gemv_fixup_bytes();
 
-constexpr int kF8ConsumerWarps = 8;                     // two warpgroups
-constexpr int kF8Threads = (kF8ConsumerWarps + 1) * 32;  // + the producer warp
-constexpr int kF8Ring = 3;                              // 16 KB code boxes in flight per CTA
+constexpr int kF8ConsumerWarps = 8;                     // two decoder warpgroups
+constexpr int kF8Threads = (kF8ConsumerWarps + 2) * 32;  // + the producer and the MMA warp
+constexpr int kF8Ring = 6;                              // 16 KB code boxes in flight per CTA
 constexpr int kF8MaxBlocks = 6;                         // 1024-blocks of x' one CTA's image holds
-constexpr int kF8TmemCols = 256;                        // per warpgroup: A 2 x 32, D 4 x 16
+constexpr int kF8RA = 6;                                // A slots (32 columns, one group) per warpgroup
+constexpr int kF8RD = 4;                                // accumulators (16 columns) per warpgroup
+constexpr int kF8Lag = 3;                               // groups between a group's MMAs and its epilogue
+constexpr int kF8TmemCols = 512;                        // 2 warpgroups x (6 x 32 + 4 x 16)
 constexpr int kF8CutSlots = 3;                          // tiles cut by the lo / mid / hi boundaries
 constexpr int kF8PartStride = kUnitRows * 8;            // floats per workspace part slot
+static_assert(kF8Lag < kUnitGroups && kF8Lag < kF8RD, "epilogue lag");
+static_assert(2 * (32 * kF8RA + 16 * kF8RD) <= kF8TmemCols, "tensor memory");
 // tcgen05 instruction descriptor: fp32 D, e4m3 A and B (both K-major), N = 16, M = 128
 constexpr uint32_t kF8Idesc = (1u << 4) | ((16u >> 3) << 17) | ((128u >> 4) << 24);
 
@@ -100,7 +104,7 @@ __host__ __device__ inline F8Layout f8_layout(int nblk) {
   L.cnt = off;
   off += 16;
   L.bars = off;
-  off += (2 * kF8Ring + 4) * 8;
+  off += (2 * kF8Ring + 4 * kF8RA + 4 * kF8RD) * 8;
   L.tslot = off;
   off += 16;
   L.total = off + 1024;  // slack to align the base to 1024
@@ -149,14 +153,8 @@ TB_DEVI int f8_mat_of(const F8Args& a, int tile) {
   return i;
 }
 
-// named barriers with immediate ids (1: the eight consumer warps; 2, 3: warpgroup 0, 1), so
-// that the kernel is known to use four of the CTA's barriers
+// the eight decoder warps' named barrier (an immediate id: the kernel uses two barriers)
 TB_DEVI void bar_consumers() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
-TB_DEVI void bar_warpgroup(int u) {
-  if (u == 0) asm volatile("bar.sync 2, 128;" ::: "memory");
-  else asm volatile("bar.sync 3, 128;" ::: "memory");
-}
-
 TB_DEVI void f8_sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
                : "memory");
@@ -180,9 +178,7 @@ TB_DEVI void store_b_chunk(uint32_t addr, const uint16_t (&T)[8]) {
 }
 
 template <int MT>
-// 112 registers: two CTAs of 288 threads fill the register file (no third CTA, whose tensor
-// memory would not fit beside the other two)
-__global__ void __maxnreg__(112)
+__global__ void __launch_bounds__(kF8Threads, 1)
     w2_gemv_f8_kernel(const __grid_constant__ F8Maps maps, const __grid_constant__ F8Args a) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -197,7 +193,12 @@ __global__ void __maxnreg__(112)
   int* cnt = reinterpret_cast<int*>(smem + L.cnt);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* empty = full + kF8Ring;
-  uint64_t* mmab = empty + kF8Ring;  // [warpgroup][A buffer]: commits of the MMAs reading it
+  // per warpgroup: A slots written (afull) / read by the MMAs (aempty); accumulators written by
+  // the MMAs (dfull) / read by the epilogue (dempty)
+  uint64_t* afull = empty + kF8Ring;
+  uint64_t* aempty = afull + 2 * kF8RA;
+  uint64_t* dfull = aempty + 2 * kF8RA;
+  uint64_t* dempty = dfull + 2 * kF8RD;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + L.tslot);
   __shared__ volatile int aborted;
 
@@ -208,6 +209,14 @@ __global__ void __maxnreg__(112)
   f8_cta_range(blockIdx.x, gridDim.x, a.n_tiles, C, a.split, lo, hi);
   const int nst = hi - lo, mid = lo + nst / 2;
   const int cnt0 = mid - lo, cnt1 = hi - mid, mboth = cnt0 < cnt1 ? cnt0 : cnt1;
+  int b1, e1, b2, e2;  // the 1024-blocks of x this CTA's units read
+  f8_blocks_needed(lo, nst, C, K, b1, e1, b2, e2);
+  const int nblk = (e1 - b1) + (e2 - b2);
+  auto img_group = [&](int gglob) {  // image atom of global group gglob (128 k)
+    const int blk = gglob >> 3;
+    const int bpos = (blk >= b1 && blk < e1) ? blk - b1 : (e1 - b1) + (blk - b2);
+    return bpos * 8 + (gglob & 7);
+  };
 
   if (threadIdx.x == 0) {
     aborted = 0;
@@ -215,12 +224,19 @@ __global__ void __maxnreg__(112)
       mbar_init(full + i, 1);
       mbar_init(empty + i, 4);  // the four warps of the warpgroup that owns the box
     }
-    for (int i = 0; i < 4; ++i) mbar_init(mmab + i, 1);
+    for (int i = 0; i < 2 * kF8RA; ++i) {
+      mbar_init(afull + i, 4);  // one arrival per warp of the warpgroup
+      mbar_init(aempty + i, 1);  // one commit
+    }
+    for (int i = 0; i < 2 * kF8RD; ++i) {
+      mbar_init(dfull + i, 1);
+      mbar_init(dempty + i, 4);
+    }
     fence_barrier_init();
   }
   for (int i = threadIdx.x; i < kF8CutSlots * kUnitRows * MT; i += blockDim.x) accs[i] = 0.f;
   if (threadIdx.x < kF8CutSlots) cnt[threadIdx.x] = 0;
-  if (warp == kF8ConsumerWarps) tmem_alloc(tslot, kF8TmemCols);
+  if (warp == 1) tmem_alloc(tslot, kF8TmemCols);
   tmem_fence_before();
   __syncthreads();
   tmem_fence_after();
@@ -234,7 +250,7 @@ __global__ void __maxnreg__(112)
     }
   };
 
-  if (warp == kF8ConsumerWarps) {
+  if (warp == 0) {
     // ---- producer: boxes of both warpgroups interleaved (the weights never depend on the
     // previous kernel, so this streams before griddepcontrol.wait)
     if (lane == 0) {
@@ -253,9 +269,7 @@ __global__ void __maxnreg__(112)
         const int tile = unit / C, chunk = unit - tile * C;
         const int slot = f % kF8Ring, k = f / kF8Ring;
         if (k > 0) wait(empty + slot, (k - 1) & 1);
-        int mi = 0;
-#pragma unroll
-        for (int q = 1; q < kMaxMats; ++q) mi += (q < a.nmat && tile >= a.tile0[q]);
+        const int mi = f8_mat_of(a, tile);
         const int row = (tile - a.tile0[mi]) * kUnitRows;
         mbar_arrive_expect_tx(full + slot, kSlotBytes);
         tma2d(ring + slot * kSlotBytes, &maps.codes[mi], chunk * 32, row, full + slot, pol);
@@ -265,27 +279,53 @@ __global__ void __maxnreg__(112)
         if (!mbar_wait(full + f % kF8Ring, (f / kF8Ring) & 1)) set_status(a.status, TB_DEV_TIMEOUT);
     }
     __syncwarp();
+  } else if (warp == 1) {
+    // ---- MMA issuer: the two warpgroups' groups in lockstep, four MMAs per group of 128 k
+    if (lane == 0) {
+      const int n4[2] = {4 * cnt0, 4 * cnt1};
+      const int nmax = n4[0] > n4[1] ? n4[0] : n4[1];
+      for (int i = 0; i < nmax; ++i) {
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          if (i >= n4[u]) continue;
+          const int sa = i % kF8RA, sd = i % kF8RD;
+          wait(afull + u * kF8RA + sa, (i / kF8RA) & 1);
+          if (i >= kF8RD) wait(dempty + u * kF8RD + sd, ((i / kF8RD) - 1) & 1);
+          tmem_fence_after();
+          const int n = i >> 2;
+          const int unit = u == 0 ? lo + n : hi - 1 - n;
+          const int chunk = unit % C;
+          const uint32_t atom = img + (uint32_t)img_group(chunk * kUnitGroups + (i & 3)) * 1024u;
+          const uint32_t tA = tmem + (uint32_t)(u * 256 + 32 * sa);
+          const uint32_t tD = tmem + (uint32_t)(u * 256 + 32 * kF8RA + 16 * sd);
+#pragma unroll
+          for (int m = 0; m < 4; ++m)
+            mma_f8f6f4_ts(tD, tA + (uint32_t)(8 * m), smem_desc_sw128(atom + 32u * m, 1024u), kF8Idesc, m > 0);
+          mma_commit(aempty + u * kF8RA + sa);
+          mma_commit(dfull + u * kF8RD + sd);
+        }
+      }
+      // every MMA issued has completed before the columns are given back
+#pragma unroll
+      for (int u = 0; u < 2; ++u)
+        if (n4[u] > 0 && !mbar_wait(dfull + u * kF8RD + (n4[u] - 1) % kF8RD, ((n4[u] - 1) / kF8RD) & 1))
+          set_status(a.status, TB_DEV_TIMEOUT);
+    }
+    __syncwarp();
   } else {
-    // ---- consumers: warpgroup u, thread r = unit row r = TMEM lane r
-    const int u = warp >> 2, q = warp & 3;
+    // ---- decoders: warpgroup u; thread r of it = unit row r = tensor-memory lane r
+    const int dw = warp - 2;
+    const int u = dw >> 2, q = warp & 3;
     const int r = q * 32 + lane;
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-    const uint32_t tA = tmem + (uint32_t)(u * 128), tD = tA + 64;
-    const bool issuer = q == 0 && lane == 0;
+    const uint32_t tAu = tmem + (uint32_t)(u * 256), tDu = tAu + 32 * kF8RA;
     const int glo = u == 0 ? lo : mid, ghi = u == 0 ? mid : hi;
     const int ncnt = ghi - glo;
     const bool back = u == 1;
-    uint64_t* mb0 = mmab + 2 * u;  // commits of the MMAs that read A buffer 0 (groups 0, 2)
-    uint64_t* mb1 = mb0 + 1;       // A buffer 1 (groups 1, 3); its last commit of a unit ends it
-
-    int b1, e1, b2, e2;
-    f8_blocks_needed(lo, nst, C, K, b1, e1, b2, e2);
-    const int nblk = (e1 - b1) + (e2 - b2);
-    auto img_group = [&](int gglob) {  // image atom of global group gglob (128 k)
-      const int blk = gglob >> 3;
-      const int bpos = (blk >= b1 && blk < e1) ? blk - b1 : (e1 - b1) + (blk - b2);
-      return bpos * 8 + (gglob & 7);
-    };
+    uint64_t* afu = afull + u * kF8RA;
+    uint64_t* aeu = aempty + u * kF8RA;
+    uint64_t* dfu = dfull + u * kF8RD;
+    uint64_t* deu = dempty + u * kF8RD;
 
     // scale and bias words of unit n for this row (8 bytes each: the unit's four groups)
     auto load_sb = [&](int n, uint2& sv, uint2& bv) {
@@ -304,13 +344,13 @@ __global__ void __maxnreg__(112)
       bv = bp ? __ldg(reinterpret_cast<const uint2*>(bp + (int64_t)row * G + chunk * kUnitGroups))
               : make_uint2(sv.x ^ 0x80008000u, sv.y ^ 0x80008000u);
     };
-    // units n - 1, n, n + 1 at the top of iteration n (the epilogue of n - 1 runs during n)
-    uint2 sv0, bv0, sv1 = make_uint2(0, 0), bv1 = make_uint2(0, 0), sv2, bv2;
+    // units n - 1, n, n + 1 at the top of iteration n
+    uint2 sv0 = make_uint2(0, 0), bv0 = make_uint2(0, 0), sv1 = make_uint2(0, 0), bv1 = make_uint2(0, 0), sv2, bv2;
     load_sb(0, sv2, bv2);
     if (a.signs) {  // the signs never depend on the previous kernel: into L1 before the wait
 #pragma unroll
       for (int qq = 0; qq < 2; ++qq) {
-        const int it = warp + qq * kF8ConsumerWarps;
+        const int it = dw + qq * kF8ConsumerWarps;
         if (it < 2 * nblk) {
           const int bi = it >> 1;
           const int b = bi < e1 - b1 ? b1 + bi : b2 + (bi - (e1 - b1));
@@ -411,7 +451,7 @@ __global__ void __maxnreg__(112)
         store_b_chunk(atom + (row0 + 2) * 128 + ((j ^ (row0 + 2)) << 4), tl);
         if ((lane & 7) == 0) cg[ig * MT + tok] = make_float2(ssum, __uint_as_float((uint32_t)(127 + E) << 23));
       };
-      for (int it = warp; it < items; it += 2 * kF8ConsumerWarps) {
+      for (int it = dw; it < items; it += 2 * kF8ConsumerWarps) {
         const int it2 = it + kF8ConsumerWarps;
         uint4 xa[4], sa[2], xb[4], sb2[2];
         load_item(it, xa, sa);
@@ -512,28 +552,34 @@ __global__ void __maxnreg__(112)
       if (lane == 0) a.ws_count[first] = 0;
     };
 
-    // y += s * (2^E (D0 + D1/16 + D2/256)) + b * S for the four groups of a finished unit
-    constexpr int kDc = MT == 1 ? 4 : 8;  // accumulator columns read per group
-    auto epilogue = [&](int chunk, const float (&d)[4][kDc], uint2 sv, uint2 bv) {
-      const float2 s01 = __half22float2(*reinterpret_cast<const __half2*>(&sv.x));
-      const float2 s23 = __half22float2(*reinterpret_cast<const __half2*>(&sv.y));
-      const float2 b01 = __half22float2(*reinterpret_cast<const __half2*>(&bv.x));
-      const float2 b23 = __half22float2(*reinterpret_cast<const __half2*>(&bv.y));
-      const float sg[4] = {s01.x, s01.y, s23.x, s23.y}, bg[4] = {b01.x, b01.y, b23.x, b23.y};
+    // Epilogue of group j of this warpgroup (group gg of a unit with chunk `chunk`): its
+    // accumulator, then y += s * 2^E (D0 + D1/16 + D2/256) + b * S
+    constexpr int kDc = MT == 1 ? 4 : 8;  // accumulator columns read
+    auto epilogue = [&](int j, int chunk, int gg, uint2 sv, uint2 bv) {
+      const int sd = j % kF8RD;
+      wait(dfu + sd, (j / kF8RD) & 1);
+      tmem_fence_after();
+      float d[kDc];
+      if constexpr (MT == 1) tmem_ld4(tDu + (uint32_t)(16 * sd) + lane_off, d);
+      else tmem_ld8(tDu + (uint32_t)(16 * sd) + lane_off, d);
+      tmem_wait_ld();
+      tmem_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(deu + sd);
+      const uint32_t sw = gg < 2 ? sv.x : sv.y, bw = gg < 2 ? bv.x : bv.y;
+      const float s = __half2float(__ushort_as_half((unsigned short)((gg & 1) ? sw >> 16 : sw & 0xFFFFu)));
+      const float bb = __half2float(__ushort_as_half((unsigned short)((gg & 1) ? bw >> 16 : bw & 0xFFFFu)));
+      const float2* c2 = cg + img_group(chunk * kUnitGroups + gg) * MT;
 #pragma unroll
-      for (int gg = 0; gg < 4; ++gg) {
-        const float2* c2 = cg + img_group(chunk * kUnitGroups + gg) * MT;
-#pragma unroll
-        for (int t = 0; t < MT; ++t) {
-          const float2 cs = c2[t];
-          const float dq = fmaf(d[gg][3 * t + 2], 0.00390625f, fmaf(d[gg][3 * t + 1], 0.0625f, d[gg][3 * t])) * cs.y;
-          acc[t] = fmaf(sg[gg], dq, fmaf(bg[gg], cs.x, acc[t]));
-        }
+      for (int t = 0; t < MT; ++t) {
+        const float2 cs = c2[t];
+        const float dq = fmaf(d[3 * t + 2], 0.00390625f, fmaf(d[3 * t + 1], 0.0625f, d[3 * t])) * cs.y;
+        acc[t] = fmaf(s, dq, fmaf(bb, cs.x, acc[t]));
       }
     };
 
     const int rsw = r & 7;
-    int ptile = -1, pchunk = 0;  // the unit whose epilogue is pending
+    int ptile = 0, pchunk = 0;  // unit n - 1
     for (int n = 0; n < ncnt; ++n) {
       const int unit = back ? ghi - 1 - n : glo + n;
       const int tile = unit / C, chunk = unit - tile * C;
@@ -548,83 +594,64 @@ __global__ void __maxnreg__(112)
       const uint32_t box = ring + (uint32_t)slot * kSlotBytes + (uint32_t)r * 128u;
 #pragma unroll
       for (int g = 0; g < kUnitGroups; ++g) {
+        const int i = 4 * n + g;
         const uint4 wa = ld_shared_v4(box + ((uint32_t)((2 * g) ^ rsw) << 4));
         const uint4 wb = ld_shared_v4(box + ((uint32_t)((2 * g + 1) ^ rsw) << 4));
         uint32_t A[32];
         const uint32_t wv[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const uint32_t w4 = wv[j] >> 4;
-          A[4 * j + 0] = wv[j] & 0x03030303u;  // codes 0, 4, 8, 12:  q * 2^-9
-          A[4 * j + 1] = wv[j] & 0x0C0C0C0Cu;  // codes 1, 5, 9, 13:  q * 2^-7
-          A[4 * j + 2] = w4 & 0x03030303u;     // codes 2, 6, 10, 14: q * 2^-9
-          A[4 * j + 3] = w4 & 0x0C0C0C0Cu;     // codes 3, 7, 11, 15: q * 2^-7
+        for (int jj = 0; jj < 8; ++jj) {
+          const uint32_t w4 = wv[jj] >> 4;
+          A[4 * jj + 0] = wv[jj] & 0x03030303u;  // codes 0, 4, 8, 12:  q * 2^-9
+          A[4 * jj + 1] = wv[jj] & 0x0C0C0C0Cu;  // codes 1, 5, 9, 13:  q * 2^-7
+          A[4 * jj + 2] = w4 & 0x03030303u;      // codes 2, 6, 10, 14: q * 2^-9
+          A[4 * jj + 3] = w4 & 0x0C0C0C0Cu;      // codes 3, 7, 11, 15: q * 2^-7
         }
         if (g == kUnitGroups - 1) {  // the box is read: the producer may refill it
           __syncwarp();
           if (lane == 0) mbar_arrive(empty + slot);
         }
-        // the A buffer is free once the MMAs that last read it are done
-        if (g == 0 && n > 0) wait(mb0, 1);
-        if (g == 2) wait(mb0, 0);
-        if (g == 3) wait(mb1, 0);
+        const int sa = i % kF8RA;
+        if (i >= kF8RA) wait(aeu + sa, ((i / kF8RA) - 1) & 1);  // the MMAs that read it are done
         tmem_fence_after();
-        tmem_st32(tA + (uint32_t)(32 * (g & 1)) + lane_off, A);
+        tmem_st32(tAu + (uint32_t)(32 * sa) + lane_off, A);
         tmem_wait_st();
-        float d[4][kDc];
-        if (g == 0 && n > 0) {  // the previous unit's accumulators, before group 0 overwrites them
-          wait(mb1, 1);
-          tmem_fence_after();
-#pragma unroll
-          for (int gg = 0; gg < 4; ++gg) {
-            if constexpr (MT == 1) tmem_ld4(tD + (uint32_t)(16 * gg) + lane_off, d[gg]);
-            else tmem_ld8(tD + (uint32_t)(16 * gg) + lane_off, d[gg]);
-          }
-          tmem_wait_ld();
-        }
         tmem_fence_before();
-        bar_warpgroup(u);
-        if (issuer) {
-          tmem_fence_after();
-          const uint32_t atom = img + (uint32_t)img_group(chunk * kUnitGroups + g) * 1024u;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(afu + sa);
+        // the epilogue runs kF8Lag groups behind: groups 1..3 of unit n - 1, then group 0 of n
+        if (i >= kF8Lag) {
+          if (g < kF8Lag) {
+            epilogue(i - kF8Lag, pchunk, g + kUnitGroups - kF8Lag, sv0, bv0);
+            if (g == kF8Lag - 1 && tile != ptile) {  // unit n - 1 is done and its tile ends there
+              flush(ptile);
 #pragma unroll
-          for (int m = 0; m < 4; ++m)
-            mma_f8f6f4_ts(tD + (uint32_t)(16 * g), tA + (uint32_t)(32 * (g & 1) + 8 * m),
-                          smem_desc_sw128(atom + 32u * m, 1024u), kF8Idesc, m > 0);
-          mma_commit(g & 1 ? mb1 : mb0);
-        }
-        if (g == 0 && n > 0) {
-          epilogue(pchunk, d, sv0, bv0);
-          if (tile != ptile) {
-            flush(ptile);
-#pragma unroll
-            for (int t = 0; t < MT; ++t) acc[t] = 0.f;
+              for (int t = 0; t < MT; ++t) acc[t] = 0.f;
+            }
+          } else {
+            epilogue(i - kF8Lag, chunk, g - kF8Lag, sv1, bv1);
           }
         }
       }
       ptile = tile;
       pchunk = chunk;
     }
-    if (ncnt > 0) {  // the last unit's epilogue
-      wait(mb1, 1);
-      tmem_fence_after();
-      float d[4][kDc];
-#pragma unroll
-      for (int gg = 0; gg < 4; ++gg) {
-        if constexpr (MT == 1) tmem_ld4(tD + (uint32_t)(16 * gg) + lane_off, d[gg]);
-        else tmem_ld8(tD + (uint32_t)(16 * gg) + lane_off, d[gg]);
+    if (ncnt > 0) {  // the last kF8Lag groups
+      const int i_end = 4 * ncnt;
+      for (int j = i_end - kF8Lag; j < i_end; ++j) {
+        if (j < 0) continue;
+        const int gg = j & 3;
+        epilogue(j, pchunk, gg, sv1, bv1);
       }
-      tmem_wait_ld();
-      epilogue(pchunk, d, sv1, bv1);
       flush(ptile);
     }
   }
 
-  // every MMA of this CTA has completed (each warpgroup waited for its last commit) and every
-  // load from tensor memory has returned: give the columns back
+  // every MMA of this CTA has completed (the issuer waited for its last commits) and every load
+  // from tensor memory has returned: give the columns back
   tmem_fence_before();
   __syncthreads();
-  if (warp == kF8ConsumerWarps) {
+  if (warp == 1) {
     tmem_fence_after();
     tmem_dealloc(tmem, kF8TmemCols);
   }
@@ -633,10 +660,10 @@ __global__ void __maxnreg__(112)
 // ------------------------------------------------------------------ host side
 template <int MT>
 static int launch_f8_mt(const F8Args& a, const F8Maps& maps, int grid, int smem_optin, cudaStream_t s) {
-  // at least 76 KB, so that shared memory too admits at most two CTAs per SM (their 2 x 256
-  // tensor-memory columns are all the SM has)
+  // at least 116 KB, so that shared memory admits one CTA per SM (it takes all 512 tensor-memory
+  // columns)
   int bytes = f8_layout<MT>(a.nblk_max).total;
-  bytes = bytes < 76 * 1024 ? 76 * 1024 : bytes;
+  bytes = bytes < 116 * 1024 ? 116 * 1024 : bytes;
   if (bytes > smem_optin) return TB_ERR_UNSUPPORTED;
   cudaError_t e = cudaFuncSetAttribute(w2_gemv_f8_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e == cudaSuccess)
