@@ -74,15 +74,15 @@ enum {
 
 /* algorithm choice for tb_packed_linear_algo */
 #define TB_ALGO_AUTO 0       /* GEMV for M <= 8, tensor-core GEMM above */
-#define TB_ALGO_GEMV 1       /* fused sign*FWHT prologue + streaming W2 GEMV; any M (passes of 8
-                                tokens): the tensor-memory GEMV where it applies, else the
-                                warp-level one */
+#define TB_ALGO_GEMV 1       /* fused sign*FWHT prologue + streaming W2 GEMV (the warp-level one);
+                                any M (passes of 8 tokens) */
 #define TB_ALGO_TC 2         /* FWHT kernel into the workspace + tcgen05/TMEM GEMM; any M */
 #define TB_ALGO_GEMV_SYNC 3  /* the warp-level GEMV only (mma.sync on fp16 operands); any M */
-#define TB_ALGO_GEMV_TMEM 4  /* the tensor-memory GEMV only (tcgen05.mma on e4m3 operands):
-                                M <= 2, K a multiple of 1024, block 0 or 1024, at most 6
-                                1024-blocks of x per SM's share of the work; TB_ERR_UNSUPPORTED
-                                where it does not apply */
+#define TB_ALGO_GEMV_TMEM 4  /* the tensor-memory GEMV (tcgen05.mma on e4m3 operands, decoded
+                                codes in tensor memory): M <= 2, K a multiple of 1024, block 0
+                                or 1024, at most 6 1024-blocks of x per SM's share of the work;
+                                TB_ERR_UNSUPPORTED where it does not apply.  Slower than the
+                                warp-level GEMV at these token counts; never chosen by AUTO */
 
 /* Human-readable text of a return code; never NULL. */
 const char* tb_status_string(int status);

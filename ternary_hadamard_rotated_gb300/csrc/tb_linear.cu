@@ -58,21 +58,19 @@ static int resolve_algo(int64_t M, int algo) {
   return algo;
 }
 
-// The streaming GEMV (decode): the tensor-memory kernel where it applies (M <= 2, K a multiple
-// of 1024) unless the warp-level one is asked for, else the warp-level TMA kernel, else (K not a
-// multiple of 1024) the row-streaming one.  `which` is TB_ALGO_GEMV, _GEMV_SYNC or _GEMV_TMEM.
+// The streaming GEMV (decode): the warp-level TMA kernel (K a multiple of 1024), else the
+// row-streaming one; the tensor-memory kernel only when asked for (TB_ALGO_GEMV_TMEM: at one or
+// two tokens it measured slower, its MMA issue rate being below the weights' arrival rate).
+// `which` is TB_ALGO_GEMV, _GEMV_SYNC or _GEMV_TMEM.
 static int launch_streaming_gemv(int which, const __half* x, int64_t M, int64_t K, const int8_t* sg,
                                  int block, int n, const uint32_t* const* w, const __half* const* sh,
                                  const __half* const* bh, const int64_t* N, __half* const* yh,
                                  void* workspace, size_t workspace_bytes, int32_t* dev_status,
                                  cudaStream_t s) {
-  if (which != TB_ALGO_GEMV_SYNC && K % kBlock == 0) {
-    const int rc = launch_gemv_f8_multi(x, M, K, sg, block, n, w, sh, bh, N, yh, workspace,
-                                        workspace_bytes, dev_status, s);
-    if (rc != TB_ERR_UNSUPPORTED || which == TB_ALGO_GEMV_TMEM) return rc;
-  } else if (which == TB_ALGO_GEMV_TMEM) {
-    return TB_ERR_UNSUPPORTED;
-  }
+  if (which == TB_ALGO_GEMV_TMEM)
+    return K % kBlock == 0 ? launch_gemv_f8_multi(x, M, K, sg, block, n, w, sh, bh, N, yh, workspace,
+                                                  workspace_bytes, dev_status, s)
+                           : TB_ERR_UNSUPPORTED;
   if (K % kBlock == 0)  // TMA-streamed GEMV; without a workspace its ranges stay on tile bounds
     return launch_gemv_tma_multi(x, M, K, sg, block, n, w, sh, bh, N, yh, workspace, workspace_bytes,
                                  dev_status, s);
