@@ -73,7 +73,8 @@ enum {
 #define TB_DEV_BAD_PLAN 8  /* tb_chain_run: the plan does not match the launch (nothing computed) */
 
 /* algorithm choice for tb_packed_linear_algo */
-#define TB_ALGO_AUTO 0       /* GEMV for M <= 8, tensor-core GEMM above */
+#define TB_ALGO_AUTO 0       /* GEMV for M <= 8, the batched-decode GEMV for 9..64 tokens,
+                                the tensor-core GEMM above */
 #define TB_ALGO_GEMV 1       /* fused sign*FWHT prologue + streaming W2 GEMV (the warp-level one);
                                 any M (passes of 8 tokens) */
 #define TB_ALGO_TC 2         /* FWHT kernel into the workspace + tcgen05/TMEM GEMM; any M */
@@ -83,6 +84,11 @@ enum {
                                 or 1024, at most 6 1024-blocks of x per SM's share of the work;
                                 TB_ERR_UNSUPPORTED where it does not apply.  Slower than the
                                 warp-level GEMV at these token counts; never chosen by AUTO */
+#define TB_ALGO_GEMV_WIDE 5  /* the batched-decode GEMV on tensor memory: the weights the MMA's
+                                128-row side (decoded to fp16 s*q + b in tensor memory), the
+                                tokens its N side; x' rotated into the workspace first, as for
+                                TB_ALGO_TC (same workspace); M <= 64 (else passes of 64 tokens),
+                                K a multiple of 1024 (TB_ERR_UNSUPPORTED otherwise) */
 
 /* Human-readable text of a return code; never NULL. */
 const char* tb_status_string(int status);

@@ -509,6 +509,9 @@ static size_t tc_part_bytes() { return (size_t)tc_sms_bound() * 2 * (2 * kTcBM) 
 
 size_t gemm_tc_x_bytes(int64_t M, int64_t K) { return tc_x_bytes(M, K); }
 
+// offset of the parts region inside the tensor-core path's workspace (after x' and the counts)
+size_t gemm_tc_part_offset(int64_t M, int64_t K, int64_t N) { return tc_x_bytes(M, K) + tc_count_bytes(M, N); }
+
 size_t gemm_tc_workspace(int64_t M, int64_t K, int64_t N) {
   return tc_x_bytes(M, K) + tc_count_bytes(M, N) + tc_part_bytes();
 }

@@ -37,6 +37,11 @@ int launch_gemv_f8_multi(const __half* x, int64_t M, int64_t K, const int8_t* si
                          int nmat, const uint32_t* const* w, const __half* const* scales,
                          const __half* const* biases, const int64_t* N, __half* const* y,
                          void* workspace, size_t ws_bytes, int32_t* status, cudaStream_t s);
+int launch_gemv_wide(const __half* xp, int64_t M, int64_t K, const uint32_t* w, const __half* scales,
+                     const __half* biases, int64_t N, __half* y, int* count, float* part, int32_t* status,
+                     cudaStream_t s);
+size_t gemv_wide_part_bytes();
+size_t gemm_tc_part_offset(int64_t M, int64_t K, int64_t N);
 constexpr int kMaxMulti = 4;
 
 // Workspace layout: [fixup region of the GEMV split schedule (zero before the first call,
@@ -53,9 +58,36 @@ static size_t natural_x_bytes(int64_t M, int64_t K) { return (size_t)((M * K * 2
 // decode (GEMV) up to this many tokens; the tensor-core GEMM above
 constexpr int64_t kGemvMaxTokens = 8;
 
+// the batched-decode GEMV up to this many tokens per pass (AUTO: above kGemvMaxTokens)
+constexpr int64_t kWideMaxTokens = 64;
+
 static int resolve_algo(int64_t M, int algo) {
-  if (algo == TB_ALGO_AUTO) return M <= kGemvMaxTokens ? TB_ALGO_GEMV : TB_ALGO_TC;
+  if (algo == TB_ALGO_AUTO)
+    return M <= kGemvMaxTokens ? TB_ALGO_GEMV : M <= kWideMaxTokens ? TB_ALGO_GEMV_WIDE : TB_ALGO_TC;
   return algo;
+}
+// the batched-decode GEMV uses the tensor-core path's workspace (x', then its parts region)
+static bool uses_tc_workspace(int use) { return use == TB_ALGO_TC || use == TB_ALGO_GEMV_WIDE; }
+
+// x' = fwht(x) in pair order into the workspace, then the batched-decode GEMV in passes of up to
+// 64 tokens over it (K a multiple of 1024).
+static int launch_wide_path(const __half* xh, int64_t M, int64_t K, const int8_t* sg, int block,
+                            const uint32_t* w, const __half* sh, const __half* bh, int64_t N, __half* yh,
+                            void* workspace, int32_t* dev_status, cudaStream_t s, bool rotate_x) {
+  char* ws = static_cast<char*>(workspace);
+  __half* xp = reinterpret_cast<__half*>(ws + fixup_region());
+  if (rotate_x) {
+    const int rc = launch_rotate_pairorder(xh, xp, sg, M, K, block != 0, s);
+    if (rc != TB_OK) return rc;
+  }
+  int* count = reinterpret_cast<int*>(ws);
+  float* part = reinterpret_cast<float*>(ws + fixup_region() + gemm_tc_part_offset(M, K, N));
+  for (int64_t m0 = 0; m0 < M; m0 += kWideMaxTokens) {
+    const int64_t mc = M - m0 < kWideMaxTokens ? M - m0 : kWideMaxTokens;
+    const int rc = launch_gemv_wide(xp + m0 * K, mc, K, w, sh, bh, N, yh + m0 * N, count, part, dev_status, s);
+    if (rc != TB_OK) return rc;
+  }
+  return TB_OK;
 }
 
 // The streaming GEMV (decode): the warp-level TMA kernel (K a multiple of 1024), else the
@@ -89,7 +121,7 @@ static int check_linear_shape(int64_t M, int64_t K, int block, int64_t N) {
 // schedule state, and x' in natural order for a block that is not fused
 static size_t linear_workspace(int64_t M, int64_t K, int64_t N, int block, int use) {
   size_t b = fixup_region();
-  if (use == TB_ALGO_TC) b += gemm_tc_workspace(M, K, N);
+  if (uses_tc_workspace(use)) b += gemm_tc_workspace(M, K, N);
   if (separate_block(block)) b += natural_x_bytes(M, K);
   return b;
 }
@@ -97,7 +129,7 @@ static size_t linear_workspace(int64_t M, int64_t K, int64_t N, int block, int u
 // where x' in natural order goes: after everything the matmul path itself uses
 static __half* natural_x(void* workspace, int64_t M, int64_t K, int64_t N, int use) {
   return reinterpret_cast<__half*>(static_cast<char*>(workspace) + fixup_region() +
-                                   (use == TB_ALGO_TC ? gemm_tc_workspace(M, K, N) : 0));
+                                   (uses_tc_workspace(use) ? gemm_tc_workspace(M, K, N) : 0));
 }
 
 }  // namespace tb
@@ -122,7 +154,7 @@ extern "C" int tb_packed_linear_algo(const uint16_t* x, int64_t M, int64_t K, co
   if (!x || !w || !scales || !y) return TB_ERR_NULL;  // biases may be NULL: each is -scale
   int rc = check_linear_shape(M, K, block, N);
   if (rc != TB_OK) return rc;
-  if (algo < TB_ALGO_AUTO || algo > TB_ALGO_GEMV_TMEM) return TB_ERR_UNSUPPORTED;
+  if (algo < TB_ALGO_AUTO || algo > TB_ALGO_GEMV_WIDE) return TB_ERR_UNSUPPORTED;
   if (!aligned16(x) || !aligned16(w) || !aligned16(scales) || (biases && !aligned16(biases)) ||
       !aligned16(y) ||
       (signs && !aligned16(signs)) || (workspace && !aligned16(workspace)))
@@ -142,6 +174,12 @@ extern "C" int tb_packed_linear_algo(const uint16_t* x, int64_t M, int64_t K, co
     xh = xn;
     sg = nullptr;
     block = 0;
+  }
+  if (use == TB_ALGO_GEMV_WIDE) {
+    if (K % kBlock) return TB_ERR_UNSUPPORTED;
+    const size_t need = fixup_region() + gemm_tc_workspace(M, K, N);
+    if (!workspace || workspace_bytes < need) return TB_ERR_WORKSPACE;
+    return launch_wide_path(xh, M, K, sg, block, w, sh, bh, N, yh, workspace, dev_status, s, true);
   }
   if (use == TB_ALGO_TC) {
     const size_t need = fixup_region() + gemm_tc_workspace(M, K, N);
@@ -192,7 +230,7 @@ extern "C" int tb_packed_linear_multi(const uint16_t* x, int64_t M, int64_t K, c
   if (separate_block(block)) {  // x' once into the workspace, then the unrotated matrices
     int64_t maxN = 0;
     for (int i = 0; i < n; ++i) maxN = N[i] > maxN ? N[i] : maxN;
-    const int use = M <= kGemvMaxTokens ? TB_ALGO_GEMV : TB_ALGO_TC;
+    const int use = resolve_algo(M, TB_ALGO_AUTO);
     if (!workspace || workspace_bytes < linear_workspace(M, K, maxN, block, use)) return TB_ERR_WORKSPACE;
     __half* xn = natural_x(workspace, M, K, maxN, use);
     int rc2 = launch_fwht(xh, xn, sg, M, K, block, 0, s);
@@ -213,6 +251,8 @@ extern "C" int tb_packed_linear_multi(const uint16_t* x, int64_t M, int64_t K, c
   void* gws = static_cast<char*>(workspace) + fixup_region() + gemm_tc_x_bytes(M, K);
   int rc = launch_rotate_pairorder(xh, xp, sg, M, K, block != 0, s);
   for (int i = 0; i < n && rc == TB_OK; ++i)
-    rc = launch_gemm_tc_rotated(xp, M, K, w[i], sh[i], bh[i], N[i], yh[i], gws, dev_status, s);
+    rc = M <= kWideMaxTokens
+             ? launch_wide_path(xh, M, K, sg, block, w[i], sh[i], bh[i], N[i], yh[i], workspace, dev_status, s, false)
+             : launch_gemm_tc_rotated(xp, M, K, w[i], sh[i], bh[i], N[i], yh[i], gws, dev_status, s);
   return rc;
 }
