@@ -7,12 +7,13 @@
 // in fp16 for the pack's b = -s.
 //
 // Per CTA (one per SM), in the GEMV's stream-K ranges of units (128 rows x 512 k):
-//  * warp 0 streams the 16 KB boxes of packed codes and, per group of 128 k, the two 64-k boxes of
-//    x' (fp16 [MT rows, 64 k] each, 128-byte swizzle; rows past M read as zero), x' being the
-//    rotation kernel's output in the pair order of a decoded word (pair p of 16 columns holds
-//    columns p and p + 8);
-//  * warps 2..5 decode the group's 128 codes of their row into 64 fp16 pairs s*q + b and store
-//    them as 64 columns of a tensor-memory A slot (six slots);
+//  * warp 0 streams the 16 KB boxes of packed codes, and warp 10, independently, per group of
+//    128 k the two 64-k boxes of x' (fp16 [MT rows, 64 k] each, 128-byte swizzle; rows past M
+//    read as zero), x' being the rotation kernel's output in the pair order of a decoded word
+//    (pair p of 16 columns holds columns p and p + 8);
+//  * warps 2..5 (groups 0 and 2 of a unit) and 6..9 (groups 1 and 3) decode a group's 128 codes
+//    of their row into 64 fp16 pairs s*q + b and store them as 64 columns of a tensor-memory A
+//    slot (six slots; a group's A slot and x' slot are released by one commit of its MMAs);
 //  * warp 1 issues the group's eight tcgen05.mma (kind::f16, M = 128, N = MT, K = 16) into the
 //    accumulator of the current tile segment (two accumulators of MT columns: a segment's is read
 //    while the next one fills);
@@ -32,11 +33,15 @@ namespace tb {
 
 int code_map(const uint32_t* w, int64_t N, int64_t K, CUtensorMap* out);
 
-constexpr int kWdThreads = 6 * 32;  // producer, MMA issuer, four decoder warps
-constexpr int kWdCodeRing = 4;      // 16 KB code boxes
-constexpr int kWdXRing = 6;         // x' slots (two 64-k boxes of MT rows each)
-constexpr int kWdRA = 6;            // A slots of 64 columns (one group of 128 k in fp16)
+constexpr int kWdThreads = 11 * 32;  // code producer, MMA issuer, two decoder warpgroups, x' producer
+constexpr int kWdRing = 6;           // A slots (64 columns of fp16 pairs: one group of 128 k)
 constexpr int kWdTmemCols = 512;
+// 16 KB code boxes and x' slots (two 64-k boxes of MT rows: one group) in about 200 KB of shared
+// memory; x' comes from L2 with a long latency, so its ring is as deep as the room allows
+template <int MT> struct WideRings {
+  static constexpr int kCode = MT <= 32 ? 6 : 4;
+  static constexpr int kX = MT <= 16 ? 24 : MT <= 32 ? 12 : MT <= 48 ? 10 : 8;
+};
 
 TB_DEVI void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc, int accumulate) {
   asm volatile(
@@ -96,11 +101,11 @@ __host__ __device__ constexpr WideLayout wide_layout() {
   WideLayout L{0, 0, 0, 0, 0};
   int off = 0;
   L.code = off;
-  off += kWdCodeRing * kSlotBytes;
+  off += WideRings<MT>::kCode * kSlotBytes;
   L.xs = off;  // 1024-aligned: two boxes of MT rows x 128 bytes per slot
-  off += kWdXRing * 2 * MT * 128;
+  off += WideRings<MT>::kX * 2 * MT * 128;
   L.bars = off;
-  off += (2 * kWdCodeRing + 2 * kWdXRing + 2 * kWdRA + 4) * 8;
+  off += (2 * WideRings<MT>::kCode + 2 * WideRings<MT>::kX + 2 * kWdRing + 4) * 8;
   L.tslot = off;
   off += 16;
   L.total = off + 1024;
@@ -122,16 +127,17 @@ __global__ void __launch_bounds__(kWdThreads, 1)
   const int C = a.C, G = a.G;
   constexpr WideLayout L = wide_layout<MT>();
   constexpr int kXSlot = 2 * MT * 128;
+  constexpr int kWdCodeRing = WideRings<MT>::kCode, kWdXRing = WideRings<MT>::kX;
   const uint32_t code = smem_u32(smem + L.code);
   const uint32_t xs = smem_u32(smem + L.xs);
   uint64_t* cfull = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* cempty = cfull + kWdCodeRing;
   uint64_t* xfull = cempty + kWdCodeRing;
-  uint64_t* xempty = xfull + kWdXRing;
+  uint64_t* xempty = xfull + kWdXRing;  // the MMAs that read the x' slot are done
   uint64_t* afull = xempty + kWdXRing;
-  uint64_t* aempty = afull + kWdRA;
-  uint64_t* dfull = aempty + kWdRA;  // [2]: a segment's accumulator is complete
-  uint64_t* dempty = dfull + 2;      // [2]: it has been read
+  uint64_t* gdone = afull + kWdRing;  // the MMAs that read the A slot are done
+  uint64_t* dfull = gdone + kWdRing;  // [2]: a segment's accumulator is complete
+  uint64_t* dempty = dfull + 2;       // [2]: it has been read
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + L.tslot);
   __shared__ volatile int aborted;
   __shared__ int fin_s;  // this CTA is the last contributor of a shared tile
@@ -146,15 +152,15 @@ __global__ void __launch_bounds__(kWdThreads, 1)
     aborted = 0;
     for (int i = 0; i < kWdCodeRing; ++i) {
       mbar_init(cfull + i, 1);
-      mbar_init(cempty + i, 4);
+      mbar_init(cempty + i, 8);  // every decoder warp reads every box
     }
     for (int i = 0; i < kWdXRing; ++i) {
       mbar_init(xfull + i, 1);
       mbar_init(xempty + i, 1);
     }
-    for (int i = 0; i < kWdRA; ++i) {
-      mbar_init(afull + i, 4);
-      mbar_init(aempty + i, 1);
+    for (int i = 0; i < kWdRing; ++i) {
+      mbar_init(afull + i, 4);  // the four warps of the warpgroup that decodes the group
+      mbar_init(gdone + i, 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(dfull + i, 1);
@@ -167,7 +173,7 @@ __global__ void __launch_bounds__(kWdThreads, 1)
   __syncthreads();
   tmem_fence_after();
   const uint32_t tmem = *tslot;
-  const uint32_t tD0 = tmem + kWdRA * 64;  // accumulators after the A slots
+  const uint32_t tD0 = tmem + kWdRing * 64;  // accumulators after the A slots
 
   auto wait = [&](uint64_t* bar, uint32_t parity) {
     if (aborted) return;
@@ -180,21 +186,26 @@ __global__ void __launch_bounds__(kWdThreads, 1)
   auto seg_end = [&](int unit) { return unit + 1 == hi || (unit + 1) % C == 0; };
 
   if (warp == 0) {
-    // ---- producer: code boxes (never dependent on the previous kernel) first, then x' per group
+    // ---- code producer: the packed weights never depend on the previous kernel
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
-      auto code_box = [&](int n) {
+      for (int n = 0; n < nunits; ++n) {
         const int unit = lo + n, tile = unit / C, chunk = unit - tile * C;
         const int slot = n % kWdCodeRing;
         if (n >= kWdCodeRing) wait(cempty + slot, ((n / kWdCodeRing) - 1) & 1);
         mbar_arrive_expect_tx(cfull + slot, kSlotBytes);
         tma2d(code + slot * kSlotBytes, &cmap, chunk * 32, tile * kUnitRows, cfull + slot, pol);
-      };
-      const int pre = nunits < kWdCodeRing ? nunits : kWdCodeRing;
-      for (int n = 0; n < pre; ++n) code_box(n);
+      }
+      // leave no copy in flight
+      for (int n = nunits - 1; n >= 0 && n >= nunits - kWdCodeRing; --n)
+        if (!mbar_wait(cfull + n % kWdCodeRing, (n / kWdCodeRing) & 1)) set_status(a.status, TB_DEV_TIMEOUT);
+    }
+    __syncwarp();
+  } else if (warp == 10) {
+    // ---- x' producer: two boxes per group, each slot refilled once its MMAs are done
+    if (lane == 0) {
       asm volatile("griddepcontrol.wait;" ::: "memory");  // x' is the previous kernel's output
       for (int n = 0; n < nunits; ++n) {
-        if (n >= pre) code_box(n);
         const int chunk = (lo + n) % C;
 #pragma unroll 1
         for (int g = 0; g < kUnitGroups; ++g) {
@@ -206,9 +217,6 @@ __global__ void __launch_bounds__(kWdThreads, 1)
           tma2d_plain(xs + slot * kXSlot + MT * 128, &xmap, k0 + 64, 0, xfull + slot);
         }
       }
-      // leave no copy in flight
-      for (int n = nunits - 1; n >= 0 && n >= nunits - kWdCodeRing; --n)
-        if (!mbar_wait(cfull + n % kWdCodeRing, (n / kWdCodeRing) & 1)) set_status(a.status, TB_DEV_TIMEOUT);
       const int ni = 4 * nunits;
       for (int i = ni - 1; i >= 0 && i >= ni - kWdXRing; --i)
         if (!mbar_wait(xfull + i % kWdXRing, (i / kWdXRing) & 1)) set_status(a.status, TB_DEV_TIMEOUT);
@@ -226,19 +234,19 @@ __global__ void __launch_bounds__(kWdThreads, 1)
 #pragma unroll 1
         for (int g = 0; g < kUnitGroups; ++g) {
           const int i = 4 * n + g;
-          const int sa = i % kWdRA, sx = i % kWdXRing, sd = seg & 1;
+          const int sl = i % kWdRing, sx = i % kWdXRing, sd = seg & 1;
           if (seg_start && g == 0 && seg >= 2) wait(dempty + sd, ((seg >> 1) - 1) & 1);
-          wait(afull + sa, (i / kWdRA) & 1);
+          wait(afull + sl, (i / kWdRing) & 1);
           wait(xfull + sx, (i / kWdXRing) & 1);
           tmem_fence_after();
           const uint32_t xb = xs + (uint32_t)(sx * kXSlot);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
             const uint32_t baddr = xb + (uint32_t)((kk >> 2) * MT * 128 + (kk & 3) * 32);
-            mma_f16_ts(tD0 + (uint32_t)(sd * MT), tmem + (uint32_t)(sa * 64 + 8 * kk),
+            mma_f16_ts(tD0 + (uint32_t)(sd * MT), tmem + (uint32_t)(sl * 64 + 8 * kk),
                        smem_desc_sw128(baddr, 1024u), idesc, (seg_start && g == 0 && kk == 0) ? 0 : 1);
           }
-          mma_commit(aempty + sa);
+          mma_commit(gdone + sl);
           mma_commit(xempty + sx);
           seg_start = false;
           if (g == kUnitGroups - 1 && seg_end(unit)) {
@@ -252,9 +260,10 @@ __global__ void __launch_bounds__(kWdThreads, 1)
       if (seg > 0 && !mbar_wait(dfull + ((seg - 1) & 1), ((seg - 1) >> 1) & 1)) set_status(a.status, TB_DEV_TIMEOUT);
     }
     __syncwarp();
-  } else {
-    // ---- decoders: thread r = unit row r = tensor-memory lane r
-    const int q = warp & 3;
+  } else if (warp < 10) {
+    // ---- decoders: warpgroup u decodes groups u and u + 2 of every unit; thread r = unit row r
+    // = tensor-memory lane r.  Warpgroup 0 also finishes the tile segments.
+    const int u = (warp - 2) >> 2, q = warp & 3;
     const int r = q * 32 + lane;
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
     const int rsw = r & 7;
@@ -308,10 +317,10 @@ __global__ void __launch_bounds__(kWdThreads, 1)
       float* mine = a.part + ((int64_t)blockIdx.x * 2 + (lo / C == tile ? 0 : 1)) * kUnitRows * MT;
 #pragma unroll
       for (int t = 0; t < MT; ++t) __stcg(mine + t * kUnitRows + r, v[t]);
-      // the four decoder warps' parts, then one count per CTA
+      // the four warps' parts, then one count per CTA
       asm volatile("bar.sync 1, 128;" ::: "memory");
       const int first = wd_owner(tb_, S, gridDim.x), lastc = wd_owner(te - 1, S, gridDim.x);
-      if (threadIdx.x == 64) {  // lane 0 of the first decoder warp
+      if (threadIdx.x == 64) {  // lane 0 of warp 2
         fence_acq_rel_gpu();
         fin_s = atomicAdd(a.count + first, 1) == lastc - first;
       }
@@ -336,35 +345,39 @@ __global__ void __launch_bounds__(kWdThreads, 1)
       if (threadIdx.x == 64) a.count[first] = 0;
     };
 
-    uint2 svc, bvc, svn, bvn;  // this unit's and the next unit's scales and biases
-    load_sb(0, svn, bvn);
+    // scale / bias words of units n, n + 1, n + 2 (loaded two units ahead of their use)
+    uint2 sv0, bv0, sv1, bv1, sv2, bv2;
+    load_sb(0, sv1, bv1);
+    load_sb(1, sv2, bv2);
     int seg = 0, pend_seg = -1, pend_tile = 0;
     bool pend_whole = false;
     for (int n = 0; n < nunits; ++n) {
       const int unit = lo + n, tile = unit / C;
       const int slot = n % kWdCodeRing;
-      svc = svn;
-      bvc = bvn;
-      load_sb(n + 1, svn, bvn);
+      sv0 = sv1;
+      bv0 = bv1;
+      sv1 = sv2;
+      bv1 = bv2;
+      load_sb(n + 2, sv2, bv2);
       wait(cfull + slot, (n / kWdCodeRing) & 1);
       const uint32_t box = code + (uint32_t)slot * kSlotBytes + (uint32_t)r * 128u;
-#pragma unroll 1
-      for (int g = 0; g < kUnitGroups; ++g) {
-        const int i = 4 * n + g, sa = i % kWdRA;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int g = u + 2 * h, i = 4 * n + g, sl = i % kWdRing;
         const uint4 wa = ld_shared_v4(box + ((uint32_t)((2 * g) ^ rsw) << 4));
         const uint4 wb = ld_shared_v4(box + ((uint32_t)((2 * g + 1) ^ rsw) << 4));
-        if (g == kUnitGroups - 1) {  // the box is read
+        if (h == 1) {  // this warp has read the box
           __syncwarp();
           if (lane == 0) mbar_arrive(cempty + slot);
         }
-        const uint32_t sw = g < 2 ? svc.x : svc.y, bw = g < 2 ? bvc.x : bvc.y;
-        const uint16_t sh = (uint16_t)((g & 1) ? sw >> 16 : sw & 0xFFFFu);
-        const uint16_t bh = (uint16_t)((g & 1) ? bw >> 16 : bw & 0xFFFFu);
+        const uint32_t sw = h ? sv0.y : sv0.x, bw = h ? bv0.y : bv0.x;  // groups u, u + 2
+        const uint16_t sh = (uint16_t)(u ? sw >> 16 : sw & 0xFFFFu);
+        const uint16_t bh = (uint16_t)(u ? bw >> 16 : bw & 0xFFFFu);
         const __half2 s2 = __halves2half2(__ushort_as_half(sh), __ushort_as_half(sh));
         const __half2 b2 = __halves2half2(__ushort_as_half(bh), __ushort_as_half(bh));
         const __half2 k1024 = __half2half2(__ushort_as_half(0x6400u));
         const uint32_t wv[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
-        if (i >= kWdRA) wait(aempty + sa, ((i / kWdRA) - 1) & 1);  // its MMAs are done
+        if (i >= kWdRing) wait(gdone + sl, ((i / kWdRing) - 1) & 1);  // its previous MMAs are done
         tmem_fence_after();
 #pragma unroll
         for (int half = 0; half < 2; ++half) {  // 4 words = 64 codes = 32 columns per store
@@ -381,14 +394,14 @@ __global__ void __launch_bounds__(kWdThreads, 1)
               A[8 * jj + p] = *reinterpret_cast<const uint32_t*>(&wh);
             }
           }
-          tmem_st32(tmem + (uint32_t)(sa * 64 + 32 * half) + lane_off, A);
+          tmem_st32(tmem + (uint32_t)(sl * 64 + 32 * half) + lane_off, A);
         }
         tmem_wait_st();
         tmem_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(afull + sa);
+        if (lane == 0) mbar_arrive(afull + sl);
         // the previous segment's accumulator, once this unit's first group is on its way
-        if (g == 0 && pend_seg >= 0) {
+        if (u == 0 && h == 0 && pend_seg >= 0) {
           finish_segment(pend_seg, pend_tile, pend_whole);
           pend_seg = -1;
         }
@@ -401,7 +414,7 @@ __global__ void __launch_bounds__(kWdThreads, 1)
         ++seg;
       }
     }
-    if (pend_seg >= 0) finish_segment(pend_seg, pend_tile, pend_whole);
+    if (u == 0 && pend_seg >= 0) finish_segment(pend_seg, pend_tile, pend_whole);
   }
 
   // every MMA has completed (the issuer waited for its last commit) and every load from tensor
