@@ -108,7 +108,8 @@ struct TcCfg {
   // activations come from HBM), 160 KB for one subtile: the rest of the SM memory stays L1,
   // which the decoders' word loads hit
   static constexpr int kStages = ((NSUB == 2 ? 192 : 160) * 1024) / kStageBytes;
-  static constexpr int kSmem = kStages * kStageBytes + 1024 + 1024;  // stages, barriers, alignment
+  static constexpr int kEpiBytes = 8 * 32 * 64;  // per decoder warp: 32 rows x 32 fp16 of y
+  static constexpr int kSmem = kStages * kStageBytes + 1024 + kEpiBytes + 1024;  // stages, barriers, y staging, alignment
   static constexpr int kTmemCols = NSUB * BN;
   // kind::f16 instruction descriptor: fp16 A and B, fp32 D, both K-major, M = 128, N = BN
   static constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(kTcBM >> 4) << 24);
@@ -130,7 +131,7 @@ struct TcSkArgs {
   int M, N, K, G;
   int tiles_n, nkb;      // tile t = (t / tiles_n) token tile, (t % tiles_n) row tile
   int units;             // tiles * nkb
-  float* part;           // [grid][2][NSUB*128][BN] fp32 parts of split tiles (scratch)
+  float* part;           // [grid][2][BN/4][NSUB*128][4] fp32 parts of split tiles (scratch)
   int* count;            // [tiles] contributions counted (zero before a call and after it)
   int32_t* status;
 };
@@ -144,6 +145,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   using Cfg = TcCfg<NSUB, BN>;
   constexpr int S = Cfg::kStages;
   constexpr int kPartFloats = NSUB * kTcBM * BN;
+  // a part is stored as [BN / 4 column quads][NSUB * 128 rows][4]: the 32 threads of a warp hold
+  // 32 consecutive rows, so each of their 16-byte stores and loads covers 512 contiguous bytes
+  constexpr int kPartRows = NSUB * kTcBM;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -258,6 +262,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int sub = NSUB == 2 ? part : 0;
     const int c0 = NSUB == 2 ? 0 : part * (BN / 2);
     const int lrow = sub * kTcBM + q * 32 + lane;  // token row within the tile
+    const uint32_t epi = smem_u32(smem + S * Cfg::kStageBytes + 1024) + (uint32_t)(warp - 2) * 2048u;
     int it = 0, seg = 0;
     for (int u = lo; u < hi; ++seg) {
       int t, k0, k1;
@@ -364,26 +369,41 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       wait(accum, seg & 1);
       tc_fence_after();
       const bool whole = k0 == 0 && k1 == nkb;
-      const int tok = m0 + lrow;
       constexpr int CW = NSUB == 2 ? BN : BN / 2;  // columns this thread drains
       // 32 accumulator columns (from c) to fp16 y
+      // 32 accumulator columns (from c) of the warp's 32 token rows to fp16 y, staged through
+      // the warp's 2 KB of shared memory so that four lanes write each row's 64 contiguous bytes
+      // (16-byte slot s of row r sits at slot s ^ ((r >> 1) & 3): conflict-free both ways).
+      // Warp-collective: every lane calls it.
       auto store_y = [&](int c, const float (&f)[32]) {
         const int n = n0 + c0 + c;
-        if (tok >= a.M || n >= a.N) return;
-        __half* dst = a.y + (int64_t)tok * a.N + n;
-        if ((a.N % 8) == 0 && n + 32 <= a.N) {
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            uint32_t h[4];
+        for (int v = 0; v < 4; ++v) {
+          uint32_t h[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) h[e] = pack_half2(f[8 * v + 2 * e], f[8 * v + 2 * e + 1]);
-            *reinterpret_cast<uint4*>(dst + 8 * v) = make_uint4(h[0], h[1], h[2], h[3]);
-          }
-        } else {
-#pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (n + e < a.N) dst[e] = __float2half_rn(f[e]);
+          for (int e = 0; e < 4; ++e) h[e] = pack_half2(f[8 * v + 2 * e], f[8 * v + 2 * e + 1]);
+          sts128(epi + (uint32_t)(lane * 4 + (v ^ ((lane >> 1) & 3))) * 16u, h[0], h[1], h[2], h[3]);
         }
+        __syncwarp();
+        const int tok0 = m0 + sub * kTcBM + q * 32;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int r = 8 * i + (lane >> 2), v = lane & 3;
+          const int tk = tok0 + r, col = n + 8 * v;
+          if (tk < a.M && col < a.N) {
+            const uint4 o = ld_shared_v4(epi + (uint32_t)(r * 4 + (v ^ ((r >> 1) & 3))) * 16u);
+            __half* dst = a.y + (int64_t)tk * a.N + col;
+            if ((a.N % 8) == 0 && col + 8 <= a.N) {
+              *reinterpret_cast<uint4*>(dst) = o;
+            } else {
+              const __half* hv = reinterpret_cast<const __half*>(&o);
+#pragma unroll
+              for (int e = 0; e < 8; ++e)
+                if (col + e < a.N) dst[e] = hv[e];
+            }
+          }
+        }
+        __syncwarp();
       };
       auto tmem_cols = [&](int c, float (&f)[32]) {
         uint32_t r[32];
@@ -407,9 +427,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int c = 0; c < CW; c += 32) {
           float f[32];
           tmem_cols(c, f);
-          float4* dst = reinterpret_cast<float4*>(mine + (int64_t)lrow * BN + c0 + c);
+          float4* dst = reinterpret_cast<float4*>(mine) + (int64_t)((c0 + c) / 4) * kPartRows + lrow;
 #pragma unroll
-          for (int v = 0; v < 8; ++v) __stcg(dst + v, make_float4(f[4 * v], f[4 * v + 1], f[4 * v + 2], f[4 * v + 3]));
+          for (int v = 0; v < 8; ++v)
+            __stcg(dst + v * kPartRows, make_float4(f[4 * v], f[4 * v + 1], f[4 * v + 2], f[4 * v + 3]));
         }
         asm volatile("bar.sync 2, 256;" ::: "memory");
         const int first = sk_owner(t * nkb, units, grid);
@@ -427,10 +448,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const int me = (int)blockIdx.x;
           auto load_part = [&](int cc, int c, float4 (&o)[8]) {
             const int slot = sk_lo(cc, units, grid) / nkb == t ? 0 : 1;
-            const float4* op = reinterpret_cast<const float4*>(
-                a.part + ((int64_t)cc * 2 + slot) * kPartFloats + (int64_t)lrow * BN + c0 + c);
+            const float4* op = reinterpret_cast<const float4*>(a.part + ((int64_t)cc * 2 + slot) * kPartFloats) +
+                               (int64_t)((c0 + c) / 4) * kPartRows + lrow;
 #pragma unroll
-            for (int v = 0; v < 8; ++v) o[v] = __ldcg(op + v);
+            for (int v = 0; v < 8; ++v) o[v] = __ldcg(op + v * kPartRows);
           };
           auto add_part = [](float (&f)[32], const float4 (&o)[8]) {
 #pragma unroll

@@ -28,7 +28,9 @@ constexpr int kGroupsOfWarps = 3;                       // unit groups
 constexpr int kWarpsPerUnit = 4;                        // 32 rows each
 constexpr int kTmaConsumers = kGroupsOfWarps * kWarpsPerUnit;
 constexpr int kMaxSlotsPerGroup = 2;  // a deeper ring measured slower: it takes the L1 that the scale and activation loads hit
-constexpr int kPreIssue = 2;        // units per group issued before the activations are loaded
+constexpr int kPreIssue = 1;        // units per group issued before the activations are loaded (two measured
+                                    // 1.8% slower on a 257-call decode step: the activation loads queue
+                                    // behind the weights; none leaves the first weights late)
 constexpr int kCutSlots = 4;        // shared sums of tiles cut by a group or CTA boundary
 constexpr int kScaleStageBytes = 32 * kUnitGroups * 8;  // per warp: 32 rows x 4 groups of fp32 (s, b)
 constexpr uint32_t kMagic1024 = 0x64006400u;
