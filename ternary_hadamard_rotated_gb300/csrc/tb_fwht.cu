@@ -124,6 +124,10 @@ __global__ void __launch_bounds__(kFwhtWarps * 32, kFwhtMinCtas) fwht1024_kernel
 __global__ void __launch_bounds__(kFwhtWarps * 32, kFwhtMinCtas) rotate_pairorder_kernel(
     const __half* __restrict__ x, __half* __restrict__ out, const int8_t* __restrict__ signs,
     int64_t M, int64_t K, int rotate) {
+  // the consumer of x' (tensor-core GEMM or batched-decode GEMV, launched as a programmatic
+  // dependent) may start its set-up and weight decoding now; it reads x' only after
+  // griddepcontrol.wait, i.e. after this grid has completed
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   __shared__ float scratch[kFwhtWarps][kWarpScratchFloats];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const bool odd = lane & 1;

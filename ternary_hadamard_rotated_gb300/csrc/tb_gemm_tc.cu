@@ -27,7 +27,11 @@
 namespace tb {
 
 constexpr int kTcBM = 128, kTcBK = 64;  // token subtile, k per stage
-constexpr int kTcThreads = 320;
+// 12 warps: 0 loads the activations, 1 issues the MMAs, 2-4, 6-8, 10-11 decode the weights and
+// 4-11 drain the accumulator (two per tensor-memory lane quarter, which warp w may read as
+// w % 4).  Warps 5 and 9 only drain, so the MMA warp shares its SM sub-partition (w % 4 == 1)
+// with no decoder: its issue loop sets the k-block rate.
+constexpr int kTcThreads = 384;
 constexpr int kTcABytes = kTcBM * kTcBK * 2;  // 16 KB
 
 // K-major operand in the 128-byte swizzle: 8-row core groups 1024 bytes apart.
@@ -50,6 +54,27 @@ TB_DEVI void tma_load_2d(void* dst, const CUtensorMap* tm, int x, int y, uint64_
       : "memory");
 }
 
+// the same box into the shared memory of every CTA of the cluster in `mask` (same offset), each
+// CTA's barrier at `bar`'s offset receiving the complete_tx of its copy
+TB_DEVI void tma_load_2d_mc(void* dst, const CUtensorMap* tm, int x, int y, uint64_t* bar, uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster "
+      "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"(mask)
+      : "memory");
+}
+
+TB_DEVI uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// every thread of every CTA of the cluster (release / acquire)
+TB_DEVI void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 TB_DEVI void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 TB_DEVI void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
@@ -65,6 +90,16 @@ TB_DEVI void tc_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                    smem_u32(bar))
                : "memory");
+}
+
+// one arrival on the barrier at `bar`'s offset in every CTA of `mask` once this thread's earlier
+// tcgen05 operations are complete
+TB_DEVI void tc_commit_mc(uint64_t* bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_u32(bar)),
+      "h"(mask)
+      : "memory");
 }
 
 TB_DEVI void tc_ld32(uint32_t taddr, uint32_t (&r)[32]) {
@@ -130,7 +165,8 @@ struct TcSkArgs {
   __half* y;             // [M, N]
   int M, N, K, G;
   int tiles_n, nkb;      // tile t = (t / tiles_n) token tile, (t % tiles_n) row tile
-  int units;             // tiles * nkb
+  int tiles_np;          // row tiles per token tile in steps of the cluster size (= tiles_n for one)
+  int units;             // (token tiles * tiles_np) * nkb: the schedule's units are a cluster's
   float* part;           // [grid][2][BN/4][NSUB*128][4] fp32 parts of split tiles (scratch)
   int* count;            // [tiles] contributions counted (zero before a call and after it)
   int32_t* status;
@@ -139,9 +175,14 @@ struct TcSkArgs {
 TB_DEVI int sk_owner(int u, int units, int grid) { return (int)(((int64_t)(u + 1) * grid - 1) / units); }
 TB_DEVI int sk_lo(int c, int units, int grid) { return (int)((int64_t)units * c / grid); }
 
-template <int NSUB, int BN>
+// CS = 1: one CTA per schedule slot.  CS = 2 (two 128-token subtiles): a cluster of two CTAs
+// takes one token tile and k-range on two neighbouring row tiles; each CTA loads one subtile of
+// every activation stage and multicasts it to both, so each SM reads half the activation bytes,
+// and a stage is refilled only when the MMAs of both CTAs have read it.
+template <int NSUB, int BN, int CS>
 __global__ void __launch_bounds__(kTcThreads, 1)
     w2_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const TcSkArgs a) {
+  static_assert(CS == 1 || (CS == 2 && NSUB == 2), "a cluster pair shares two token subtiles");
   using Cfg = TcCfg<NSUB, BN>;
   constexpr int S = Cfg::kStages;
   constexpr int kPartFloats = NSUB * kTcBM * BN;
@@ -153,25 +194,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (base - raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * Cfg::kStageBytes);
-  uint64_t* fullA = bars;
-  uint64_t* fullB = bars + S;
-  uint64_t* empty = bars + 2 * S;
-  uint64_t* accum = bars + 3 * S;      // one phase per segment: its accumulator is complete
-  uint64_t* tfree = bars + 3 * S + 1;  // one phase per segment: its accumulator has been read
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * S + 2);
+  // full[s]: the stage's activations have landed (expect_tx by the producer) and its weights are
+  // decoded (one arrival per decoder warp), so the MMA warp waits once per k-block
+  uint64_t* full = bars;
+  uint64_t* empty = bars + S;
+  uint64_t* accum = bars + 2 * S;      // one phase per segment: its accumulator is complete
+  uint64_t* tfree = bars + 2 * S + 1;  // one phase per segment: its accumulator has been read
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 2);
   __shared__ volatile int aborted;
   __shared__ int last_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nkb = a.nkb, units = a.units, grid = gridDim.x;
-  const int lo = sk_lo(blockIdx.x, units, grid), hi = sk_lo(blockIdx.x + 1, units, grid);
+  const int crank = CS > 1 ? (int)cluster_rank() : 0;  // row tile within the cluster's pair
+  const int cid = (int)blockIdx.x / CS;                 // the schedule works in clusters
+  const int nkb = a.nkb, units = a.units, grid = (int)gridDim.x / CS;
+  const int lo = sk_lo(cid, units, grid), hi = sk_lo(cid + 1, units, grid);
 
   if (threadIdx.x == 0) {
     aborted = 0;
     for (int s = 0; s < S; ++s) {
-      mbar_init(fullA + s, 1);
-      mbar_init(fullB + s, 256);
-      mbar_init(empty + s, 1);
+      mbar_init(full + s, 1 + 8);
+      mbar_init(empty + s, CS);  // the MMAs of every CTA that reads the stage
     }
     mbar_init(accum, 1);
     mbar_init(tfree, 8);  // lane 0 of each of the 8 decoder warps
@@ -186,17 +229,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (CS > 1) cluster_sync();  // the peer's barriers exist before anything lands in them
   tc_fence_after();
   const uint32_t tmem_d = *tmem_slot;
 
   auto wait = [&](uint64_t* bar, uint32_t parity) {
-    if (aborted) return;
+    if (mbar_try_wait(bar, parity) || aborted) return;  // the common case costs one test
     if (!mbar_wait(bar, parity)) {
       aborted = 1;
       set_status(a.status, TB_DEV_TIMEOUT);
     }
   };
-  // segment starting at unit u: tile t, k-blocks [k0, k1)
+  // segment starting at unit u: the cluster's tile t (token tile t / tiles_np), k-blocks [k0, k1)
   auto segment = [&](int u, int& t, int& k0, int& k1) {
     t = u / nkb;
     k0 = u - t * nkb;
@@ -206,21 +250,36 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (warp == 0) {
     if (lane == 0) {
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
+      // x' is the previous kernel's output (programmatic launch): everything before this, and the
+      // decoders' first stages, overlap that kernel's tail
+      asm volatile("griddepcontrol.wait;" ::: "memory");
       int it = 0;
       for (int u = lo; u < hi;) {
         int t, k0, k1;
         segment(u, t, k0, k1);
-        const int m0 = (t / a.tiles_n) * (NSUB * kTcBM);
+        const int m0 = (t / a.tiles_np) * (NSUB * kTcBM);
         for (int kb = k0; kb < k1; ++kb, ++it) {
           const int s = it % S, ph = it / S;
           if (ph > 0) wait(empty + s, (ph - 1) & 1);
-          mbar_arrive_expect_tx(fullA + s, NSUB * kTcABytes);
+          mbar_arrive_expect_tx(full + s, NSUB * kTcABytes);
+          if constexpr (CS == 1) {
 #pragma unroll
-          for (int sub = 0; sub < NSUB; ++sub)
-            tma_load_2d(smem + s * Cfg::kStageBytes + sub * kTcABytes, &tmA, kb * kTcBK,
-                        m0 + sub * kTcBM, fullA + s);
+            for (int sub = 0; sub < NSUB; ++sub)
+              tma_load_2d(smem + s * Cfg::kStageBytes + sub * kTcABytes, &tmA, kb * kTcBK,
+                          m0 + sub * kTcBM, full + s);
+          } else {
+            tma_load_2d_mc(smem + s * Cfg::kStageBytes + crank * kTcABytes, &tmA, kb * kTcBK,
+                           m0 + crank * kTcBM, full + s, (uint16_t)((1u << CS) - 1u));
+          }
         }
         u += k1 - k0;
+      }
+      if constexpr (CS > 1) {
+        // the peer's last commits into this CTA's barriers have landed before the cluster exits
+        for (int s = 0; s < S && s < it; ++s) {
+          const int last = it - 1 - ((it - 1 - s) % S);  // the last k-block that used stage s
+          wait(empty + s, (last / S) & 1);
+        }
       }
     }
     __syncwarp();
@@ -234,8 +293,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc_fence_after();
         for (int kb = k0; kb < k1; ++kb, ++it) {
           const int s = it % S, ph = it / S;
-          wait(fullA + s, ph & 1);
-          wait(fullB + s, ph & 1);
+          wait(full + s, ph & 1);
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + s * Cfg::kStageBytes);
           const uint64_t bd = umma_desc_sw128(sa + NSUB * kTcABytes);
@@ -245,7 +303,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int sub = 0; sub < NSUB; ++sub)
               tc_mma(tmem_d + sub * BN, umma_desc_sw128(sa + sub * kTcABytes) + 2 * k, bd + 2 * k,
                      Cfg::kIdesc, (kb != k0) || (k != 0));
-          tc_commit(empty + s);
+          if constexpr (CS > 1) tc_commit_mc(empty + s, (uint16_t)((1u << CS) - 1u));
+          else tc_commit(empty + s);
         }
         tc_commit(accum);
         u += k1 - k0;
@@ -254,22 +313,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __syncwarp();
   } else {
     // ---- decoders: thread d owns (part of) row n0 + d % BN of the B tile ----
+    const bool is_dec = warp != 5 && warp != 9;
+    const bool is_epi = warp >= 4;
+    const int dt = (warp - 2 - (warp > 5) - (warp > 9)) * 32 + lane;  // decoder thread 0..255
     constexpr int WPT = 4 / Cfg::kThreadsPerRow;  // packed words per thread per k-block
-    const int d = (threadIdx.x - 64) % BN;
-    const int wq = ((threadIdx.x - 64) / BN) * WPT;  // first word of this thread
+    const int d = dt % BN;
+    const int wq = (dt / BN) * WPT;          // first word of this thread
     const int q = warp & 3;                 // TMEM lane quarter this warp may read
-    const int part = (warp - 2) >> 2;       // which half of the columns / which subtile
+    const int part = (warp - 4) >> 2;       // which half of the columns / which subtile
     const int sub = NSUB == 2 ? part : 0;
     const int c0 = NSUB == 2 ? 0 : part * (BN / 2);
     const int lrow = sub * kTcBM + q * 32 + lane;  // token row within the tile
-    const uint32_t epi = smem_u32(smem + S * Cfg::kStageBytes + 1024) + (uint32_t)(warp - 2) * 2048u;
+    const uint32_t epi = smem_u32(smem + S * Cfg::kStageBytes + 1024) + (uint32_t)(warp - 4) * 2048u;
     int it = 0, seg = 0;
     for (int u = lo; u < hi; ++seg) {
       int t, k0, k1;
       segment(u, t, k0, k1);
-      const int n0 = (t % a.tiles_n) * BN, m0 = (t / a.tiles_n) * (NSUB * kTcBM);
+      const int nt = (t % a.tiles_np) * CS + crank;  // this CTA's row tile
+      const bool has_tile = nt < a.tiles_n;           // false: the partner of an odd last row tile
+      const int n0 = nt * BN, m0 = (t / a.tiles_np) * (NSUB * kTcBM);
+      const int tile = (t / a.tiles_np) * a.tiles_n + nt;  // its count slot when split
       const int row = n0 + d;
-      const bool valid = row < a.N;
+      const bool valid = is_dec && row < a.N;  // the drain-only warps load nothing
       const __half* srow = a.scales + (int64_t)(valid ? row : 0) * a.G;
       // no biases given: each is the pack's -scale (the fp16 sign bit flipped), not read
       const bool has_b = a.biases != nullptr;
@@ -327,7 +392,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       uint4 s_cur, b_cur, s_nxt, b_nxt;
       load_sb8(k0 >> 4, s_cur, b_cur);
       load_sb8((k0 >> 4) + 1, s_nxt, b_nxt);
-      for (int kb = k0; kb < k1; ++kb, ++it) {
+      for (int kb = k0; kb < (is_dec ? k1 : k0); ++kb, ++it) {
         const int s = it % S, ph = it / S;
         uint32_t nx4[WPT];
 #pragma unroll
@@ -356,8 +421,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           sts128(bt + (((2 * j) ^ sw) << 4), o[0], o[1], o[2], o[3]);
           sts128(bt + (((2 * j + 1) ^ sw) << 4), o[4], o[5], o[6], o[7]);
         }
-        fence_proxy_async_smem();
-        mbar_arrive(fullB + s);
+        fence_proxy_async_smem();  // this thread's stores, before the warp's arrival
+        __syncwarp();
+        if (lane == 0) mbar_arrive(full + s);
         if ((kb & 15) == 15) {  // the next k-block starts a new block of eight groups
           s_cur = s_nxt;
           b_cur = b_nxt;
@@ -365,142 +431,147 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
       }
 
-      // ---- epilogue of the segment: TMEM -> fp16 y; a split tile goes through the parts ----
-      wait(accum, seg & 1);
-      tc_fence_after();
-      const bool whole = k0 == 0 && k1 == nkb;
-      constexpr int CW = NSUB == 2 ? BN : BN / 2;  // columns this thread drains
-      // 32 accumulator columns (from c) to fp16 y
-      // 32 accumulator columns (from c) of the warp's 32 token rows to fp16 y, staged through
-      // the warp's 2 KB of shared memory so that four lanes write each row's 64 contiguous bytes
-      // (16-byte slot s of row r sits at slot s ^ ((r >> 1) & 3): conflict-free both ways).
-      // Warp-collective: every lane calls it.
-      auto store_y = [&](int c, const float (&f)[32]) {
-        const int n = n0 + c0 + c;
-#pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          uint32_t h[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) h[e] = pack_half2(f[8 * v + 2 * e], f[8 * v + 2 * e + 1]);
-          sts128(epi + (uint32_t)(lane * 4 + (v ^ ((lane >> 1) & 3))) * 16u, h[0], h[1], h[2], h[3]);
-        }
-        __syncwarp();
-        const int tok0 = m0 + sub * kTcBM + q * 32;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int r = 8 * i + (lane >> 2), v = lane & 3;
-          const int tk = tok0 + r, col = n + 8 * v;
-          if (tk < a.M && col < a.N) {
-            const uint4 o = ld_shared_v4(epi + (uint32_t)(r * 4 + (v ^ ((r >> 1) & 3))) * 16u);
-            __half* dst = a.y + (int64_t)tk * a.N + col;
-            if ((a.N % 8) == 0 && col + 8 <= a.N) {
-              *reinterpret_cast<uint4*>(dst) = o;
-            } else {
-              const __half* hv = reinterpret_cast<const __half*>(&o);
-#pragma unroll
-              for (int e = 0; e < 8; ++e)
-                if (col + e < a.N) dst[e] = hv[e];
-            }
+      if (is_epi) {
+        // ---- epilogue of the segment: TMEM -> fp16 y; a split tile goes through the parts ----
+        wait(accum, seg & 1);
+        tc_fence_after();
+        const bool whole = k0 == 0 && k1 == nkb;
+        constexpr int CW = NSUB == 2 ? BN : BN / 2;  // columns this thread drains
+        // 32 accumulator columns (from c) of the warp's 32 token rows to fp16 y, staged through
+        // the warp's 2 KB of shared memory so that four lanes write each row's 64 contiguous bytes
+        // (16-byte slot s of row r sits at slot s ^ ((r >> 1) & 3): conflict-free both ways).
+        // Warp-collective: every lane calls it.
+        auto store_y = [&](int c, const float (&f)[32]) {
+          const int n = n0 + c0 + c;
+  #pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            uint32_t h[4];
+  #pragma unroll
+            for (int e = 0; e < 4; ++e) h[e] = pack_half2(f[8 * v + 2 * e], f[8 * v + 2 * e + 1]);
+            sts128(epi + (uint32_t)(lane * 4 + (v ^ ((lane >> 1) & 3))) * 16u, h[0], h[1], h[2], h[3]);
           }
-        }
-        __syncwarp();
-      };
-      auto tmem_cols = [&](int c, float (&f)[32]) {
-        uint32_t r[32];
-        tc_ld32(tmem_d + ((uint32_t)(q * 32) << 16) + (uint32_t)(sub * BN + c0 + c), r);
-#pragma unroll
-        for (int e = 0; e < 32; ++e) f[e] = __uint_as_float(r[e]);
-      };
-      if (whole) {
-#pragma unroll 1
-        for (int c = 0; c < CW; c += 32) {
-          float f[32];
-          tmem_cols(c, f);
-          store_y(c, f);
-        }
-      } else {
-        // A split tile: each contributor writes its part; the last to count in adds the
-        // parts in CTA order (its own from tensor memory), so the sum does not depend on the
-        // order of arrival, and writes y.
-        float* mine = a.part + ((int64_t)blockIdx.x * 2 + (u == lo ? 0 : 1)) * kPartFloats;
-#pragma unroll 1
-        for (int c = 0; c < CW; c += 32) {
-          float f[32];
-          tmem_cols(c, f);
-          float4* dst = reinterpret_cast<float4*>(mine) + (int64_t)((c0 + c) / 4) * kPartRows + lrow;
-#pragma unroll
-          for (int v = 0; v < 8; ++v)
-            __stcg(dst + v * kPartRows, make_float4(f[4 * v], f[4 * v + 1], f[4 * v + 2], f[4 * v + 3]));
-        }
-        asm volatile("bar.sync 2, 256;" ::: "memory");
-        const int first = sk_owner(t * nkb, units, grid);
-        const int lastc = sk_owner(t * nkb + nkb - 1, units, grid);
-        if (threadIdx.x == 64) {
-          fence_acq_rel_gpu();
-          last_flag = atomicAdd(a.count + t, 1) == lastc - first;
-          if (last_flag) {
-            fence_acq_rel_gpu();
-            a.count[t] = 0;
-          }
-        }
-        asm volatile("bar.sync 2, 256;" ::: "memory");
-        if (last_flag) {
-          const int me = (int)blockIdx.x;
-          auto load_part = [&](int cc, int c, float4 (&o)[8]) {
-            const int slot = sk_lo(cc, units, grid) / nkb == t ? 0 : 1;
-            const float4* op = reinterpret_cast<const float4*>(a.part + ((int64_t)cc * 2 + slot) * kPartFloats) +
-                               (int64_t)((c0 + c) / 4) * kPartRows + lrow;
-#pragma unroll
-            for (int v = 0; v < 8; ++v) o[v] = __ldcg(op + v * kPartRows);
-          };
-          auto add_part = [](float (&f)[32], const float4 (&o)[8]) {
-#pragma unroll
-            for (int v = 0; v < 8; ++v) {
-              f[4 * v] += o[v].x;
-              f[4 * v + 1] += o[v].y;
-              f[4 * v + 2] += o[v].z;
-              f[4 * v + 3] += o[v].w;
-            }
-          };
-#pragma unroll 1
-          for (int c = 0; c < CW; c += 32) {
-            float f[32];
-#pragma unroll
-            for (int e = 0; e < 32; ++e) f[e] = 0.f;
-            // the parts in CTA order, its own from tensor memory; the other contributors' parts
-            // two at a time, both loads in flight together
-            for (int cc = first; cc <= lastc;) {
-              const int o0 = cc == me ? cc + 1 : cc;
-              const int o1 = o0 + 1 == me ? o0 + 2 : o0 + 1;
-              float4 A[8], B[8];
-              if (o0 <= lastc) load_part(o0, c, A);
-              if (o1 <= lastc) load_part(o1, c, B);
-              const int end = o1 < lastc ? o1 : lastc;
-              for (; cc <= end; ++cc) {
-                if (cc == me) {
-                  float m[32];
-                  tmem_cols(c, m);
-#pragma unroll
-                  for (int e = 0; e < 32; ++e) f[e] += m[e];
-                } else {
-                  add_part(f, cc == o0 ? A : B);
-                }
+          __syncwarp();
+          const int tok0 = m0 + sub * kTcBM + q * 32;
+  #pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int r = 8 * i + (lane >> 2), v = lane & 3;
+            const int tk = tok0 + r, col = n + 8 * v;
+            if (tk < a.M && col < a.N) {
+              const uint4 o = ld_shared_v4(epi + (uint32_t)(r * 4 + (v ^ ((r >> 1) & 3))) * 16u);
+              __half* dst = a.y + (int64_t)tk * a.N + col;
+              if ((a.N % 8) == 0 && col + 8 <= a.N) {
+                *reinterpret_cast<uint4*>(dst) = o;
+              } else {
+                const __half* hv = reinterpret_cast<const __half*>(&o);
+  #pragma unroll
+                for (int e = 0; e < 8; ++e)
+                  if (col + e < a.N) dst[e] = hv[e];
               }
             }
+          }
+          __syncwarp();
+        };
+        auto tmem_cols = [&](int c, float (&f)[32]) {
+          uint32_t r[32];
+          tc_ld32(tmem_d + ((uint32_t)(q * 32) << 16) + (uint32_t)(sub * BN + c0 + c), r);
+  #pragma unroll
+          for (int e = 0; e < 32; ++e) f[e] = __uint_as_float(r[e]);
+        };
+        if (!has_tile) {
+          // the partner of an odd last row tile computed zeros: nothing to write
+        } else if (whole) {
+  #pragma unroll 1
+          for (int c = 0; c < CW; c += 32) {
+            float f[32];
+            tmem_cols(c, f);
             store_y(c, f);
           }
+        } else {
+          // A split tile: each contributor writes its part; the last to count in adds the
+          // parts in CTA order (its own from tensor memory), so the sum does not depend on the
+          // order of arrival, and writes y.
+          float* mine = a.part + ((int64_t)blockIdx.x * 2 + (u == lo ? 0 : 1)) * kPartFloats;
+  #pragma unroll 1
+          for (int c = 0; c < CW; c += 32) {
+            float f[32];
+            tmem_cols(c, f);
+            float4* dst = reinterpret_cast<float4*>(mine) + (int64_t)((c0 + c) / 4) * kPartRows + lrow;
+  #pragma unroll
+            for (int v = 0; v < 8; ++v)
+              __stcg(dst + v * kPartRows, make_float4(f[4 * v], f[4 * v + 1], f[4 * v + 2], f[4 * v + 3]));
+          }
+          asm volatile("bar.sync 2, 256;" ::: "memory");
+          const int first = sk_owner(t * nkb, units, grid);
+          const int lastc = sk_owner(t * nkb + nkb - 1, units, grid);
+          if (threadIdx.x == 128) {  // warp 4, lane 0
+            fence_acq_rel_gpu();
+            last_flag = atomicAdd(a.count + tile, 1) == lastc - first;
+            if (last_flag) {
+              fence_acq_rel_gpu();
+              a.count[tile] = 0;
+            }
+          }
+          asm volatile("bar.sync 2, 256;" ::: "memory");
+          if (last_flag) {
+            const int me = cid;  // contributors are counted in clusters; cluster cc's CTA of this row tile
+            auto load_part = [&](int cc, int c, float4 (&o)[8]) {
+              const int slot = sk_lo(cc, units, grid) / nkb == t ? 0 : 1;
+              const float4* op = reinterpret_cast<const float4*>(
+                                     a.part + ((int64_t)(cc * CS + crank) * 2 + slot) * kPartFloats) +
+                                 (int64_t)((c0 + c) / 4) * kPartRows + lrow;
+  #pragma unroll
+              for (int v = 0; v < 8; ++v) o[v] = __ldcg(op + v * kPartRows);
+            };
+            auto add_part = [](float (&f)[32], const float4 (&o)[8]) {
+  #pragma unroll
+              for (int v = 0; v < 8; ++v) {
+                f[4 * v] += o[v].x;
+                f[4 * v + 1] += o[v].y;
+                f[4 * v + 2] += o[v].z;
+                f[4 * v + 3] += o[v].w;
+              }
+            };
+  #pragma unroll 1
+            for (int c = 0; c < CW; c += 32) {
+              float f[32];
+  #pragma unroll
+              for (int e = 0; e < 32; ++e) f[e] = 0.f;
+              // the parts in CTA order, its own from tensor memory; the other contributors' parts
+              // two at a time, both loads in flight together
+              for (int cc = first; cc <= lastc;) {
+                const int o0 = cc == me ? cc + 1 : cc;
+                const int o1 = o0 + 1 == me ? o0 + 2 : o0 + 1;
+                float4 A[8], B[8];
+                if (o0 <= lastc) load_part(o0, c, A);
+                if (o1 <= lastc) load_part(o1, c, B);
+                const int end = o1 < lastc ? o1 : lastc;
+                for (; cc <= end; ++cc) {
+                  if (cc == me) {
+                    float m[32];
+                    tmem_cols(c, m);
+  #pragma unroll
+                    for (int e = 0; e < 32; ++e) f[e] += m[e];
+                  } else {
+                    add_part(f, cc == o0 ? A : B);
+                  }
+                }
+              }
+              store_y(c, f);
+            }
+          }
         }
+        // the accumulator is read: the next segment's first mma may overwrite it
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tfree);
       }
-      // the accumulator is read: the next segment's first mma may overwrite it
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(tfree);
       u += k1 - k0;
     }
   }
 
   tc_fence_before();
   __syncthreads();
+  if constexpr (CS > 1) cluster_sync();  // nothing of the peer's still lands in this CTA
   if (warp == 1) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_d),
@@ -537,6 +608,63 @@ size_t gemm_tc_workspace(int64_t M, int64_t K, int64_t N) {
   return tc_x_bytes(M, K) + tc_count_bytes(M, N) + tc_part_bytes();
 }
 
+template <int NS, int B, int CS>
+static cudaError_t launch_tc(int grid, const CUtensorMap& tm, const TcSkArgs& a, cudaStream_t s) {
+  constexpr int smem = TcCfg<NS, B>::kSmem;
+  cudaError_t e = cudaFuncSetAttribute(w2_gemm_tc_kernel<NS, B, CS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[2];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see griddepcontrol.wait
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  at[1].id = cudaLaunchAttributeClusterDimension;
+  at[1].val.clusterDim.x = CS;
+  at[1].val.clusterDim.y = 1;
+  at[1].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = CS > 1 ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, w2_gemm_tc_kernel<NS, B, CS>, tm, a);
+}
+
+// How many two-CTA clusters of the 256 x 256 kernel can be resident at once on the current
+// device (0: none, or the query failed: the pair schedule is not used).
+static int64_t tc_resident_pairs() {
+  static int cached[64];
+  static bool known[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (known[dev]) return cached[dev];
+  int n = 0;
+  constexpr int smem = TcCfg<2, 256>::kSmem;
+  if (cudaFuncSetAttribute(w2_gemm_tc_kernel<2, 256, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) ==
+      cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2);
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 2;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, w2_gemm_tc_kernel<2, 256, 2>, &cfg) != cudaSuccess) {
+      (void)cudaGetLastError();
+      n = 0;
+    }
+  } else {
+    (void)cudaGetLastError();
+  }
+  cached[dev] = n;
+  known[dev] = true;
+  return n;
+}
+
 // the GEMM alone, on x' already rotated into pair order in xp (fp16 [M, K]); `gws` is the
 // workspace after x' (counts, then parts)
 int launch_gemm_tc_rotated(const __half* xp, int64_t M, int64_t K, const uint32_t* w,
@@ -559,9 +687,11 @@ int launch_gemm_tc_rotated(const __half* xp, int64_t M, int64_t K, const uint32_
 
   // Tile shape and schedule.  Above 128 tokens: 256 x 256 tiles (two 128-token subtiles share
   // each decoded weight tile, which halves the decode work and the activation reads per flop
-  // of smaller tiles; the per-k-block decode then hides behind the k-block's mma), as stream-K
-  // over the SMs when every SM gets a tile, one CTA per tile when the tiles fill most of the
-  // SMs, else every tile split into q <= 4 k-ranges.  Up to 128 tokens: 128 x 256 tiles the
+  // of smaller tiles; the per-k-block decode then hides behind the k-block's mma), taken by
+  // clusters of two CTAs on neighbouring row tiles that share each activation stage (one
+  // multicast load per CTA) when pairs can be resident; as stream-K over the resident slots
+  // (CTAs or pairs) when every slot gets a tile, one slot per tile when the tiles fill most of
+  // the slots, else every tile split into q <= 4 k-ranges.  Up to 128 tokens: 128 x 256 tiles the
   // same way, or 128 x 128 tiles when those keep more SMs busy (the cost of a k-block grows with
   // the tile's rows, so the count of SMs in use sets the time when tokens are few).
   DeviceFacts f;
@@ -570,15 +700,19 @@ int launch_gemm_tc_rotated(const __half* xp, int64_t M, int64_t K, const uint32_
   if (f.sms > 256) return TB_ERR_TOO_LARGE;
   const int64_t sms = f.sms;
   auto tiles = [&](int ns, int b) { return ((M + ns * kTcBM - 1) / (ns * kTcBM)) * ((N + b - 1) / b); };
-  int nsub = 1, bn = 256;
-  int64_t grid64 = 0;  // 0: one CTA per tile
+  int nsub = 1, bn = 256, cs = 1;
+  int64_t grid64 = 0;  // in schedule slots (clusters of cs CTAs); 0: one slot per tile
   const int64_t full = sms * 4 / 5;
   const int64_t nkb0 = K / kTcBK;  // a split never leaves a CTA without a k-block
+  const int64_t tiles_n = (N + 255) / 256;
   if (M > kTcBM) {
     nsub = 2;
-    const int64_t T2 = tiles(2, 256);
-    if (T2 >= sms) grid64 = sms;                            // stream-K, two CTAs per tile at most
-    else if (T2 < full) grid64 = T2 * std::min<int64_t>(std::min<int64_t>(4, nkb0), sms / T2);
+    const int64_t pairs = tiles_n >= 2 ? tc_resident_pairs() : 0;
+    cs = pairs > 0 ? 2 : 1;
+    const int64_t slots = cs == 2 ? pairs : sms;
+    const int64_t T2 = ((M + 2 * kTcBM - 1) / (2 * kTcBM)) * ((tiles_n + cs - 1) / cs);
+    if (T2 >= slots) grid64 = slots;  // stream-K, two slots per tile at most
+    else if (T2 < slots * 4 / 5) grid64 = T2 * std::min<int64_t>(std::min<int64_t>(4, nkb0), slots / T2);
   } else if (tiles(1, 256) >= sms) { grid64 = sms; }
   else if (tiles(1, 256) >= full) {}
   else {  // few tiles: the tile width (256 or 128 rows, split into q <= 4 k-ranges, or one CTA
@@ -594,10 +728,11 @@ int launch_gemm_tc_rotated(const __half* xp, int64_t M, int64_t K, const uint32_
       grid64 = g256;
     }
   }
-  const int64_t T = tiles(nsub, bn);
+  const int64_t tn = (N + bn - 1) / bn, tnp = (tn + cs - 1) / cs;
+  const int64_t T = ((M + nsub * kTcBM - 1) / (nsub * kTcBM)) * tnp;  // schedule tiles
   const int64_t nkb = K / kTcBK;
   if (T * nkb > 0x7fffffffLL) return TB_ERR_SHAPE;
-  const int grid = (int)(grid64 ? grid64 : T);
+  const int grid = (int)((grid64 ? grid64 : T) * cs);
   TcSkArgs a;
   a.w = w;
   a.scales = scales;
@@ -607,24 +742,18 @@ int launch_gemm_tc_rotated(const __half* xp, int64_t M, int64_t K, const uint32_
   a.N = (int)N;
   a.K = (int)K;
   a.G = (int)(K / kGroup);
-  a.tiles_n = (int)((N + bn - 1) / bn);
+  a.tiles_n = (int)tn;
+  a.tiles_np = (int)tnp;
   a.nkb = (int)nkb;
   a.units = (int)(T * nkb);
   a.count = static_cast<int*>(gws);
   a.part = reinterpret_cast<float*>(static_cast<char*>(gws) + tc_count_bytes(M, N));
   a.status = status;
-  cudaError_t e = cudaSuccess;
-#define TB_LAUNCH_TC(NS, B)                                                                        \
-  do {                                                                                            \
-    e = cudaFuncSetAttribute(w2_gemm_tc_kernel<NS, B>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
-                             TcCfg<NS, B>::kSmem);                                                 \
-    if (e == cudaSuccess) w2_gemm_tc_kernel<NS, B><<<grid, kTcThreads, TcCfg<NS, B>::kSmem, s>>>(tm, a); \
-  } while (0)
-  if (nsub == 2 && bn == 256) TB_LAUNCH_TC(2, 256);
-  else if (nsub == 2) TB_LAUNCH_TC(2, 128);
-  else if (bn == 256) TB_LAUNCH_TC(1, 256);
-  else TB_LAUNCH_TC(1, 128);
-#undef TB_LAUNCH_TC
+  cudaError_t e;
+  if (nsub == 2 && cs == 2) e = launch_tc<2, 256, 2>(grid, tm, a, s);
+  else if (nsub == 2) e = launch_tc<2, 256, 1>(grid, tm, a, s);
+  else if (bn == 256) e = launch_tc<1, 256, 1>(grid, tm, a, s);
+  else e = launch_tc<1, 128, 1>(grid, tm, a, s);
   if (e != cudaSuccess) {
     record_cuda_error(e);
     return TB_ERR_CUDA;
