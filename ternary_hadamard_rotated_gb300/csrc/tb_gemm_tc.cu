@@ -143,8 +143,12 @@ struct TcCfg {
   // activations come from HBM), 160 KB for one subtile: the rest of the SM memory stays L1,
   // which the decoders' word loads hit
   static constexpr int kStages = ((NSUB == 2 ? 192 : 160) * 1024) / kStageBytes;
-  static constexpr int kEpiBytes = 8 * 32 * 64;  // per decoder warp: 32 rows x 32 fp16 of y
-  static constexpr int kSmem = kStages * kStageBytes + 1024 + kEpiBytes + 1024;  // stages, barriers, y staging, alignment
+  static constexpr int kEpiBytes = 8 * 32 * 64;  // per drain warp: 32 rows x 32 fp16 of y
+  // packed words of one k-block (BN rows x 16 bytes) per slot, loaded by TMA four k-blocks ahead
+  static constexpr int kWSlots = 4;
+  static constexpr int kWBytes = BN * 16;
+  static constexpr int kSmem = kStages * kStageBytes + 1024 + kEpiBytes + kWSlots * kWBytes + 1024;
+  // stages, barriers, y staging, word ring, alignment
   static constexpr int kTmemCols = NSUB * BN;
   // kind::f16 instruction descriptor: fp16 A and B, fp32 D, both K-major, M = 128, N = BN
   static constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(kTcBM >> 4) << 24);
@@ -181,7 +185,8 @@ TB_DEVI int sk_lo(int c, int units, int grid) { return (int)((int64_t)units * c 
 // and a stage is refilled only when the MMAs of both CTAs have read it.
 template <int NSUB, int BN, int CS>
 __global__ void __launch_bounds__(kTcThreads, 1)
-    w2_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const TcSkArgs a) {
+    w2_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
+                      const TcSkArgs a) {
   static_assert(CS == 1 || (CS == 2 && NSUB == 2), "a cluster pair shares two token subtiles");
   using Cfg = TcCfg<NSUB, BN>;
   constexpr int S = Cfg::kStages;
@@ -201,6 +206,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint64_t* accum = bars + 2 * S;      // one phase per segment: its accumulator is complete
   uint64_t* tfree = bars + 2 * S + 1;  // one phase per segment: its accumulator has been read
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 2);
+  // word ring: wfull[j % 4] when k-block j's packed words have landed, wempty when every decoder
+  // warp has read them
+  constexpr int kWS = Cfg::kWSlots;
+  uint64_t* wfull = bars + 2 * S + 3;
+  uint64_t* wempty = wfull + kWS;
+  uint8_t* wring = smem + S * Cfg::kStageBytes + 1024 + Cfg::kEpiBytes;
   __shared__ volatile int aborted;
   __shared__ int last_flag;
 
@@ -217,7 +228,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(empty + s, CS);  // the MMAs of every CTA that reads the stage
     }
     mbar_init(accum, 1);
-    mbar_init(tfree, 8);  // lane 0 of each of the 8 decoder warps
+    mbar_init(tfree, 8);  // lane 0 of each of the 8 drain warps
+    for (int i = 0; i < kWS; ++i) {
+      mbar_init(wfull + i, 1);
+      mbar_init(wempty + i, 8);  // lane 0 of each decoder warp
+    }
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -250,6 +265,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (warp == 0) {
     if (lane == 0) {
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmW)) : "memory");
+      // the packed words of the CTA's k-block j (unit lo + j): its row tile's 16 bytes per row
+      const int nblk = hi - lo;
+      auto issue_words = [&](int j) {
+        const int u = lo + j, tt = u / nkb, kb = u - tt * nkb;
+        const int nt = (tt % a.tiles_np) * CS + crank;
+        const int sl = j % kWS;
+        mbar_arrive_expect_tx(wfull + sl, Cfg::kWBytes);
+        tma_load_2d(wring + sl * Cfg::kWBytes, &tmW, kb * 4, nt * BN, wfull + sl);
+      };
+      for (int j = 0; j < kWS && j < nblk; ++j) issue_words(j);  // the weights need no wait
       // x' is the previous kernel's output (programmatic launch): everything before this, and the
       // decoders' first stages, overlap that kernel's tail
       asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -270,6 +296,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           } else {
             tma_load_2d_mc(smem + s * Cfg::kStageBytes + crank * kTcABytes, &tmA, kb * kTcBK,
                            m0 + crank * kTcBM, full + s, (uint16_t)((1u << CS) - 1u));
+          }
+          const int jw = it + kWS;  // the words four k-blocks ahead, once their slot is read
+          if (jw < nblk) {
+            wait(wempty + jw % kWS, (jw / kWS - 1) & 1);
+            issue_words(jw);
           }
         }
         u += k1 - k0;
@@ -366,49 +397,31 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const uint32_t w2 = (g >> 2) ? ((g >> 1) & 1 ? v.w : v.z) : ((g >> 1) & 1 ? v.y : v.x);
         return __ushort_as_half((uint16_t)((g & 1) ? (w2 >> 16) : (w2 & 0xFFFFu)));
       };
-      const uint4* wrow = reinterpret_cast<const uint4*>(a.w + (int64_t)(valid ? row : 0) * (a.K / 16));
-      const uint32_t* wrow32 = reinterpret_cast<const uint32_t*>(wrow) + wq;
-      auto load_words = [&](int kb, uint32_t (&wv)[WPT]) {
-        if constexpr (WPT == 4) {
-          const uint4 v = __ldg(wrow + kb);
-          wv[0] = v.x;
-          wv[1] = v.y;
-          wv[2] = v.z;
-          wv[3] = v.w;
-        } else {
-          const uint2 v = __ldg(reinterpret_cast<const uint2*>(wrow32 + kb * 4));
-          wv[0] = v.x;
-          wv[1] = v.y;
-        }
-      };
-      // packed words four k-blocks ahead (the loads go to HBM when the weights are read once)
-      uint32_t cur[WPT], nx1[WPT], nx2[WPT], nx3[WPT];
-#pragma unroll
-      for (int j = 0; j < WPT; ++j) cur[j] = nx1[j] = nx2[j] = nx3[j] = 0;
-      if (valid) load_words(k0, cur);
-      if (valid && k0 + 1 < k1) load_words(k0 + 1, nx1);
-      if (valid && k0 + 2 < k1) load_words(k0 + 2, nx2);
-      if (valid && k0 + 3 < k1) load_words(k0 + 3, nx3);
       uint4 s_cur, b_cur, s_nxt, b_nxt;
       load_sb8(k0 >> 4, s_cur, b_cur);
       load_sb8((k0 >> 4) + 1, s_nxt, b_nxt);
       for (int kb = k0; kb < (is_dec ? k1 : k0); ++kb, ++it) {
         const int s = it % S, ph = it / S;
-        uint32_t nx4[WPT];
-#pragma unroll
-        for (int j = 0; j < WPT; ++j) nx4[j] = 0;
-        if (valid && kb + 4 < k1) load_words(kb + 4, nx4);
+        // this row's packed words of the k-block from the word ring (rows past N are zeros)
+        const int wsl = it % kWS;
+        wait(wfull + wsl, (it / kWS) & 1);
+        uint32_t wv[WPT];
+        const uint32_t wa = smem_u32(wring + wsl * Cfg::kWBytes) + (uint32_t)(d * 16 + wq * 4);
+        if constexpr (WPT == 4) {
+          const uint4 v = ld_shared_v4(wa);
+          wv[0] = v.x;
+          wv[1] = v.y;
+          wv[2] = v.z;
+          wv[3] = v.w;
+        } else {
+          const uint2 v = ld_shared_v2(wa);
+          wv[0] = v.x;
+          wv[1] = v.y;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(wempty + wsl);
         if (ph > 0) wait(empty + s, (ph - 1) & 1);
         const uint32_t stage = smem_u32(smem + s * Cfg::kStageBytes);
-        uint32_t wv[WPT];
-#pragma unroll
-        for (int j = 0; j < WPT; ++j) {
-          wv[j] = cur[j];
-          cur[j] = nx1[j];
-          nx1[j] = nx2[j];
-          nx2[j] = nx3[j];
-          nx3[j] = nx4[j];
-        }
         const int g = (kb >> 1) & 7;
         const __half sv = pick(s_cur, g), bv = pick(b_cur, g);
         const uint32_t bt = stage + NSUB * kTcABytes + d * 128;
@@ -443,16 +456,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // Warp-collective: every lane calls it.
         auto store_y = [&](int c, const float (&f)[32]) {
           const int n = n0 + c0 + c;
-  #pragma unroll
+#pragma unroll
           for (int v = 0; v < 4; ++v) {
             uint32_t h[4];
-  #pragma unroll
+#pragma unroll
             for (int e = 0; e < 4; ++e) h[e] = pack_half2(f[8 * v + 2 * e], f[8 * v + 2 * e + 1]);
             sts128(epi + (uint32_t)(lane * 4 + (v ^ ((lane >> 1) & 3))) * 16u, h[0], h[1], h[2], h[3]);
           }
           __syncwarp();
           const int tok0 = m0 + sub * kTcBM + q * 32;
-  #pragma unroll
+#pragma unroll
           for (int i = 0; i < 4; ++i) {
             const int r = 8 * i + (lane >> 2), v = lane & 3;
             const int tk = tok0 + r, col = n + 8 * v;
@@ -463,7 +476,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 *reinterpret_cast<uint4*>(dst) = o;
               } else {
                 const __half* hv = reinterpret_cast<const __half*>(&o);
-  #pragma unroll
+#pragma unroll
                 for (int e = 0; e < 8; ++e)
                   if (col + e < a.N) dst[e] = hv[e];
               }
@@ -474,13 +487,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         auto tmem_cols = [&](int c, float (&f)[32]) {
           uint32_t r[32];
           tc_ld32(tmem_d + ((uint32_t)(q * 32) << 16) + (uint32_t)(sub * BN + c0 + c), r);
-  #pragma unroll
+#pragma unroll
           for (int e = 0; e < 32; ++e) f[e] = __uint_as_float(r[e]);
         };
         if (!has_tile) {
           // the partner of an odd last row tile computed zeros: nothing to write
         } else if (whole) {
-  #pragma unroll 1
+#pragma unroll 1
           for (int c = 0; c < CW; c += 32) {
             float f[32];
             tmem_cols(c, f);
@@ -491,12 +504,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           // parts in CTA order (its own from tensor memory), so the sum does not depend on the
           // order of arrival, and writes y.
           float* mine = a.part + ((int64_t)blockIdx.x * 2 + (u == lo ? 0 : 1)) * kPartFloats;
-  #pragma unroll 1
+#pragma unroll 1
           for (int c = 0; c < CW; c += 32) {
             float f[32];
             tmem_cols(c, f);
             float4* dst = reinterpret_cast<float4*>(mine) + (int64_t)((c0 + c) / 4) * kPartRows + lrow;
-  #pragma unroll
+#pragma unroll
             for (int v = 0; v < 8; ++v)
               __stcg(dst + v * kPartRows, make_float4(f[4 * v], f[4 * v + 1], f[4 * v + 2], f[4 * v + 3]));
           }
@@ -519,11 +532,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               const float4* op = reinterpret_cast<const float4*>(
                                      a.part + ((int64_t)(cc * CS + crank) * 2 + slot) * kPartFloats) +
                                  (int64_t)((c0 + c) / 4) * kPartRows + lrow;
-  #pragma unroll
+#pragma unroll
               for (int v = 0; v < 8; ++v) o[v] = __ldcg(op + v * kPartRows);
             };
             auto add_part = [](float (&f)[32], const float4 (&o)[8]) {
-  #pragma unroll
+#pragma unroll
               for (int v = 0; v < 8; ++v) {
                 f[4 * v] += o[v].x;
                 f[4 * v + 1] += o[v].y;
@@ -531,29 +544,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 f[4 * v + 3] += o[v].w;
               }
             };
-  #pragma unroll 1
+#pragma unroll 1
             for (int c = 0; c < CW; c += 32) {
               float f[32];
-  #pragma unroll
+#pragma unroll
               for (int e = 0; e < 32; ++e) f[e] = 0.f;
-              // the parts in CTA order, its own from tensor memory; the other contributors' parts
-              // two at a time, both loads in flight together
-              for (int cc = first; cc <= lastc;) {
-                const int o0 = cc == me ? cc + 1 : cc;
-                const int o1 = o0 + 1 == me ? o0 + 2 : o0 + 1;
-                float4 A[8], B[8];
-                if (o0 <= lastc) load_part(o0, c, A);
-                if (o1 <= lastc) load_part(o1, c, B);
-                const int end = o1 < lastc ? o1 : lastc;
-                for (; cc <= end; ++cc) {
-                  if (cc == me) {
-                    float m[32];
-                    tmem_cols(c, m);
-  #pragma unroll
-                    for (int e = 0; e < 32; ++e) f[e] += m[e];
-                  } else {
-                    add_part(f, cc == o0 ? A : B);
-                  }
+              // the parts in CTA order, its own from tensor memory (one part in flight: two measured
+              // no faster and hold 30 more registers across the whole kernel)
+              for (int cc = first; cc <= lastc; ++cc) {
+                if (cc == me) {
+                  float m[32];
+                  tmem_cols(c, m);
+#pragma unroll
+                  for (int e = 0; e < 32; ++e) f[e] += m[e];
+                } else {
+                  float4 A[8];
+                  load_part(cc, c, A);
+                  add_part(f, A);
                 }
               }
               store_y(c, f);
@@ -609,7 +616,8 @@ size_t gemm_tc_workspace(int64_t M, int64_t K, int64_t N) {
 }
 
 template <int NS, int B, int CS>
-static cudaError_t launch_tc(int grid, const CUtensorMap& tm, const TcSkArgs& a, cudaStream_t s) {
+static cudaError_t launch_tc(int grid, const CUtensorMap& tm, const CUtensorMap& tw, const TcSkArgs& a,
+                             cudaStream_t s) {
   constexpr int smem = TcCfg<NS, B>::kSmem;
   cudaError_t e = cudaFuncSetAttribute(w2_gemm_tc_kernel<NS, B, CS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
@@ -627,7 +635,7 @@ static cudaError_t launch_tc(int grid, const CUtensorMap& tm, const TcSkArgs& a,
   at[1].val.clusterDim.z = 1;
   cfg.attrs = at;
   cfg.numAttrs = CS > 1 ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, w2_gemm_tc_kernel<NS, B, CS>, tm, a);
+  return cudaLaunchKernelEx(&cfg, w2_gemm_tc_kernel<NS, B, CS>, tm, tw, a);
 }
 
 // How many two-CTA clusters of the 256 x 256 kernel can be resident at once on the current
@@ -749,11 +757,22 @@ int launch_gemm_tc_rotated(const __half* xp, int64_t M, int64_t K, const uint32_
   a.count = static_cast<int*>(gws);
   a.part = reinterpret_cast<float*>(static_cast<char*>(gws) + tc_count_bytes(M, N));
   a.status = status;
+  // the packed words [N][K/16] as a 2-D tensor: one box = one k-block (4 words) of bn rows
+  CUtensorMap tw;
+  {
+    const cuuint64_t wd[2] = {(cuuint64_t)(K / 16), (cuuint64_t)N};
+    const cuuint64_t wst[1] = {(cuuint64_t)(K / 16) * 4};
+    const cuuint32_t wbox[2] = {4, (cuuint32_t)bn};
+    cr = encode(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t*>(w), wd, wst, wbox, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (cr != CUDA_SUCCESS) return TB_ERR_CUDA;
+  }
   cudaError_t e;
-  if (nsub == 2 && cs == 2) e = launch_tc<2, 256, 2>(grid, tm, a, s);
-  else if (nsub == 2) e = launch_tc<2, 256, 1>(grid, tm, a, s);
-  else if (bn == 256) e = launch_tc<1, 256, 1>(grid, tm, a, s);
-  else e = launch_tc<1, 128, 1>(grid, tm, a, s);
+  if (nsub == 2 && cs == 2) e = launch_tc<2, 256, 2>(grid, tm, tw, a, s);
+  else if (nsub == 2) e = launch_tc<2, 256, 1>(grid, tm, tw, a, s);
+  else if (bn == 256) e = launch_tc<1, 256, 1>(grid, tm, tw, a, s);
+  else e = launch_tc<1, 128, 1>(grid, tm, tw, a, s);
   if (e != cudaSuccess) {
     record_cuda_error(e);
     return TB_ERR_CUDA;
