@@ -513,6 +513,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int v = 0; v < 8; ++v)
               __stcg(dst + v * kPartRows, make_float4(f[4 * v], f[4 * v + 1], f[4 * v + 2], f[4 * v + 3]));
           }
+          // every writer fences its own stores: the barrier orders them only within the CTA
+          fence_acq_rel_gpu();
           asm volatile("bar.sync 2, 256;" ::: "memory");
           const int first = sk_owner(t * nkb, units, grid);
           const int lastc = sk_owner(t * nkb + nkb - 1, units, grid);
@@ -526,6 +528,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
           asm volatile("bar.sync 2, 256;" ::: "memory");
           if (last_flag) {
+            fence_acq_rel_gpu();  // each reader's acquire of the counted parts
             const int me = cid;  // contributors are counted in clusters; cluster cc's CTA of this row tile
             auto load_part = [&](int cc, int c, float4 (&o)[8]) {
               const int slot = sk_lo(cc, units, grid) / nkb == t ? 0 : 1;

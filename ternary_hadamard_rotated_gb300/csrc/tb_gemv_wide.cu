@@ -317,11 +317,12 @@ __global__ void __launch_bounds__(kWdThreads, 1)
       float* mine = a.part + ((int64_t)blockIdx.x * 2 + (lo / C == tile ? 0 : 1)) * kUnitRows * MT;
 #pragma unroll
       for (int t = 0; t < MT; ++t) __stcg(mine + t * kUnitRows + r, v[t]);
-      // the four warps' parts, then one count per CTA
+      // the four warps' parts, then one count per CTA: every writer fences its own stores (the
+      // barrier orders them only within the CTA)
+      fence_acq_rel_gpu();
       asm volatile("bar.sync 1, 128;" ::: "memory");
       const int first = wd_owner(tb_, S, gridDim.x), lastc = wd_owner(te - 1, S, gridDim.x);
       if (threadIdx.x == 64) {  // lane 0 of warp 2
-        fence_acq_rel_gpu();
         fin_s = atomicAdd(a.count + first, 1) == lastc - first;
       }
       asm volatile("bar.sync 1, 128;" ::: "memory");
