@@ -418,8 +418,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           wv[0] = v.x;
           wv[1] = v.y;
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(wempty + wsl);
         if (ph > 0) wait(empty + s, (ph - 1) & 1);
         const uint32_t stage = smem_u32(smem + s * Cfg::kStageBytes);
         const int g = (kb >> 1) & 7;
@@ -434,9 +432,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           sts128(bt + (((2 * j) ^ sw) << 4), o[0], o[1], o[2], o[3]);
           sts128(bt + (((2 * j + 1) ^ sw) << 4), o[4], o[5], o[6], o[7]);
         }
-        fence_proxy_async_smem();  // this thread's stores, before the warp's arrival
+        // this thread's stores before the tensor core reads them, and its reads of the word slot
+        // before the copy engine refills it (generic accesses, then async-proxy ones)
+        fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(full + s);
+        if (lane == 0) {
+          mbar_arrive(full + s);
+          mbar_arrive(wempty + wsl);
+        }
         if ((kb & 15) == 15) {  // the next k-block starts a new block of eight groups
           s_cur = s_nxt;
           b_cur = b_nxt;

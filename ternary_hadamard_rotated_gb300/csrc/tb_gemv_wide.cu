@@ -367,7 +367,8 @@ __global__ void __launch_bounds__(kWdThreads, 1)
         const int g = u + 2 * h, i = 4 * n + g, sl = i % kWdRing;
         const uint4 wa = ld_shared_v4(box + ((uint32_t)((2 * g) ^ rsw) << 4));
         const uint4 wb = ld_shared_v4(box + ((uint32_t)((2 * g + 1) ^ rsw) << 4));
-        if (h == 1) {  // this warp has read the box
+        if (h == 1) {  // this warp has read the box: its loads before the copy that refills it
+          fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) mbar_arrive(cempty + slot);
         }
