@@ -172,7 +172,9 @@ struct TcSkArgs {
   int tiles_np;          // row tiles per token tile in steps of the cluster size (= tiles_n for one)
   int units;             // (token tiles * tiles_np) * nkb: the schedule's units are a cluster's
   float* part;           // [grid][2][BN/4][NSUB*128][4] fp32 parts of split tiles (scratch)
-  int* count;            // [tiles] contributions counted (zero before a call and after it)
+  int* count;            // [tiles] claims of split tiles, then at done_off [tiles] parts written
+                         // (both zero before a call and after it)
+  int done_off;
   int32_t* status;
 };
 
@@ -212,6 +214,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint64_t* wfull = bars + 2 * S + 3;
   uint64_t* wempty = wfull + kWS;
   uint8_t* wring = smem + S * Cfg::kStageBytes + 1024 + Cfg::kEpiBytes;
+  // the split-tile fixup of a CTA's last segment streams the other parts through the idle stage
+  // ring: six 32 KB slots, filled by bulk copies (pfull) and released by the eight drain warps
+  constexpr int kFixSlots = 6;
+  constexpr bool kBulkFix = NSUB == 2 && BN == 256;
+  static_assert(!kBulkFix || kFixSlots * 32 * 2 * kTcBM * 4 <= S * Cfg::kStageBytes, "fixup slots fit the ring");
+  uint64_t* pfull = wempty + kWS;
+  uint64_t* pempty = pfull + kFixSlots;
   __shared__ volatile int aborted;
   __shared__ int last_flag;
 
@@ -232,6 +241,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     for (int i = 0; i < kWS; ++i) {
       mbar_init(wfull + i, 1);
       mbar_init(wempty + i, 8);  // lane 0 of each decoder warp
+    }
+    for (int i = 0; i < kFixSlots; ++i) {
+      mbar_init(pfull + i, 1);
+      mbar_init(pempty + i, 8);  // lane 0 of each drain warp
     }
     fence_barrier_init();
   }
@@ -503,73 +516,145 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             store_y(c, f);
           }
         } else {
-          // A split tile: each contributor writes its part; the last to count in adds the
-          // parts in CTA order (its own from tensor memory), so the sum does not depend on the
-          // order of arrival, and writes y.
-          float* mine = a.part + ((int64_t)blockIdx.x * 2 + (u == lo ? 0 : 1)) * kPartFloats;
-#pragma unroll 1
-          for (int c = 0; c < CW; c += 32) {
-            float f[32];
-            tmem_cols(c, f);
-            float4* dst = reinterpret_cast<float4*>(mine) + (int64_t)((c0 + c) / 4) * kPartRows + lrow;
-#pragma unroll
-            for (int v = 0; v < 8; ++v)
-              __stcg(dst + v * kPartRows, make_float4(f[4 * v], f[4 * v + 1], f[4 * v + 2], f[4 * v + 3]));
-          }
-          // every writer fences its own stores: the barrier orders them only within the CTA
-          fence_acq_rel_gpu();
-          asm volatile("bar.sync 2, 256;" ::: "memory");
+          // A split tile: each contributor claims a turn as its accumulator completes.  The last
+          // to claim adds the parts in CTA order (its own from tensor memory, never written out),
+          // so the sum does not depend on the order of arrival, and writes y; the others write
+          // their parts and count them done.  The last claimer waits only for CTAs that claimed
+          // before it: those are running and have nothing left to do but write their parts.
           const int first = sk_owner(t * nkb, units, grid);
           const int lastc = sk_owner(t * nkb + nkb - 1, units, grid);
-          if (threadIdx.x == 128) {  // warp 4, lane 0
-            fence_acq_rel_gpu();
-            last_flag = atomicAdd(a.count + tile, 1) == lastc - first;
-            if (last_flag) {
-              fence_acq_rel_gpu();
-              a.count[tile] = 0;
-            }
-          }
+          int* done = a.count + a.done_off + tile;
+          if (threadIdx.x == 128) last_flag = atomicAdd(a.count + tile, 1) == lastc - first;  // warp 4, lane 0
           asm volatile("bar.sync 2, 256;" ::: "memory");
-          if (last_flag) {
-            fence_acq_rel_gpu();  // each reader's acquire of the counted parts
-            const int me = cid;  // contributors are counted in clusters; cluster cc's CTA of this row tile
-            auto load_part = [&](int cc, int c, float4 (&o)[8]) {
-              const int slot = sk_lo(cc, units, grid) / nkb == t ? 0 : 1;
-              const float4* op = reinterpret_cast<const float4*>(
-                                     a.part + ((int64_t)(cc * CS + crank) * 2 + slot) * kPartFloats) +
-                                 (int64_t)((c0 + c) / 4) * kPartRows + lrow;
-#pragma unroll
-              for (int v = 0; v < 8; ++v) o[v] = __ldcg(op + v * kPartRows);
-            };
-            auto add_part = [](float (&f)[32], const float4 (&o)[8]) {
-#pragma unroll
-              for (int v = 0; v < 8; ++v) {
-                f[4 * v] += o[v].x;
-                f[4 * v + 1] += o[v].y;
-                f[4 * v + 2] += o[v].z;
-                f[4 * v + 3] += o[v].w;
-              }
-            };
+          if (!last_flag) {
+            float* mine = a.part + ((int64_t)blockIdx.x * 2 + (u == lo ? 0 : 1)) * kPartFloats;
 #pragma unroll 1
             for (int c = 0; c < CW; c += 32) {
               float f[32];
+              tmem_cols(c, f);
+              float4* dst = reinterpret_cast<float4*>(mine) + (int64_t)((c0 + c) / 4) * kPartRows + lrow;
 #pragma unroll
-              for (int e = 0; e < 32; ++e) f[e] = 0.f;
-              // the parts in CTA order, its own from tensor memory (one part in flight: two measured
-              // no faster and hold 30 more registers across the whole kernel)
-              for (int cc = first; cc <= lastc; ++cc) {
-                if (cc == me) {
-                  float m[32];
-                  tmem_cols(c, m);
-#pragma unroll
-                  for (int e = 0; e < 32; ++e) f[e] += m[e];
-                } else {
-                  float4 A[8];
-                  load_part(cc, c, A);
-                  add_part(f, A);
+              for (int v = 0; v < 8; ++v)
+                __stcg(dst + v * kPartRows, make_float4(f[4 * v], f[4 * v + 1], f[4 * v + 2], f[4 * v + 3]));
+            }
+            // every writer fences its own stores: the barrier orders them only within the CTA
+            fence_acq_rel_gpu();
+            asm volatile("bar.sync 2, 256;" ::: "memory");
+            if (threadIdx.x == 128) atomicAdd(done, 1);
+          } else {
+            if (threadIdx.x == 128) {
+              const uint64_t t0 = globaltimer_ns();
+              while (ld_acquire_gpu(reinterpret_cast<const uint32_t*>(done)) != (uint32_t)(lastc - first)) {
+                if (globaltimer_ns() - t0 > TB_WAIT_NS) {
+                  aborted = 1;
+                  set_status(a.status, TB_DEV_TIMEOUT);
+                  break;
                 }
               }
-              store_y(c, f);
+              a.count[tile] = 0;
+              *done = 0;
+            }
+            asm volatile("bar.sync 2, 256;" ::: "memory");
+          }
+          if (last_flag) {
+            fence_acq_rel_gpu();  // each reader's acquire of the counted parts
+            const int me = cid;  // contributors are counted in clusters; cluster cc's CTA of this row tile
+            if (kBulkFix && u + (k1 - k0) >= hi) {
+              // Last segment: no stage is loaded again and every MMA is complete, so the ring
+              // holds the other contributors' parts, 32 columns of one part per slot, in the order
+              // they are added (chunk by chunk, contributors in CTA order).
+              constexpr uint32_t kSlotBytes = 32u * kPartRows * 4u;
+              const int nothers = lastc - first;
+              const int ncopy = (CW / 32) * nothers;
+              auto issue = [&](int j) {  // copy j: chunk j / nothers of the (j % nothers)-th other
+                const int i = j % nothers, cc = first + i + (first + i >= me ? 1 : 0);
+                const int slot = sk_lo(cc, units, grid) / nkb == t ? 0 : 1;
+                const float* src = a.part + ((int64_t)(cc * CS + crank) * 2 + slot) * kPartFloats +
+                                   (int64_t)((c0 + (j / nothers) * 32) / 4) * kPartRows * 4;
+                const int sl = j % kFixSlots;
+                mbar_arrive_expect_tx(pfull + sl, kSlotBytes);
+                bulk_g2s(smem + sl * kSlotBytes, src, kSlotBytes, pfull + sl);
+              };
+              if (threadIdx.x == 128) {
+                asm volatile("fence.proxy.async.global;" ::: "memory");  // parts read by the copy engine
+                for (int j = 0; j < ncopy && j < kFixSlots; ++j) issue(j);
+              }
+              int j = 0;
+#pragma unroll 1
+              for (int c = 0; c < CW; c += 32) {
+                float f[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) f[e] = 0.f;
+                for (int cc = first; cc <= lastc; ++cc) {
+                  if (cc == me) {
+                    float m[32];
+                    tmem_cols(c, m);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) f[e] += m[e];
+                    continue;
+                  }
+                  const int sl = j % kFixSlots;
+                  wait(pfull + sl, (j / kFixSlots) & 1);
+                  const uint32_t src = smem_u32(smem + sl * kSlotBytes) + (uint32_t)lrow * 16u;
+#pragma unroll
+                  for (int v = 0; v < 8; ++v) {
+                    const uint4 o = ld_shared_v4(src + (uint32_t)(v * kPartRows * 16));
+                    f[4 * v] += __uint_as_float(o.x);
+                    f[4 * v + 1] += __uint_as_float(o.y);
+                    f[4 * v + 2] += __uint_as_float(o.z);
+                    f[4 * v + 3] += __uint_as_float(o.w);
+                  }
+                  fence_proxy_async_smem();  // these loads before the copy that refills the slot
+                  __syncwarp();
+                  if (lane == 0) mbar_arrive(pempty + sl);
+                  if (threadIdx.x == 128 && j + kFixSlots < ncopy) {
+                    wait(pempty + sl, (j / kFixSlots) & 1);  // all eight warps have read the slot
+                    issue(j + kFixSlots);
+                  }
+                  __syncwarp();  // converged again before the next tensor-memory load
+                  ++j;
+                }
+                store_y(c, f);
+              }
+            } else {
+              auto load_part = [&](int cc, int c, float4 (&o)[8]) {
+                const int slot = sk_lo(cc, units, grid) / nkb == t ? 0 : 1;
+                const float4* op = reinterpret_cast<const float4*>(
+                                       a.part + ((int64_t)(cc * CS + crank) * 2 + slot) * kPartFloats) +
+                                   (int64_t)((c0 + c) / 4) * kPartRows + lrow;
+#pragma unroll
+                for (int v = 0; v < 8; ++v) o[v] = __ldcg(op + v * kPartRows);
+              };
+              auto add_part = [](float (&f)[32], const float4 (&o)[8]) {
+#pragma unroll
+                for (int v = 0; v < 8; ++v) {
+                  f[4 * v] += o[v].x;
+                  f[4 * v + 1] += o[v].y;
+                  f[4 * v + 2] += o[v].z;
+                  f[4 * v + 3] += o[v].w;
+                }
+              };
+#pragma unroll 1
+              for (int c = 0; c < CW; c += 32) {
+                float f[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) f[e] = 0.f;
+                // the parts in CTA order, its own from tensor memory (one part in flight: two measured
+                // no faster and hold 30 more registers across the whole kernel)
+                for (int cc = first; cc <= lastc; ++cc) {
+                  if (cc == me) {
+                    float m[32];
+                    tmem_cols(c, m);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) f[e] += m[e];
+                  } else {
+                    float4 A[8];
+                    load_part(cc, c, A);
+                    add_part(f, A);
+                  }
+                }
+                store_y(c, f);
+              }
             }
           }
         }
@@ -607,9 +692,9 @@ static int64_t tc_sms_bound() {
 }
 static size_t rup256(size_t v) { return (v + 255) / 256 * 256; }
 static size_t tc_x_bytes(int64_t M, int64_t K) { return rup256((size_t)M * (size_t)K * 2); }
-static size_t tc_count_bytes(int64_t M, int64_t N) {
-  return rup256((size_t)((M + kTcBM - 1) / kTcBM) * (size_t)((N + 127) / 128) * 4);
-}
+// two int32 counters per output tile of the smallest tile shape (claims, parts written)
+static int64_t tc_count_tiles(int64_t M, int64_t N) { return ((M + kTcBM - 1) / kTcBM) * ((N + 127) / 128); }
+static size_t tc_count_bytes(int64_t M, int64_t N) { return rup256((size_t)tc_count_tiles(M, N) * 2 * 4); }
 static size_t tc_part_bytes() { return (size_t)tc_sms_bound() * 2 * (2 * kTcBM) * 256 * 4; }
 
 size_t gemm_tc_x_bytes(int64_t M, int64_t K) { return tc_x_bytes(M, K); }
@@ -761,6 +846,7 @@ int launch_gemm_tc_rotated(const __half* xp, int64_t M, int64_t K, const uint32_
   a.nkb = (int)nkb;
   a.units = (int)(T * nkb);
   a.count = static_cast<int*>(gws);
+  a.done_off = (int)tc_count_tiles(M, N);
   a.part = reinterpret_cast<float*>(static_cast<char*>(gws) + tc_count_bytes(M, N));
   a.status = status;
   // the packed words [N][K/16] as a 2-D tensor: one box = one k-block (4 words) of bn rows
