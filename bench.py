@@ -341,6 +341,29 @@ def run_calls(tb, link_args, ws, status):
             tb.tb_packed_linear_multi(x, sg, block, mats, ys, ws, status)
 
 
+def gguf_links(tb, torch, links0, fmt, status):
+    """The scale-only links with every matrix re-encoded on the device as GGUF blocks of fmt
+    (tb_encode_gguf), each matrix one tb_gguf_linear call (its own rotation of the link's input).
+    Returns (calls, bytes of the blocks, the block tensors)."""
+    dev = torch.device("cuda")
+    bpb = 34 if fmt == tb.TB_FMT_PQ2_0 else 28
+    calls, keep, nbytes = [], [], 0
+    for x, sg, block, mats, ys in links0:
+        for (w, s, _), y in zip(mats, ys):
+            N, G = s.shape
+            blk = torch.empty(N * G * bpb, dtype=torch.uint8, device=dev)
+            tb.tb_encode_gguf(w, s, fmt, blk, status)
+            keep.append(blk)
+            nbytes += blk.numel()
+            calls.append((x, sg, block, blk, y))
+    return calls, nbytes, keep
+
+
+def run_gguf(tb, calls, fmt, ws, status):
+    for x, sg, block, blk, y in calls:
+        tb.tb_gguf_linear(x, sg, block, blk, fmt, y, ws, status)
+
+
 def embed(tb, st, ids, e_out, status, biases=True):
     tb.tb_embed_lookup(ids, st.emb.w, st.emb.s, st.emb.b if biases else None, st.signs[ti.HIDDEN],
                        1024, e_out, status)
@@ -565,6 +588,14 @@ def run_sweep(args, dist, tb, tdev, torch):
     scale_graph = capture(torch, lambda: (embed(tb, st, ids, e_out, status, biases=False),
                                           run_calls(tb, links0, ws, status)))
     gemv_graph = capture(torch, lambda: run_calls(tb, links, ws, status))
+    # the same step read straight from GGUF blocks (PTQ1_0: 1.75 bits per weight; PQ2_0: 2.125)
+    gws = torch.empty(tb.tb_gguf_linear_workspace_size(1, ti.MLP, 1024), dtype=torch.uint8, device=dev)
+    gguf = {}
+    for name, fmt in (("PTQ1_0", tb.TB_FMT_PTQ1_0), ("PQ2_0", tb.TB_FMT_PQ2_0)):
+        calls, nbytes, keep = gguf_links(tb, torch, links0, fmt, status)
+        g = capture(torch, lambda calls=calls, fmt=fmt: (embed(tb, st, ids, e_out, status, biases=False),
+                                                         run_gguf(tb, calls, fmt, gws, status)))
+        gguf[name] = (g, nbytes, keep)
 
     def chain_step():
         embed(tb, st, ids, e_out, status)
@@ -621,6 +652,12 @@ def run_sweep(args, dist, tb, tdev, torch):
     for _ in range(3):
         scale_graph.replay()
     ssecs = dist.max(time_steps(scale_graph.replay, args.steps))
+    gsecs = {}
+    for name, (g, nbytes, _) in gguf.items():
+        for _ in range(3):
+            g.replay()
+        gsecs[name] = (dist.max(time_steps(g.replay, args.steps)), nbytes)
+    del gguf
     torch.cuda.synchronize()
     assert int(status.item()) == 0, f"device status {int(status.item())}"
     assert bool(torch.isfinite(st.logits).all()), "non-finite logits"
@@ -686,6 +723,14 @@ def run_sweep(args, dist, tb, tdev, torch):
                 "weights_gb_per_step": round((st.scale_only_bytes + ti.HIDDEN // 4 + ti.HIDDEN // 64) / 1e9, 4),
                 "note": "calls path with biases = NULL (each bias is the pack's -scale, not read); "
                         "the same arithmetic on the same values as the stored-bias step",
+            },
+            "gguf": {
+                **{name: {"tok_s": round(n * args.steps / sec, 3),
+                          "weights_gb_per_step": round((nb + ti.HIDDEN // 4 + ti.HIDDEN // 64) / 1e9, 4)}
+                   for name, (sec, nb) in gsecs.items()},
+                "note": "the same trits and scales re-encoded on the device as GGUF blocks (tb_encode_gguf) "
+                        "and read straight from them (tb_gguf_linear, decoded on the CUDA cores), one call "
+                        "per matrix with its own rotation of the link's input; embedding as in scale_only",
             },
             "parallelism": f"replicas x{n}",
         },

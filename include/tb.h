@@ -147,6 +147,41 @@ int tb_transcode_gguf(const uint8_t* blocks, int format, int64_t N, int64_t K, u
                       uint16_t* scales, uint16_t* biases, int32_t* dev_status, void* stream);
 
 /*
+ * tb_gguf_linear — the packed layer read straight from GGUF blocks, no transcoding:
+ *   y[M,N] = fwht(x)[M,K] . W[N,K]^T,  W[n, 128g + i] = d[n,g] * t[n, 128g + i],
+ * the trits t and block scales d as the blocks hold them (the layout tb_transcode_gguf reads;
+ * the scale-only form: a code q = t + 1 decodes to d * (q - 1)).  [ARCH] "打包格式的工程":
+ * PQ2_0 and PTQ1_0 carry the same trits and scales as the 2.25-bit container; PTQ1_0 is the
+ * densest of the three (1.75 bits per weight) and costs extra arithmetic to decode.
+ *   x       fp16 [M, K];  signs, block: as tb_packed_linear (block 0: x used as it is);
+ *   blocks  uint8, N * (K/128) blocks of `format` back to back, row by row; 16-byte aligned;
+ *   format  TB_FMT_PQ2_0 or TB_FMT_PTQ1_0 (else TB_ERR_UNSUPPORTED);
+ *   y       fp16 [M, N] (out);
+ *   workspace  device scratch of at least tb_gguf_linear_workspace_size(M, K, block) bytes
+ *           (x' [M, K] fp16; none needed for block 0), 16-byte aligned.
+ * K a multiple of 1024 (TB_ERR_SHAPE otherwise), M, N >= 1.  dev_status optional:
+ * TB_DEV_BAD_CODE when a PQ2_0 slot holds 3 (read as d * 2), a PTQ1_0 byte is 243 or more (read
+ * as five trits of -1) or a PTQ1_0 digit past trit 127 is not zero (not read).  Tokens are taken
+ * in passes of up to 4 (fewer when x' of 4 tokens does not fit in shared memory).
+ */
+/*
+ * tb_encode_gguf — the other direction: the W2-g128 container (words and scales, the scale-only
+ * reading: each bias taken as -scale, not read) written as GGUF blocks of `format`, in the layout
+ * tb_transcode_gguf reads.  Lossless for codes 0..2; a code of 3 is not a trit: TB_DEV_BAD_CODE,
+ * kept in its slot by PQ2_0, written as 2 by PTQ1_0.
+ *   w       uint32 [N, K/16], 16-byte aligned;  scales fp16 [N, K/128];
+ *   blocks  uint8 (out), N * (K/128) blocks; 2-byte aligned for PQ2_0, 4-byte for PTQ1_0.
+ * K a positive multiple of 128, N >= 1.
+ */
+int tb_encode_gguf(const uint32_t* w, const uint16_t* scales, int64_t N, int64_t K, int format,
+                   uint8_t* blocks, int32_t* dev_status, void* stream);
+
+size_t tb_gguf_linear_workspace_size(int64_t M, int64_t K, int block);
+int tb_gguf_linear(const uint16_t* x, const int8_t* signs, int block, const uint8_t* blocks, int format,
+                   int64_t M, int64_t K, int64_t N, uint16_t* y, void* workspace, size_t workspace_bytes,
+                   int32_t* dev_status, void* stream);
+
+/*
  * tb_fwht — sign * normalised Walsh-Hadamard transform over blocks of `block` elements.
  * [ARCH] "Hadamard 旋转": fwht uses hadamard_transform with scale 1/sqrt(block);
  * forward multiplies by the signs first, the inverse multiplies by them again at the end.

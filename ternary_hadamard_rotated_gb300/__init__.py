@@ -72,6 +72,9 @@ _SIGNATURES = {
     "tb_chain_set_wait": (_INT, [_P, _I64, ctypes.c_int32, _P]),
     "tb_chain_run": (_INT, [_P, _INT, _I64, _I64, _P, _SZ, _P, _P]),
     "tb_transcode_gguf": (_INT, [_P, _INT, _I64, _I64, _P, _P, _P, _P, _P]),
+    "tb_gguf_linear_workspace_size": (ctypes.c_size_t, [_I64, _I64, _INT]),
+    "tb_encode_gguf": (_INT, [_P, _P, _I64, _I64, _INT, _P, _P, _P]),
+    "tb_gguf_linear": (_INT, [_P, _P, _INT, _P, _INT, _I64, _I64, _I64, _P, _P, ctypes.c_size_t, _P, _P]),
 }
 
 EXPORTED = tuple(_SIGNATURES)
@@ -136,6 +139,27 @@ def tb_transcode_gguf(blocks, fmt, N, K, w, scales, biases=None, dev_status=None
     container: w uint32 [N, K/16] (as int32), scales fp16 [N, K/128], biases = -scales (or None)."""
     _check("tb_transcode_gguf", load().tb_transcode_gguf(_ptr(blocks), fmt, N, K, _ptr(w), _ptr(scales),
                                                          _ptr(biases), _ptr(dev_status), _stream(stream)))
+
+
+def tb_encode_gguf(w, scales, fmt, blocks, dev_status=None, stream=None):
+    """W2 words [N, K/16] and scales [N, K/128] -> GGUF blocks of fmt (scale-only reading)."""
+    N, G = scales.shape
+    _check("tb_encode_gguf", load().tb_encode_gguf(_ptr(w), _ptr(scales), N, G * 128, fmt, _ptr(blocks),
+                                                   _ptr(dev_status), _stream(stream)))
+
+
+def tb_gguf_linear_workspace_size(M, K, block=1024):
+    return int(load().tb_gguf_linear_workspace_size(M, K, block))
+
+
+def tb_gguf_linear(x, signs, block, blocks, fmt, y, workspace=None, dev_status=None, stream=None):
+    """y[M,N] = fwht(x)[M,K] . W^T with W read from GGUF blocks (TB_FMT_PQ2_0 / TB_FMT_PTQ1_0)."""
+    M, K = x.shape
+    N = y.shape[-1]
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("tb_gguf_linear", load().tb_gguf_linear(_ptr(x), _ptr(signs), block, _ptr(blocks), fmt, M, K, N,
+                                                   _ptr(y), _ptr(workspace), ws_bytes, _ptr(dev_status),
+                                                   _stream(stream)))
 
 
 def tb_unpack_w2(w, codes, stream=None):

@@ -102,6 +102,64 @@ __global__ void __launch_bounds__(256) transcode_ptq1_0_kernel(const uint32_t* _
   if (bad) set_status(status, TB_DEV_BAD_CODE);
 }
 
+// The other direction, W2 words and group scales -> GGUF blocks, in the scale-only reading (each
+// bias is the pack's -scale and is not read).  A code of 3 is not a trit: it is flagged, PQ2_0
+// keeps it in its slot and PTQ1_0 writes it as 2.
+__global__ void __launch_bounds__(256) encode_pq2_0_kernel(const uint32_t* __restrict__ w,
+                                                          const uint16_t* __restrict__ scales,
+                                                          int64_t n_blocks, uint16_t* __restrict__ blk,
+                                                          int32_t* __restrict__ status) {
+  bool bad = false;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n_blocks;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const uint4* src = reinterpret_cast<const uint4*>(w + i * 8);
+    const uint4 a = __ldg(src), b = __ldg(src + 1);
+    const uint32_t wd[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    uint16_t* p = blk + i * (kPq2Bytes / 2);
+    p[0] = __ldg(scales + i);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      bad |= (wd[k] & (wd[k] >> 1) & 0x55555555u) != 0;
+      p[1 + 2 * k] = (uint16_t)(wd[k] & 0xFFFFu);
+      p[2 + 2 * k] = (uint16_t)(wd[k] >> 16);
+    }
+  }
+  if (bad) set_status(status, TB_DEV_BAD_CODE);
+}
+
+__global__ void __launch_bounds__(256) encode_ptq1_0_kernel(const uint32_t* __restrict__ w,
+                                                           const uint16_t* __restrict__ scales,
+                                                           int64_t n_blocks, uint32_t* __restrict__ blk,
+                                                           int32_t* __restrict__ status) {
+  bool bad = false;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n_blocks;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const uint4* src = reinterpret_cast<const uint4*>(w + i * 8);
+    const uint4 a = __ldg(src), b = __ldg(src + 1);
+    const uint32_t wd[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    uint32_t out[7] = {(uint32_t)__ldg(scales + i), 0, 0, 0, 0, 0, 0};
+#pragma unroll
+    for (int j = 0; j < 26; ++j) {  // byte 2 + j: trits 5j .. 5j+4 below 128, first the least significant
+      uint32_t v = 0;
+#pragma unroll
+      for (int d = 4; d >= 0; --d) {
+        const int p = 5 * j + d;
+        if (p >= 128) continue;
+        uint32_t q = (wd[p >> 4] >> (2 * (p & 15))) & 3u;
+        bad |= q == 3u;
+        q = q == 3u ? 2u : q;
+        v = 3u * v + q;
+      }
+      const int byte = 2 + j;
+      out[byte >> 2] |= v << (8 * (byte & 3));
+    }
+    uint32_t* p = blk + i * (kPtq1Bytes / 4);
+#pragma unroll
+    for (int k = 0; k < 7; ++k) p[k] = out[k];
+  }
+  if (bad) set_status(status, TB_DEV_BAD_CODE);
+}
+
 }  // namespace tb
 
 extern "C" int tb_transcode_gguf(const uint8_t* blocks, int format, int64_t N, int64_t K, uint32_t* w,
@@ -129,5 +187,32 @@ extern "C" int tb_transcode_gguf(const uint8_t* blocks, int format, int64_t N, i
   else
     transcode_ptq1_0_kernel<<<(int)grid, 256, 0, s>>>(reinterpret_cast<const uint32_t*>(blocks), n_blocks, w,
                                                        scales, biases, dev_status);
+  return check_launch();
+}
+
+extern "C" int tb_encode_gguf(const uint32_t* w, const uint16_t* scales, int64_t N, int64_t K, int format,
+                              uint8_t* blocks, int32_t* dev_status, void* stream) {
+  using namespace tb;
+  if (!w || !scales || !blocks) return TB_ERR_NULL;
+  if (format != TB_FMT_PQ2_0 && format != TB_FMT_PTQ1_0) return TB_ERR_UNSUPPORTED;
+  if (N < 1 || K < kGroup || K % kGroup) return TB_ERR_SHAPE;
+  const uintptr_t ba = reinterpret_cast<uintptr_t>(blocks);
+  if ((format == TB_FMT_PQ2_0 && (ba & 1u)) || (format == TB_FMT_PTQ1_0 && (ba & 3u)) || !aligned16(w) ||
+      (reinterpret_cast<uintptr_t>(scales) & 1u))
+    return TB_ERR_ALIGN;
+  DeviceFacts f;
+  int rc = device_facts(&f);
+  if (rc != TB_OK) return rc;
+  const int64_t n_blocks = N * (K / kGroup);
+  int64_t grid = (n_blocks + 255) / 256;
+  const int64_t cap = (int64_t)f.sms * 16;
+  if (grid > cap) grid = cap;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (format == TB_FMT_PQ2_0)
+    encode_pq2_0_kernel<<<(int)grid, 256, 0, s>>>(w, scales, n_blocks, reinterpret_cast<uint16_t*>(blocks),
+                                                  dev_status);
+  else
+    encode_ptq1_0_kernel<<<(int)grid, 256, 0, s>>>(w, scales, n_blocks, reinterpret_cast<uint32_t*>(blocks),
+                                                   dev_status);
   return check_launch();
 }

@@ -94,17 +94,18 @@ def test_workspace_size_query(lib):
     fix = ws(1, 5120, 17408, 1024)                  # decode path: the fixup region only
     assert 1024 < fix <= 3 << 20 and fix % 1024 == 0
     assert ws(8, 5120, 17408, 1024) == fix
-    # tensor-core path: x' (fp16 [M, K]), one counter per 128 x 128 output tile, then two
-    # fp32 256 x 256 parts per SM for the stream-K schedule's split tiles (with no GPU visible
-    # the bound is 256 SMs), each region rounded up to 256 bytes
+    # tensor-core path: x' (fp16 [M, K]), two int32 counters per 128 x 128 output tile (claims
+    # of a split tile, parts written), then two fp32 256 x 256 parts per SM for the stream-K
+    # schedule's split tiles (with no GPU visible the bound is 256 SMs), each region rounded up
+    # to 256 bytes
     def up(v):
         return (v + 255) // 256 * 256
 
     def tc(M, K, N, sms):
-        return up(M * K * 2) + up(-(-M // 128) * -(-N // 128) * 4) + sms * 2 * 256 * 256 * 4
+        return up(M * K * 2) + up(-(-M // 128) * -(-N // 128) * 8) + sms * 2 * 256 * 256 * 4
 
     big = ws(512, 5120, 17408, 1024)
-    sms = (big - fix - up(512 * 5120 * 2) - up(4 * 136 * 4)) // (2 * 256 * 256 * 4)
+    sms = (big - fix - up(512 * 5120 * 2) - up(4 * 136 * 8)) // (2 * 256 * 256 * 4)
     assert 1 <= sms <= 256
     assert big == fix + tc(512, 5120, 17408, sms)
     assert ws(512, 1000, 17408, 1024) == 0          # invalid shape -> 0
@@ -243,3 +244,30 @@ def test_binding_signatures_match_the_header():
     for name, n in protos.items():
         assert name in tb._SIGNATURES, name
         assert len(tb._SIGNATURES[name][1]) == n, (name, n, len(tb._SIGNATURES[name][1]))
+
+
+def test_gguf_linear_refuses_bad_arguments(lib):
+    f = lib.tb_gguf_linear
+    ws = lib.tb_gguf_linear_workspace_size
+    assert ws(2, 4096, 1024) == 2 * 4096 * 2 and ws(2, 4096, 0) == 0
+    # (x, signs, block, blocks, format, M, K, N, y, workspace, workspace_bytes, status, stream)
+    assert f(None, None, 0, P, 1, 1, 1024, 8, P, None, 0, None, None) == -1       # x NULL
+    assert f(P, None, 0, P, 3, 1, 1024, 8, P, None, 0, None, None) == -3          # format
+    assert f(P, None, 768, P, 1, 1, 1536, 8, P, P, 1 << 20, None, None) == -3     # block
+    assert f(P, None, 0, P, 1, 1, 1536, 8, P, None, 0, None, None) == -2          # K % 1024
+    assert f(P, None, 0, P, 2, 0, 1024, 8, P, None, 0, None, None) == -2          # M
+    assert f(P, None, 0, P + 2, 1, 1, 1024, 8, P, None, 0, None, None) == -6      # blocks alignment
+    assert f(P, None, 1024, P, 1, 2, 2048, 8, P, P, 2 * 2048 * 2 - 16, None, None) == -7  # workspace
+    assert f(P, None, 1024, P, 2, 2, 2048, 8, P, None, 0, None, None) == -7       # no workspace
+
+
+def test_encode_gguf_refuses_bad_arguments(lib):
+    f = lib.tb_encode_gguf
+    # (w, scales, N, K, format, blocks, status, stream)
+    assert f(None, P, 4, 1024, 1, P, None, None) == -1
+    assert f(P, P, 4, 1024, 0, P, None, None) == -3
+    assert f(P, P, 4, 100, 1, P, None, None) == -2
+    assert f(P, P, 0, 1024, 2, P, None, None) == -2
+    assert f(P, P, 4, 1024, 1, P + 1, None, None) == -6
+    assert f(P, P, 4, 1024, 2, P + 2, None, None) == -6
+    assert f(P + 4, P, 4, 1024, 1, P, None, None) == -6
