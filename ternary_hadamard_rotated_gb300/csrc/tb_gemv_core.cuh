@@ -9,9 +9,10 @@
 // Work unit: 128 output rows x 512 k (4 groups of 128) = one 16 KB TMA box of packed codes
 // (128 rows x 128 B, 128-byte swizzle).  Arithmetic per group of 128 and token: LOP3 puts each
 // 2-bit code into the mantissa of an fp16 1024.0 (1024 + sigma*q, exact; sigma = 4^j from the
-// field's bit position j); those half2 are mma.sync A fragments, x'/sigma the B fragment, and
-// the accumulator starts at -1024*sum(x'/sigma), so the tensor core returns D = sum q*x':
-//   y += s * D + b * S,   S = sum x' over the group.
+// field's bit position j); those half2 are mma.sync A fragments, x'/sigma the B fragment.  The
+// first MMA of a group starts from zero (no register moves for the start value) and the
+// epilogue takes C = 1024*sum(x'/sigma) off, which leaves D - C = sum q*x':
+//   y += s * (D - C) + b * S,   S = sum x' over the group.
 #pragma once
 
 #include <cuda.h>
@@ -88,6 +89,16 @@ TB_DEVI void mma16816_acc(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, 
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+
+TB_DEVI void mma16816_zero(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                           uint32_t b0, uint32_t b1) {
+  const float z = 0.f;
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%10,%10,%10,%10};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(z));
+}
+
 TB_DEVI void decode_word_sigma(uint32_t w, uint32_t (&P)[8]) {
   const uint32_t w6 = w >> 6;
   P[0] = lop3_and_or(w, 0x00030003u, kMagic1024);   // codes 0, 8   sigma 1
@@ -134,13 +145,6 @@ TB_DEVI void unit_group(uint32_t box, int R0, int t, int gi, int grp, uint32_t i
   const float2 cs1 = MT > 1 ? ld_shared_f2(csa + (grp * MT + t1) * 8) : cs0;
   float d[2][4];
 #pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    d[j][0] = -cs0.x;
-    d[j][1] = -cs1.x;
-    d[j][2] = -cs0.x;
-    d[j][3] = -cs1.x;
-  }
-#pragma unroll
   for (int half = 0; half < 2; ++half) {
     const uint4 i0 = ld_shared_v4(imgt + (grp * 4 + 2 * half) * MT * 64);
     const uint4 i1 = ld_shared_v4(imgt + (grp * 4 + 2 * half + 1) * MT * 64);
@@ -151,7 +155,10 @@ TB_DEVI void unit_group(uint32_t box, int R0, int t, int gi, int grp, uint32_t i
       decode_word_sigma(half ? w[j][1].y : w[j][1].x, Q[j]);
     }
 #pragma unroll
-    for (int j = 0; j < 2; ++j) mma16816_acc(d[j], P[j][0], Q[j][0], P[j][1], Q[j][1], i0.x, i0.y);
+    for (int j = 0; j < 2; ++j) {
+      if (half == 0) mma16816_zero(d[j], P[j][0], Q[j][0], P[j][1], Q[j][1], i0.x, i0.y);
+      else mma16816_acc(d[j], P[j][0], Q[j][0], P[j][1], Q[j][1], i0.x, i0.y);
+    }
 #pragma unroll
     for (int j = 0; j < 2; ++j) mma16816_acc(d[j], P[j][2], Q[j][2], P[j][3], Q[j][3], i0.z, i0.w);
 #pragma unroll
@@ -164,11 +171,11 @@ TB_DEVI void unit_group(uint32_t box, int R0, int t, int gi, int grp, uint32_t i
     const int ra = 16 * j + rA, rb = ra + 8;  // rows within the warp's 32
     const float2 A = ld_shared_f2(ss + (ra * kUnitGroups + gi) * 8);  // (s, b) of row ra
     const float2 B = ld_shared_f2(ss + (rb * kUnitGroups + gi) * 8);
-    acc[j][0] = fmaf(A.x, d[j][0], fmaf(A.y, cs0.y, acc[j][0]));
-    acc[j][2] = fmaf(B.x, d[j][2], fmaf(B.y, cs0.y, acc[j][2]));
+    acc[j][0] = fmaf(A.x, d[j][0] - cs0.x, fmaf(A.y, cs0.y, acc[j][0]));
+    acc[j][2] = fmaf(B.x, d[j][2] - cs0.x, fmaf(B.y, cs0.y, acc[j][2]));
     if (MT > 1) {  // D columns 2t+1 hold a second token only when there is one
-      acc[j][1] = fmaf(A.x, d[j][1], fmaf(A.y, cs1.y, acc[j][1]));
-      acc[j][3] = fmaf(B.x, d[j][3], fmaf(B.y, cs1.y, acc[j][3]));
+      acc[j][1] = fmaf(A.x, d[j][1] - cs1.x, fmaf(A.y, cs1.y, acc[j][1]));
+      acc[j][3] = fmaf(B.x, d[j][3] - cs1.x, fmaf(B.y, cs1.y, acc[j][3]));
     }
   }
 }

@@ -21,15 +21,16 @@
 // keeps its partial sums in registers while it stays in one tile; a tile that lies wholly in
 // the group's sub-range is written straight from registers; a tile cut by a group boundary is
 // summed in shared memory, and one cut by a CTA boundary is summed in an fp32 workspace slot
-// whose last contributor converts it to y and returns slot and counter to zero.  A producer
-// warp keeps a ring of slots in flight; before the activations are loaded it issues only one
-// unit per group, so the loads of x are not queued behind megabytes of weight traffic.
+// whose last contributor converts it to y and returns slot and counter to zero.  One producer
+// warp per group keeps that group's ring of slots in flight (a group that is slow to release a
+// slot holds back no other group's refill); before the activations are loaded each issues only
+// one unit, so the loads of x are not queued behind megabytes of weight traffic.
 //
 // Arithmetic (per group of 128, per token): LOP3 puts each 2-bit code into the mantissa of
 // an fp16 1024.0 (1024 + sigma*q, exact; sigma = 4^j from the field's bit position j);
-// those half2 are mma.sync A fragments, x'/sigma the B fragment, and the accumulator
-// starts at -1024*sum(x'/sigma) so the tensor core returns D = sum q*x' directly:
-//   y += s * D + b * S,   S = sum x' over the group.
+// those half2 are mma.sync A fragments, x'/sigma the B fragment; the group's first MMA
+// starts from zero and C = 1024*sum(x'/sigma) is taken off in the epilogue:
+//   y += s * (D - C) + b * S,   S = sum x' over the group.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -73,10 +74,11 @@ TB_DEVI int mat_of(const GemvTmaArgs& a, int tile) {
   return i;
 }
 
-// Warp roles: warps 0..11 consume (three unit groups of four), warp 12 produces; warps 13..15
-// only complete the producer's warpgroup so that registers can move between the roles: the
-// launch gives 128 per thread, the producer warpgroup drops to 40 and the consumers rise to 152
-// (12 x 32 x 152 + 4 x 32 x 40 = 63488 of the 65536 the block was launched with).
+// Warp roles: warps 0..11 consume (three unit groups of four), warps 12..14 produce (one per
+// group); warp 15 only completes the producers' warpgroup so that registers can move between
+// the roles: the launch gives 128 per thread, the producer warpgroup drops to 40 and the
+// consumers rise to 152 (12 x 32 x 152 + 4 x 32 x 40 = 63488 of the 65536 the block was
+// launched with).
 constexpr int kWsThreads = 16 * 32;
 template <int MT>
 __global__ void __launch_bounds__(kWsThreads, 1)
@@ -139,46 +141,35 @@ __global__ void __launch_bounds__(kWsThreads, 1)
 
   if (warp >= kTmaConsumers) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 40;" ::: "memory");
-    if (warp != kTmaConsumers) return;
-    // ---- producer: the packed weights never depend on the previous kernel ----
+    const int u = warp - kTmaConsumers;  // one producer warp per unit group
+    if (u >= kGroupsOfWarps) return;
+    // ---- producer of group u: the packed weights never depend on the previous kernel ----
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
-      int tl[kGroupsOfWarps], ch[kGroupsOfWarps], cntu[kGroupsOfWarps];
-      int maxcnt = 0;
-#pragma unroll
-      for (int u = 0; u < kGroupsOfWarps; ++u) {
-        int glo, ghi;
-        group_range(u, glo, ghi);
-        cntu[u] = ghi - glo;
-        const int first = u == kGroupsOfWarps - 1 ? ghi - 1 : glo;
-        tl[u] = first / C;
-        ch[u] = first - tl[u] * C;
-        maxcnt = cntu[u] > maxcnt ? cntu[u] : maxcnt;
-      }
-      for (int n = 0, si = 0, k = 0; n < maxcnt; ++n) {  // si = n % DW, k = n / DW
+      int glo, ghi;
+      group_range(u, glo, ghi);
+      const int cntu = ghi - glo;
+      const bool back = u == kGroupsOfWarps - 1;
+      const int first = back ? ghi - 1 : glo;
+      int tl = first / C, ch = first - (first / C) * C;
+      for (int n = 0, si = 0, k = 0; n < cntu; ++n) {  // si = n % DW, k = n / DW
         if (n == kPreIssue) wait(xready, 0);  // the activations have been read
-#pragma unroll
-        for (int u = 0; u < kGroupsOfWarps; ++u) {
-          if (n >= cntu[u]) continue;
-          const int slot = u * DW + si;
-          if (k > 0) wait(empty + slot, (k - 1) & 1);
-          const int mi = mat_of(a, tl[u]);
-          const int row = (tl[u] - a.tile0[mi]) * kUnitRows;
-          mbar_arrive_expect_tx(full + slot, kSlotBytes);
-          tma2d(slots_u32 + slot * kSlotBytes, &maps.codes[mi], ch[u] * 32, row, full + slot, pol);
-          step_unit(tl[u], ch[u], C, u == kGroupsOfWarps - 1);
-        }
+        const int slot = u * DW + si;
+        if (k > 0) wait(empty + slot, (k - 1) & 1);
+        const int mi = mat_of(a, tl);
+        const int row = (tl - a.tile0[mi]) * kUnitRows;
+        mbar_arrive_expect_tx(full + slot, kSlotBytes);
+        tma2d(slots_u32 + slot * kSlotBytes, &maps.codes[mi], ch * 32, row, full + slot, pol);
+        step_unit(tl, ch, C, back);
         if (++si == DW) {
           si = 0;
           ++k;
         }
       }
       // leave no copy in flight: wait (bounded, even after a timeout) for the last fill of
-      // every slot
-#pragma unroll
-      for (int u = 0; u < kGroupsOfWarps; ++u)
-        for (int n = cntu[u] - 1; n >= 0 && n >= cntu[u] - DW; --n)
-          if (!mbar_wait(full + u * DW + n % DW, (n / DW) & 1)) set_status(a.status, TB_DEV_TIMEOUT);
+      // every slot of this group
+      for (int n = cntu - 1; n >= 0 && n >= cntu - DW; --n)
+        if (!mbar_wait(full + u * DW + n % DW, (n / DW) & 1)) set_status(a.status, TB_DEV_TIMEOUT);
     }
     __syncwarp();
     return;
