@@ -73,8 +73,9 @@ enum {
 #define TB_DEV_BAD_PLAN 8  /* tb_chain_run: the plan does not match the launch (nothing computed) */
 
 /* algorithm choice for tb_packed_linear_algo */
-#define TB_ALGO_AUTO 0       /* GEMV for M <= 8, the batched-decode GEMV for 9..64 tokens,
-                                the tensor-core GEMM above */
+#define TB_ALGO_AUTO 0       /* the GEMV for M <= 2, the batched GEMV on mma.sync for 3..32
+                                tokens, the batched-decode GEMV on tensor memory for 33..64, the
+                                tensor-core GEMM above */
 #define TB_ALGO_GEMV 1       /* fused sign*FWHT prologue + streaming W2 GEMV (the warp-level one);
                                 any M (passes of 8 tokens) */
 #define TB_ALGO_TC 2         /* FWHT kernel into the workspace + tcgen05/TMEM GEMM; any M */
@@ -89,6 +90,13 @@ enum {
                                 tokens its N side; x' rotated into the workspace first, as for
                                 TB_ALGO_TC (same workspace); M <= 64 (else passes of 64 tokens),
                                 K a multiple of 1024 (TB_ERR_UNSUPPORTED otherwise) */
+#define TB_ALGO_GEMV_BATCH 6 /* the batched-decode GEMV on mma.sync: x' rotated once into the
+                                workspace as the mma's operand image (per 512-k chunk and pass of
+                                8, 16, 32 or 64 tokens), then every unit of packed codes decoded
+                                once and run against all tokens of the pass; any M (passes of 64
+                                tokens above 32), K a multiple of 1024 (TB_ERR_UNSUPPORTED
+                                otherwise); tb_packed_linear_algo_workspace_size gives its
+                                workspace */
 
 /* Human-readable text of a return code; never NULL. */
 const char* tb_status_string(int status);
@@ -255,8 +263,9 @@ int tb_packed_linear_algo(const uint16_t* x, int64_t M, int64_t K, const int8_t*
  * those matrices); K must be a positive multiple of 1024 (and of block); block as for
  * tb_packed_linear (512, 2048, 4096: x' computed once into the workspace).  Workspace as for
  * tb_packed_linear, sized with tb_packed_linear_workspace_size(M, K, max N, block).
- * M <= 8: one decode GEMV launch for all matrices.  M > 8: one rotation, then one tensor-core
- * GEMM per matrix.
+ * The kernels are those AUTO picks for M: M <= 2, one decode GEMV launch for all matrices;
+ * 3..32, one rotation into the operand image, then one batched GEMV launch per matrix; above,
+ * one rotation, then one batched-decode GEMV (33..64) or tensor-core GEMM launch per matrix.
  */
 int tb_packed_linear_multi(const uint16_t* x, int64_t M, int64_t K, const int8_t* signs, int block,
                            int n, const uint32_t* const* w, const uint16_t* const* scales,

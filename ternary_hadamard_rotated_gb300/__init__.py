@@ -39,6 +39,7 @@ TB_ALGO_TC = 2
 TB_ALGO_GEMV_SYNC = 3
 TB_ALGO_GEMV_TMEM = 4
 TB_ALGO_GEMV_WIDE = 5
+TB_ALGO_GEMV_BATCH = 6
 
 TB_FMT_PQ2_0 = 1
 TB_FMT_PTQ1_0 = 2

@@ -1,5 +1,6 @@
-// Entry points of the non-embedding path: argument checks and the choice between the
-// streaming GEMV (decode, M <= 8 tokens) and the tensor-core GEMM (prefill).
+// Entry points of the non-embedding path: argument checks and the choice of kernel by token
+// count: the streaming GEMV (M <= 2), the batched GEMV on mma.sync (3..32), the batched GEMV on
+// tensor memory (33..64) and the tensor-core GEMM (prefill).
 //
 // [ARCH] kwkr.cn/news/564617, section "Hadamard 旋转把量化误差抹平的免费午餐":
 //   the module's forward pass rotates the input (signs, then the normalised block Hadamard
@@ -42,6 +43,11 @@ int launch_gemv_wide(const __half* xp, int64_t M, int64_t K, const uint32_t* w, 
                      cudaStream_t s);
 size_t gemv_wide_part_bytes();
 size_t gemm_tc_part_offset(int64_t M, int64_t K, int64_t N);
+size_t gemv_batch_bytes(int64_t M, int64_t K);
+int launch_batch_image(const __half* x, int64_t M, int64_t K, const int8_t* signs, int rotate,
+                       void* region, cudaStream_t s);
+int launch_batch_gemv(int64_t M, int64_t K, const uint32_t* w, const __half* scales, const __half* biases,
+                      int64_t N, __half* y, void* region, int32_t* status, cudaStream_t s);
 constexpr int kMaxMulti = 4;
 
 // Workspace layout: [fixup region of the GEMV split schedule (zero before the first call,
@@ -55,15 +61,22 @@ static size_t fixup_region() { return (gemv_fixup_bytes() + 1023) / 1024 * 1024;
 static bool separate_block(int block) { return block != 0 && block != kBlock; }
 static size_t natural_x_bytes(int64_t M, int64_t K) { return (size_t)((M * K * 2 + 1023) / 1024 * 1024); }
 
-// decode (GEMV) up to this many tokens; the tensor-core GEMM above
-constexpr int64_t kGemvMaxTokens = 8;
-
-// the batched-decode GEMV up to this many tokens per pass (AUTO: above kGemvMaxTokens)
+// AUTO's token-count bounds, from same-box timings of the four kernels on the 27B model's layer
+// shapes (5120 -> 17408, 17408 -> 5120, 5120 -> 6144): the streaming GEMV up to kGemvMaxTokens
+// (its fused prologue transforms every token's x in every CTA, which costs more per token than
+// the batched GEMV's one rotation pass from three tokens on), the batched GEMV on mma.sync up to
+// kBatchMaxTokens (above it, 40..64 tokens, its MMAs cost more than the tensor-memory kernel's),
+// the tensor-memory one up to kWideMaxTokens, the tensor-core GEMM above
+constexpr int64_t kGemvMaxTokens = 2;
+constexpr int64_t kBatchMaxTokens = 32;
 constexpr int64_t kWideMaxTokens = 64;
 
 static int resolve_algo(int64_t M, int algo) {
   if (algo == TB_ALGO_AUTO)
-    return M <= kGemvMaxTokens ? TB_ALGO_GEMV : M <= kWideMaxTokens ? TB_ALGO_GEMV_WIDE : TB_ALGO_TC;
+    return M <= kGemvMaxTokens    ? TB_ALGO_GEMV
+           : M <= kBatchMaxTokens ? TB_ALGO_GEMV_BATCH
+           : M <= kWideMaxTokens  ? TB_ALGO_GEMV_WIDE
+                                  : TB_ALGO_TC;
   return algo;
 }
 // the batched-decode GEMV uses the tensor-core path's workspace (x', then its parts region)
@@ -117,11 +130,18 @@ static int check_linear_shape(int64_t M, int64_t K, int block, int64_t N) {
   return TB_OK;
 }
 
-// bytes of workspace one call needs: the GEMV's fixup region, the tensor-core path's x' and
-// schedule state, and x' in natural order for a block that is not fused
+// bytes the matmul path itself needs after the GEMV's fixup region: the tensor-core path's x'
+// and schedule state, or the batched GEMV's counters, parts and operand images
+static size_t matmul_region(int64_t M, int64_t K, int64_t N, int use) {
+  if (uses_tc_workspace(use)) return gemm_tc_workspace(M, K, N);
+  if (use == TB_ALGO_GEMV_BATCH) return gemv_batch_bytes(M, K);
+  return 0;
+}
+
+// bytes of workspace one call needs: the GEMV's fixup region, the matmul path's region, and x'
+// in natural order for a block that is not fused
 static size_t linear_workspace(int64_t M, int64_t K, int64_t N, int block, int use) {
-  size_t b = fixup_region();
-  if (uses_tc_workspace(use)) b += gemm_tc_workspace(M, K, N);
+  size_t b = fixup_region() + matmul_region(M, K, N, use);
   if (separate_block(block)) b += natural_x_bytes(M, K);
   return b;
 }
@@ -129,7 +149,19 @@ static size_t linear_workspace(int64_t M, int64_t K, int64_t N, int block, int u
 // where x' in natural order goes: after everything the matmul path itself uses
 static __half* natural_x(void* workspace, int64_t M, int64_t K, int64_t N, int use) {
   return reinterpret_cast<__half*>(static_cast<char*>(workspace) + fixup_region() +
-                                   (uses_tc_workspace(use) ? gemm_tc_workspace(M, K, N) : 0));
+                                   matmul_region(M, K, N, use));
+}
+
+// x' once into the batch region as the operand image, then the batched GEMV per matrix
+static int launch_batch_path(const __half* xh, int64_t M, int64_t K, const int8_t* sg, int block, int n,
+                             const uint32_t* const* w, const __half* const* sh, const __half* const* bh,
+                             const int64_t* N, __half* const* yh, void* workspace, int32_t* dev_status,
+                             cudaStream_t s) {
+  void* region = static_cast<char*>(workspace) + fixup_region();
+  int rc = launch_batch_image(xh, M, K, sg, block != 0, region, s);
+  for (int i = 0; i < n && rc == TB_OK; ++i)
+    rc = launch_batch_gemv(M, K, w[i], sh[i], bh[i], N[i], yh[i], region, dev_status, s);
+  return rc;
 }
 
 }  // namespace tb
@@ -154,7 +186,7 @@ extern "C" int tb_packed_linear_algo(const uint16_t* x, int64_t M, int64_t K, co
   if (!x || !w || !scales || !y) return TB_ERR_NULL;  // biases may be NULL: each is -scale
   int rc = check_linear_shape(M, K, block, N);
   if (rc != TB_OK) return rc;
-  if (algo < TB_ALGO_AUTO || algo > TB_ALGO_GEMV_WIDE) return TB_ERR_UNSUPPORTED;
+  if (algo < TB_ALGO_AUTO || algo > TB_ALGO_GEMV_BATCH) return TB_ERR_UNSUPPORTED;
   if (!aligned16(x) || !aligned16(w) || !aligned16(scales) || (biases && !aligned16(biases)) ||
       !aligned16(y) ||
       (signs && !aligned16(signs)) || (workspace && !aligned16(workspace)))
@@ -174,6 +206,11 @@ extern "C" int tb_packed_linear_algo(const uint16_t* x, int64_t M, int64_t K, co
     xh = xn;
     sg = nullptr;
     block = 0;
+  }
+  if (use == TB_ALGO_GEMV_BATCH) {
+    if (K % kBlock) return TB_ERR_UNSUPPORTED;
+    if (!workspace || workspace_bytes < fixup_region() + gemv_batch_bytes(M, K)) return TB_ERR_WORKSPACE;
+    return launch_batch_path(xh, M, K, sg, block, 1, &w, &sh, &bh, &N, &yh, workspace, dev_status, s);
   }
   if (use == TB_ALGO_GEMV_WIDE) {
     if (K % kBlock) return TB_ERR_UNSUPPORTED;
@@ -242,6 +279,10 @@ extern "C" int tb_packed_linear_multi(const uint16_t* x, int64_t M, int64_t K, c
   if (M <= kGemvMaxTokens)
     return launch_streaming_gemv(TB_ALGO_GEMV, xh, M, K, sg, block, n, w, sh, bh, N, yh, workspace,
                                  workspace_bytes, dev_status, s);
+  if (M <= kBatchMaxTokens) {  // one rotation into the operand image, then one launch per matrix
+    if (!workspace || workspace_bytes < fixup_region() + gemv_batch_bytes(M, K)) return TB_ERR_WORKSPACE;
+    return launch_batch_path(xh, M, K, sg, block, n, w, sh, bh, N, yh, workspace, dev_status, s);
+  }
   // prefill: one rotation of x into the workspace, then one GEMM per matrix
   int64_t maxN = 0;
   for (int i = 0; i < n; ++i) maxN = N[i] > maxN ? N[i] : maxN;

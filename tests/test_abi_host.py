@@ -93,7 +93,19 @@ def test_workspace_size_query(lib):
     ws = lib.tb_packed_linear_workspace_size
     fix = ws(1, 5120, 17408, 1024)                  # decode path: the fixup region only
     assert 1024 < fix <= 3 << 20 and fix % 1024 == 0
-    assert ws(8, 5120, 17408, 1024) == fix
+    assert ws(2, 5120, 17408, 1024) == fix
+
+    # batched GEMV (3..32 tokens): 1 KB of counters, fp32 parts [256 CTAs][2][128][MT], then the
+    # operand images: per pass of MT tokens and 512-k chunk, 1024 MT + 32 MT bytes (1 KB rounded)
+    def batch(M, K):
+        MT = 8 if M <= 8 else 16 if M <= 16 else 32 if M <= 32 else 64
+        passes = -(-M // MT)
+        return 1024 + 256 * 2 * 128 * MT * 4 + (passes * (K // 512) * 1056 * MT + 1023) // 1024 * 1024
+
+    assert ws(8, 5120, 17408, 1024) == fix + batch(8, 5120)
+    assert ws(3, 17408, 5120, 1024) == fix + batch(3, 17408)
+    assert ws(32, 5120, 6144, 1024) == fix + batch(32, 5120)
+    assert lib.tb_packed_linear_algo_workspace_size(100, 2048, 64, 1024, 6) == fix + batch(100, 2048)
     # tensor-core path: x' (fp16 [M, K]), two int32 counters per 128 x 128 output tile (claims
     # of a split tile, parts written), then two fp32 256 x 256 parts per SM for the stream-K
     # schedule's split tiles (with no GPU visible the bound is 256 SMs), each region rounded up

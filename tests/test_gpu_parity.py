@@ -55,12 +55,15 @@ def run_linear(tb, x16, signs, block, w, s, b, N, algo=0, workspace="zeros", rep
     assert int(st.item()) == 0
     if ws is not None:  # the counters of shared output tiles are left zero for the next call
         assert int(ws[:1024].count_nonzero().item()) == 0
-        if algo == 2 or (algo == 0 and M > 8):
+        use = algo or (1 if M <= 2 else 6 if M <= 32 else 5 if M <= 64 else 2)  # AUTO's choice
+        if use == 2:
             # tensor-core path: after the 2 MB fixup region and x' (rounded up to 256 bytes)
             # come the stream-K tile counters, left zero as well
             c0 = 2098176 + (M * K * 2 + 255) // 256 * 256
             nc = -(-M // 128) * -(-N // 128)
             assert int(ws[c0:c0 + 4 * nc].count_nonzero().item()) == 0
+        if use == 6:  # the batched GEMV's counters open the region after the fixup region
+            assert int(ws[2098176:2098176 + 1024].count_nonzero().item()) == 0
     if repeat > 1:
         return [o.cpu().numpy() for o in outs]
     return outs[0].cpu().numpy()
