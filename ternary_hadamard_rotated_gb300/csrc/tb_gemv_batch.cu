@@ -30,9 +30,6 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
-#include <mutex>
-#include <unordered_map>
-
 #include "tb_common.cuh"
 #include "tb_gemv_core.cuh"
 #include "tb_host.h"
@@ -40,6 +37,7 @@
 namespace tb {
 
 int code_map(const uint32_t* w, int64_t N, int64_t K, CUtensorMap* out);
+int group_map(const __half* p, int64_t N, int64_t G, CUtensorMap* out);
 
 constexpr int kBtConsumers = 8;                         // warps of 16 rows: one 128-row unit
 constexpr int kBtThreads = (kBtConsumers + 1) * 32;     // and the producer warp
@@ -457,46 +455,6 @@ int launch_batch_image(const __half* x, int64_t M, int64_t K, const int8_t* sign
       batch_image_kernel<64><<<blocks, kBtImgWarps * 32, 0, s>>>(x, signs, (int)M, (int)K, rotate, (int)n_tok, blob);
   }
   return check_launch();
-}
-
-// tensor map of a [N, G] fp16 array of scales or biases (box 8 groups x 128 rows, no swizzle),
-// cached by (pointer, shape)
-static int group_map(const __half* p, int64_t N, int64_t G, CUtensorMap* out) {
-  struct Key {
-    const void* p;
-    int64_t N, G;
-    bool operator==(const Key& o) const { return p == o.p && N == o.N && G == o.G; }
-  };
-  struct Hash {
-    size_t operator()(const Key& k) const { return std::hash<const void*>()(k.p) ^ std::hash<int64_t>()(k.N * 131 + k.G); }
-  };
-  static std::mutex mu;
-  static std::unordered_map<Key, CUtensorMap, Hash> cache;
-  const Key key{p, N, G};
-  {
-    std::lock_guard<std::mutex> lock(mu);
-    auto it = cache.find(key);
-    if (it != cache.end()) {
-      *out = it->second;
-      return TB_OK;
-    }
-  }
-  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
-  if (!enc) return TB_ERR_CUDA;
-  CUtensorMap m;
-  const cuuint64_t dims[2] = {(cuuint64_t)G, (cuuint64_t)N};
-  const cuuint64_t strides[1] = {(cuuint64_t)G * 2};
-  const cuuint32_t box[2] = {8, (cuuint32_t)kUnitRows};
-  const cuuint32_t es[2] = {1, 1};
-  if (enc(&m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<__half*>(p), dims, strides, box, es,
-          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-    return TB_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(mu);
-  if (cache.size() > 4096) cache.clear();
-  cache[key] = m;
-  *out = m;
-  return TB_OK;
 }
 
 template <int NT>

@@ -46,11 +46,11 @@ __host__ __device__ inline int rup(int v, int a) { return (v + a - 1) / a * a; }
 
 
 template <int MT>
-__host__ __device__ inline GemvTmaLayout gemv_tma_layout(int G, int dw) {
+__host__ __device__ inline GemvTmaLayout gemv_tma_layout(int G, int dw, int slot = kSlotBytes) {
   GemvTmaLayout L;
   int off = 0;
   L.codes = off;  // 1024-aligned slots (the 128-byte swizzle repeats every 1024 bytes)
-  off += kGroupsOfWarps * dw * kSlotBytes;
+  off += kGroupsOfWarps * dw * slot;
   L.img = off;
   off += G * 256 * MT;
   L.cs = off;

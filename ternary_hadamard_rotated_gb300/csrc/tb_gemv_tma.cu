@@ -9,9 +9,11 @@
 // Work unit: 128 output rows x 512 k (4 groups of 128) = one 16 KB TMA box of packed codes
 // (128 rows x 128 B, 128-byte swizzle; rows past N are zero-filled).  Each SM can keep only
 // a handful of TMA requests in flight, so requests are made large: 16 KB boxes stream at
-// the HBM rate where 2-4 KB requests stall at a fraction of it.  Scales and biases (8 B per
-// row per unit) are read by the consumer warps themselves, two units ahead, and staged
-// through shared memory.
+// the HBM rate where 2-4 KB requests stall at a fraction of it.  The scales and biases of the
+// unit's rows come in the same ring slot, as TMA boxes of 8 groups (the unit's 4 and its
+// neighbour's: a tensor copy's inner extent is at least 16 bytes), so the consumer warps issue
+// no global loads of their own in the stream; each warp stages its rows' values as fp32
+// pairs in shared memory.
 //
 // Schedule (stream-K): the units of all 128-row tiles, tile-major, are cut into one
 // contiguous, equal range per CTA (one persistent CTA per SM), and each CTA's range into
@@ -62,8 +64,14 @@ struct GemvTmaArgs {
   int32_t* status;
 };
 
+// ring slot: the unit's code box, then the scales and the biases of its 128 rows for the two
+// chunks around it (boxes of 8 groups: the smallest inner extent a tensor copy takes)
+constexpr int kGvSbBox = kUnitRows * 8 * 2;
+constexpr int kGvSlot = kSlotBytes + 2 * kGvSbBox;
+
 struct CodeMaps {
   CUtensorMap codes[kMaxMats];   // uint32 [N][K/16], box 32 x 128, 128-byte swizzle
+  CUtensorMap sb[kMaxMats][2];   // fp16 scales, biases [N][G], box 8 x 128
 };
 
 // matrix of a global tile index
@@ -88,7 +96,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
   uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int DW = a.dw, C = a.C, G = a.G, K = a.K;
-  const GemvTmaLayout L = gemv_tma_layout<MT>(G, DW);
+  const GemvTmaLayout L = gemv_tma_layout<MT>(G, DW, kGvSlot);
   const uint32_t slots_u32 = smem_u32(smem + L.codes);
   __half* img = reinterpret_cast<__half*>(smem + L.img);
   float2* cs = reinterpret_cast<float2*>(smem + L.cs);    // [G][MT] = (1024 sum x'/sigma, sum x')
@@ -158,8 +166,12 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         if (k > 0) wait(empty + slot, (k - 1) & 1);
         const int mi = mat_of(a, tl);
         const int row = (tl - a.tile0[mi]) * kUnitRows;
-        mbar_arrive_expect_tx(full + slot, kSlotBytes);
-        tma2d(slots_u32 + slot * kSlotBytes, &maps.codes[mi], ch * 32, row, full + slot, pol);
+        const bool hb = a.biases[mi] != nullptr;
+        mbar_arrive_expect_tx(full + slot, kSlotBytes + (hb ? 2 : 1) * kGvSbBox);
+        const uint32_t dst = slots_u32 + slot * kGvSlot;
+        tma2d(dst, &maps.codes[mi], ch * 32, row, full + slot, pol);
+        tma2d(dst + kSlotBytes, &maps.sb[mi][0], 8 * (ch >> 1), row, full + slot, pol);
+        if (hb) tma2d(dst + kSlotBytes + kGvSbBox, &maps.sb[mi][1], 8 * (ch >> 1), row, full + slot, pol);
         step_unit(tl, ch, C, back);
         if (++si == DW) {
           si = 0;
@@ -189,36 +201,6 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     tile = first / C;
     chunk = first - tile * C;
   }
-  // scale / bias prefetch (rows 32*wi + lane of a unit), two units ahead of the one computed;
-  // the row's pointers are looked up only when the prefetch enters a new tile
-  int ptile = tile, pchunk = chunk, pn = 0, prow_tile = -1;
-  const __half* psrow = nullptr;
-  const __half* pbrow = nullptr;
-  auto load_sb = [&](uint2& sv, uint2& bv) {
-    sv = make_uint2(0, 0);
-    bv = make_uint2(0, 0);
-    if (pn < ncnt) {
-      if (ptile != prow_tile) {
-        prow_tile = ptile;
-        const int mi = mat_of(a, ptile);
-        const int row = (ptile - a.tile0[mi]) * kUnitRows + 32 * wi + lane;
-        const bool in = row < a.N[mi];
-        psrow = in ? a.scales[mi] + (int64_t)row * G : nullptr;
-        pbrow = in && a.biases[mi] ? a.biases[mi] + (int64_t)row * G : nullptr;
-      }
-      if (psrow) {
-        sv = __ldg(reinterpret_cast<const uint2*>(psrow + pchunk * kUnitGroups));
-        // no biases given: each is the pack's -scale (the fp16 sign bit flipped), not read
-        bv = pbrow ? __ldg(reinterpret_cast<const uint2*>(pbrow + pchunk * kUnitGroups))
-                   : make_uint2(sv.x ^ 0x80008000u, sv.y ^ 0x80008000u);
-      }
-    }
-    ++pn;
-    step_unit(ptile, pchunk, C, back);
-  };
-  uint2 sA, bA, sB, bB;
-  load_sb(sA, bA);
-  load_sb(sB, bB);
   if (a.signs) {  // the signs never depend on the previous kernel: into L1 before the wait
     int pb1, pe1, pb2, pe2;
     blocks_needed(lo, nst, C, K, pb1, pe1, pb2, pe2);
@@ -491,8 +473,19 @@ __global__ void __launch_bounds__(kWsThreads, 1)
   int si = 0;        // ring slot of the current unit within the group's DW slots: n % DW
   uint32_t ph = 0;   // its fill parity: (n / DW) & 1
   // unit n with its scales and biases in (sv, bv), which are then reloaded for unit n + 2
-  auto body = [&](int n, uint2& sv, uint2& bv) {
-    {
+  auto body = [&](int n) {
+    const int slot = ug * DW + si;
+    wait(full + slot, ph);
+    if (++si == DW) {
+      si = 0;
+      ph ^= 1;
+    }
+    const uint32_t box = slots_u32 + slot * kGvSlot;
+    {  // this warp's 32 rows' (s, b) of the unit's four groups, from the slot, as fp32 pairs
+      const uint32_t sp = box + kSlotBytes + (32 * wi + lane) * 16 + (chunk & 1) * 8;
+      const uint2 sv = ld_shared_v2(sp);
+      const uint2 bv = a.biases[mat_of(a, tile)] ? ld_shared_v2(sp + kGvSbBox)
+                                                 : make_uint2(sv.x ^ 0x80008000u, sv.y ^ 0x80008000u);
       const uint32_t r = ss + lane * kUnitGroups * 8;
       const float2 sf0 = __half22float2(*reinterpret_cast<const __half2*>(&sv.x));
       const float2 sf1 = __half22float2(*reinterpret_cast<const __half2*>(&sv.y));
@@ -502,21 +495,11 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       asm volatile("st.shared.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(r + 16), "f"(sf1.x), "f"(bf1.x), "f"(sf1.y), "f"(bf1.y) : "memory");
       __syncwarp();
     }
-    const int slot = ug * DW + si;
-    wait(full + slot, ph);
-    if (++si == DW) {
-      si = 0;
-      ph ^= 1;
-    }
-    const uint32_t box = slots_u32 + slot * kSlotBytes;
 #pragma unroll
     for (int gi = 0; gi < kUnitGroups; ++gi)
       unit_group<MT>(box, R0, t, gi, chunk * kUnitGroups + gi, imgt, ss, rA, csa, t0, t1, acc);
     __syncwarp();
     if (lane == 0) mbar_arrive(empty + slot);
-    // the next loads are issued only after the release of the slot, which would otherwise
-    // wait for them to complete
-    load_sb(sv, bv);
     const int cur = tile;
     step_unit(tile, chunk, C, back);
     if (tile != cur || n == ncnt - 1) {
@@ -527,10 +510,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         for (int e = 0; e < 4; ++e) acc[j][e] = 0.f;
     }
   };
-  for (int n = 0; n < ncnt; n += 2) {  // two bodies per pass: no register copies between loads
-    body(n, sA, bA);
-    if (n + 1 < ncnt) body(n + 1, sB, bB);
-  }
+  for (int n = 0; n < ncnt; ++n) body(n);
 }
 
 // ------------------------------------------------------------------ host side
@@ -609,10 +589,10 @@ static int launch_tma_mt(GemvTmaArgs a, const CodeMaps& maps, int64_t M, int64_t
                          const DeviceFacts& f, cudaStream_t s) {
   // slots per unit group from what is left of shared memory
   int dw = kMaxSlotsPerGroup;
-  while (dw >= 1 && gemv_tma_layout<MT>(a.G, dw).total > f.smem_optin) --dw;
+  while (dw >= 1 && gemv_tma_layout<MT>(a.G, dw, kGvSlot).total > f.smem_optin) --dw;
   if (dw < 1) return TB_ERR_SHAPE;
   a.dw = dw;
-  const int bytes = gemv_tma_layout<MT>(a.G, dw).total;
+  const int bytes = gemv_tma_layout<MT>(a.G, dw, kGvSlot).total;
   cudaError_t e = cudaFuncSetAttribute(w2_gemv_tma_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e != cudaSuccess) {
     record_cuda_error(e);
@@ -654,13 +634,53 @@ static int tma_tokens_per_pass(int64_t M, int G, int smem_optin) {
   int mt = M >= 5 ? 8 : M >= 3 ? 4 : M == 2 ? 2 : 1;
   auto fits = [&](int total) { return total <= smem_optin; };
   while (mt > 1) {
-    const bool ok = mt == 8 ? fits(gemv_tma_layout<8>(G, 2).total)
-                  : mt == 4 ? fits(gemv_tma_layout<4>(G, 2).total)
-                            : fits(gemv_tma_layout<2>(G, 2).total);
+    const bool ok = mt == 8 ? fits(gemv_tma_layout<8>(G, 2, kGvSlot).total)
+                  : mt == 4 ? fits(gemv_tma_layout<4>(G, 2, kGvSlot).total)
+                            : fits(gemv_tma_layout<2>(G, 2, kGvSlot).total);
     if (ok) break;
     mt >>= 1;
   }
   return mt;
+}
+
+// tensor map of a [N, G] fp16 array of scales or biases (box 8 groups x 128 rows, no swizzle),
+// cached by (pointer, shape)
+int group_map(const __half* p, int64_t N, int64_t G, CUtensorMap* out) {
+  struct Key {
+    const void* p;
+    int64_t N, G;
+    bool operator==(const Key& o) const { return p == o.p && N == o.N && G == o.G; }
+  };
+  struct Hash {
+    size_t operator()(const Key& k) const { return std::hash<const void*>()(k.p) ^ std::hash<int64_t>()(k.N * 131 + k.G); }
+  };
+  static std::mutex mu;
+  static std::unordered_map<Key, CUtensorMap, Hash> cache;
+  const Key key{p, N, G};
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) {
+      *out = it->second;
+      return TB_OK;
+    }
+  }
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return TB_ERR_CUDA;
+  CUtensorMap m;
+  const cuuint64_t dims[2] = {(cuuint64_t)G, (cuuint64_t)N};
+  const cuuint64_t strides[1] = {(cuuint64_t)G * 2};
+  const cuuint32_t box[2] = {8, (cuuint32_t)kUnitRows};
+  const cuuint32_t es[2] = {1, 1};
+  if (enc(&m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<__half*>(p), dims, strides, box, es,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return TB_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache.size() > 4096) cache.clear();
+  cache[key] = m;
+  *out = m;
+  return TB_OK;
 }
 
 // One launch for up to kMaxMats packed matrices that read the same x (their row tiles are
@@ -680,6 +700,9 @@ int launch_gemv_tma_multi(const __half* x, int64_t M, int64_t K, const int8_t* s
   for (int i = 0; i < nmat; ++i) {
     if (N[i] < 1 || N[i] > (1LL << 30)) return TB_ERR_SHAPE;
     rc = code_map(w[i], N[i], K, &maps.codes[i]);
+    if (rc == TB_OK) rc = group_map(scales[i], N[i], K / kGroup, &maps.sb[i][0]);
+    if (rc == TB_OK) rc = biases[i] ? group_map(biases[i], N[i], K / kGroup, &maps.sb[i][1]) : TB_OK;
+    if (!biases[i]) maps.sb[i][1] = maps.sb[i][0];
     if (rc != TB_OK) return rc;
     a.scales[i] = scales[i];
     a.biases[i] = biases[i];
@@ -691,7 +714,11 @@ int launch_gemv_tma_multi(const __half* x, int64_t M, int64_t K, const int8_t* s
   // unit indices (tiles x K/512) are 32-bit in the kernel
   if (tiles * (K / (kUnitGroups * kGroup)) > (int64_t)INT32_MAX / 2) return TB_ERR_SHAPE;
   for (int i = nmat; i <= kMaxMats; ++i) a.tile0[i] = (int)tiles;
-  for (int i = nmat; i < kMaxMats; ++i) maps.codes[i] = maps.codes[0];
+  for (int i = nmat; i < kMaxMats; ++i) {
+    maps.codes[i] = maps.codes[0];
+    maps.sb[i][0] = maps.sb[0][0];
+    maps.sb[i][1] = maps.sb[0][1];
+  }
   a.nmat = nmat;
   a.x = x;
   a.signs = signs;
