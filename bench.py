@@ -33,10 +33,10 @@ METRIC = "decode tok/s at 27B shapes (M=1) + fused W2 GEMV HBM GB/s as % of GB30
 # DRAM bytes (read + write) of one chain launch from an ncu capture, or None until taken
 CHAIN_TRAFFIC = None
 # DRAM bytes per launch of the per-call decode GEMV over its algorithmic bytes, from an ncu
-# capture (dram__bytes_read.sum + dram__bytes_write.sum) of the kernel as it is now:
-# 25,166,080 B read, 0 written, for 25,067,520 B of 5120 -> 17408 weights
-# (profiles/w2_gemv_tma_5120x17408_traffic.md).
-GEMV_TRAFFIC_RATIO = 25166080 / 25067520
+# capture (dram__bytes_read.sum + dram__bytes_write.sum) of the kernel as it is now (scales and
+# biases in the TMA ring): 25,150,208 B read, 0 written, for 25,067,520 B of 5120 -> 17408
+# weights (profiles/w2_gemv_tma_5120x17408_traffic.md).
+GEMV_TRAFFIC_RATIO = 25150208 / 25067520
 GEMV_TRAFFIC_NOTE = "not captured"
 CHAIN_TRAFFIC_NOTE = "not captured yet for this kernel"
 FALLBACK_HBM_GBS = 6800.0
