@@ -3,6 +3,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <map>
 #include <mutex>
 
 #include "tb_host.h"
@@ -14,6 +15,21 @@ static thread_local char g_last_cuda_error[256] = "";
 void record_cuda_error(cudaError_t e) {
   snprintf(g_last_cuda_error, sizeof(g_last_cuda_error), "%s: %s", cudaGetErrorName(e),
            cudaGetErrorString(e));
+}
+
+int ensure_dynamic_smem(const void* func, int device, int bytes) {
+  static std::mutex mu;
+  static std::map<std::pair<const void*, int>, int> set;
+  std::lock_guard<std::mutex> lock(mu);
+  int& have = set[{func, device}];
+  if (have >= bytes) return TB_OK;
+  const cudaError_t e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) {
+    record_cuda_error(e);
+    return TB_ERR_CUDA;
+  }
+  have = bytes;
+  return TB_OK;
 }
 
 int device_facts(DeviceFacts* f) {

@@ -39,6 +39,13 @@
 namespace tb {
 
 int code_map(const uint32_t* w, int64_t N, int64_t K, CUtensorMap* out);
+int group_map(const __half* p, int64_t N, int64_t G, CUtensorMap* out);
+
+// ring slot: a unit's code box, then the scales and the biases of its 128 rows for its chunk and
+// the neighbouring one (TMA boxes of 8 groups: a tensor copy's inner extent is at least 16 bytes)
+constexpr int kChSbBox = kUnitRows * 8 * 2;
+constexpr int kChSlot = kSlotBytes + 2 * kChSbBox;
+constexpr int kChMapsPerMat = 3;  // codes, scales, biases (the scales' map again without biases)
 
 constexpr uint32_t kChainMagic = 0x54424348u;  // "TBCH"
 constexpr int kChainMaxCtas = 256;                // parts slots of the fixup region
@@ -145,7 +152,7 @@ __global__ void __launch_bounds__(kChainThreads, 1) w2_gemv_chain_kernel(const _
   uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int DW = a.dw;
-  const GemvTmaLayout L = gemv_tma_layout<MT>(a.max_K / kGroup, DW);
+  const GemvTmaLayout L = gemv_tma_layout<MT>(a.max_K / kGroup, DW, kChSlot);
   const uint32_t slots_u32 = smem_u32(smem + L.codes);
   __half* img = reinterpret_cast<__half*>(smem + L.img);
   float2* cs = reinterpret_cast<float2*>(smem + L.cs);
@@ -200,7 +207,7 @@ __global__ void __launch_bounds__(kChainThreads, 1) w2_gemv_chain_kernel(const _
         int tile0[kMaxMats + 1];
 #pragma unroll
         for (int k = 0; k <= kMaxMats; ++k) tile0[k] = lk->tile0[k];
-        const CUtensorMap* maps = a.maps + lk->map0;
+        const CUtensorMap* maps = a.maps + kChMapsPerMat * lk->map0;
         const LinkRange r = link_range(lk->n_tiles, C);
         int tl[kGroupsOfWarps], ch[kGroupsOfWarps], cntu[kGroupsOfWarps];
         int maxcnt = 0;
@@ -223,8 +230,13 @@ __global__ void __launch_bounds__(kChainThreads, 1) w2_gemv_chain_kernel(const _
             if (kf[u] > 0) wait(empty + slot, (kf[u] - 1) & 1);
             const int mi = link_mat_of(tile0, nmat, tl[u]);
             const int row = (tl[u] - tile0[mi]) * kUnitRows;
-            mbar_arrive_expect_tx(full + slot, kSlotBytes);
-            tma2d(slots_u32 + slot * kSlotBytes, maps + mi, ch[u] * 32, row, full + slot, pol);
+            const bool hb = lk->biases[mi] != nullptr;
+            mbar_arrive_expect_tx(full + slot, kSlotBytes + (hb ? 2 : 1) * kChSbBox);
+            const uint32_t dst = slots_u32 + slot * kChSlot;
+            const CUtensorMap* mm = maps + kChMapsPerMat * mi;
+            tma2d(dst, mm, ch[u] * 32, row, full + slot, pol);
+            tma2d(dst + kSlotBytes, mm + 1, 8 * (ch[u] >> 1), row, full + slot, pol);
+            if (hb) tma2d(dst + kSlotBytes + kChSbBox, mm + 2, 8 * (ch[u] >> 1), row, full + slot, pol);
             step_unit(tl[u], ch[u], C, u == kGroupsOfWarps - 1);
             if (++si[u] == DW) {
               si[u] = 0;
@@ -268,7 +280,7 @@ __global__ void __launch_bounds__(kChainThreads, 1) w2_gemv_chain_kernel(const _
 
   for (int li = 0; li < a.n_links; ++li) {
     const ChainLink* lk = links + li;
-    const int C = lk->C, G = lk->G, K = lk->K;
+    const int C = lk->C, K = lk->K;
     const int S = lk->n_tiles * C;
     const LinkRange r = link_range(lk->n_tiles, C);
     // everything the prologue needs but x itself is read before the wait on the previous link
@@ -298,36 +310,6 @@ __global__ void __launch_bounds__(kChainThreads, 1) w2_gemv_chain_kernel(const _
       tile = first / C;
       chunk = first - tile * C;
     }
-    // scale / bias prefetch (rows 32*wi + lane of a unit), two units ahead of the one computed
-    int ptile = tile, pchunk = chunk, pn = 0, prow_tile = -1;
-    const __half* psrow = nullptr;
-    const __half* pbrow = nullptr;
-    auto load_sb = [&](uint2& sv, uint2& bv) {
-      sv = make_uint2(0, 0);
-      bv = make_uint2(0, 0);
-      if (pn < ncnt) {
-        if (ptile != prow_tile) {
-          prow_tile = ptile;
-          int t0m;
-          const int mi = link_mat_of_g(lk, ptile, t0m);
-          const int row = (ptile - t0m) * kUnitRows + 32 * wi + lane;
-          const bool in = row < lk->N[mi];
-          psrow = in ? lk->scales[mi] + (int64_t)row * G : nullptr;
-          pbrow = in && lk->biases[mi] ? lk->biases[mi] + (int64_t)row * G : nullptr;
-        }
-        if (psrow) {
-          sv = __ldg(reinterpret_cast<const uint2*>(psrow + pchunk * kUnitGroups));
-          // no biases given: each is the pack's -scale (the fp16 sign bit flipped), not read
-          bv = pbrow ? __ldg(reinterpret_cast<const uint2*>(pbrow + pchunk * kUnitGroups))
-                     : make_uint2(sv.x ^ 0x80008000u, sv.y ^ 0x80008000u);
-        }
-      }
-      ++pn;
-      step_unit(ptile, pchunk, C, back);
-    };
-    uint2 sA, bA, sB, bB;
-    load_sb(sA, bA);
-    load_sb(sB, bB);
 
     // x of this link may be an output of the previous one: wait until every CTA has
     // counted that link complete
@@ -352,7 +334,7 @@ __global__ void __launch_bounds__(kChainThreads, 1) w2_gemv_chain_kernel(const _
       // scratch of the transform: the slot after the one that holds this group's first unit
       // of the link; the producer fills it only after every consumer warp has arrived on
       // xready for this link
-      const uint32_t scratch = slots_u32 + (ug * DW + (si + 1 == DW ? 0 : si + 1)) * kSlotBytes + wi * 4096;
+      const uint32_t scratch = slots_u32 + (ug * DW + (si + 1 == DW ? 0 : si + 1)) * kChSlot + wi * 4096;
       prologue_image<MT>(lx, lsg, K, Mc, lrot, b1, e1, b2, e2, warp, kTmaConsumers, lane, img, cs, scratch);
     }
     fence_proxy_async_smem();  // the scratch's generic accesses before the copies that refill it
@@ -474,8 +456,26 @@ __global__ void __launch_bounds__(kChainThreads, 1) w2_gemv_chain_kernel(const _
     };
 
     float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-    auto body = [&](int n, uint2& sv, uint2& bv) {
-      {
+    int hb_tile = -1;
+    bool has_b = true;
+    auto body = [&](int n) {
+      const int slot = ug * DW + si;
+      wait(full + slot, ph);
+      if (++si == DW) {
+        si = 0;
+        ph ^= 1;
+      }
+      const uint32_t box = slots_u32 + slot * kChSlot;
+      {  // this warp's 32 rows' (s, b) of the unit's four groups, from the slot, as fp32 pairs
+        if (tile != hb_tile) {  // whether the tile's matrix has biases, looked up per tile
+          hb_tile = tile;
+          int t0m;
+          has_b = lk->biases[link_mat_of_g(lk, tile, t0m)] != nullptr;
+        }
+        const uint32_t sp = box + kSlotBytes + (32 * wi + lane) * 16 + (chunk & 1) * 8;
+        const uint2 sv = ld_shared_v2(sp);
+        // no biases given: each is the pack's -scale (the fp16 sign bit flipped)
+        const uint2 bv = has_b ? ld_shared_v2(sp + kChSbBox) : make_uint2(sv.x ^ 0x80008000u, sv.y ^ 0x80008000u);
         const uint32_t rr = ss + lane * kUnitGroups * 8;
         const float2 sf0 = __half22float2(*reinterpret_cast<const __half2*>(&sv.x));
         const float2 sf1 = __half22float2(*reinterpret_cast<const __half2*>(&sv.y));
@@ -485,19 +485,11 @@ __global__ void __launch_bounds__(kChainThreads, 1) w2_gemv_chain_kernel(const _
         asm volatile("st.shared.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(rr + 16), "f"(sf1.x), "f"(bf1.x), "f"(sf1.y), "f"(bf1.y) : "memory");
         __syncwarp();
       }
-      const int slot = ug * DW + si;
-      wait(full + slot, ph);
-      if (++si == DW) {
-        si = 0;
-        ph ^= 1;
-      }
-      const uint32_t box = slots_u32 + slot * kSlotBytes;
 #pragma unroll
       for (int gi = 0; gi < kUnitGroups; ++gi)
         unit_group<MT>(box, R0, t, gi, chunk * kUnitGroups + gi, imgt, ss, rA, csa, t0, t1, acc);
       __syncwarp();
       if (lane == 0) mbar_arrive(empty + slot);
-      load_sb(sv, bv);
       const int cur = tile;
       step_unit(tile, chunk, C, back);
       if (tile != cur || n == ncnt - 1) {
@@ -508,10 +500,7 @@ __global__ void __launch_bounds__(kChainThreads, 1) w2_gemv_chain_kernel(const _
           for (int e = 0; e < 4; ++e) acc[j][e] = 0.f;
       }
     };
-    for (int n = 0; n < ncnt; n += 2) {
-      body(n, sA, bA);
-      if (n + 1 < ncnt) body(n + 1, sB, bB);
-    }
+    for (int n = 0; n < ncnt; ++n) body(n);
 
     // every output of this link from this CTA is written: count the link complete (a release
     // reduction: the CTA's writes, ordered before it by the barrier, become visible first; the
@@ -533,7 +522,7 @@ __global__ void __launch_bounds__(kChainThreads, 1) w2_gemv_chain_kernel(const _
 
 // ------------------------------------------------------------------ host side
 static size_t plan_bytes_for(int n_links, int n_maps) {
-  return sizeof(ChainHeader) + 64 + (size_t)n_maps * sizeof(CUtensorMap) +
+  return sizeof(ChainHeader) + 64 + (size_t)n_maps * kChMapsPerMat * sizeof(CUtensorMap) +
          (size_t)n_links * sizeof(ChainLink);
 }
 
@@ -542,7 +531,7 @@ static int tokens_per_pass(int64_t M) { return M >= 5 ? 8 : M >= 3 ? 4 : M == 2 
 template <int MT>
 static int chain_slots(int max_K, int smem_optin) {
   int dw = kMaxSlotsPerGroup;
-  while (dw >= 2 && gemv_tma_layout<MT>(max_K / kGroup, dw).total > smem_optin) --dw;
+  while (dw >= 2 && gemv_tma_layout<MT>(max_K / kGroup, dw, kChSlot).total > smem_optin) --dw;
   return dw >= 2 ? dw : 0;
 }
 
@@ -557,7 +546,7 @@ static int chain_slots_for(int mt, int max_K, int smem_optin) {
 
 template <int MT>
 static int launch_chain_mt(const ChainRun& a, int grid, cudaStream_t s) {
-  const int bytes = gemv_tma_layout<MT>(a.max_K / kGroup, a.dw).total;
+  const int bytes = gemv_tma_layout<MT>(a.max_K / kGroup, a.dw, kChSlot).total;
   cudaError_t e = cudaFuncSetAttribute(w2_gemv_chain_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e != cudaSuccess) {
     record_cuda_error(e);
@@ -630,7 +619,7 @@ extern "C" int tb_chain_plan(const tb_chain_link* links, int n_links, int64_t M,
   h.M = (int32_t)M;
   h.max_K = (int32_t)max_K;
   h.maps_off = 128;  // 128-byte aligned tensor maps (a TMA descriptor needs 64)
-  h.links_off = h.maps_off + (int64_t)n_maps * sizeof(CUtensorMap);
+  h.links_off = h.maps_off + (int64_t)n_maps * kChMapsPerMat * sizeof(CUtensorMap);
   h.bytes = (int64_t)need;
   memcpy(host.data(), &h, sizeof(h));
   CUtensorMap* maps = reinterpret_cast<CUtensorMap*>(host.data() + h.maps_off);
@@ -643,7 +632,12 @@ extern "C" int tb_chain_plan(const tb_chain_link* links, int n_links, int64_t M,
     int64_t tiles = 0;
     for (int j = 0; j < kMaxMats; ++j) {
       if (j < l.n) {
-        int rc = code_map(l.w[j], l.N[j], l.K, &maps[map + j]);
+        CUtensorMap* mm = &maps[kChMapsPerMat * (map + j)];
+        int rc = code_map(l.w[j], l.N[j], l.K, mm);
+        if (rc == TB_OK) rc = group_map(reinterpret_cast<const __half*>(l.scales[j]), l.N[j], l.K / kGroup, mm + 1);
+        if (rc == TB_OK && l.biases[j])
+          rc = group_map(reinterpret_cast<const __half*>(l.biases[j]), l.N[j], l.K / kGroup, mm + 2);
+        if (!l.biases[j]) mm[2] = mm[1];
         if (rc != TB_OK) return rc;
         d.scales[j] = reinterpret_cast<const __half*>(l.scales[j]);
         d.biases[j] = reinterpret_cast<const __half*>(l.biases[j]);

@@ -459,15 +459,13 @@ int launch_batch_image(const __half* x, int64_t M, int64_t K, const int8_t* sign
 
 template <int NT>
 static int launch_batch_nt(const CUtensorMap& map, const CUtensorMap& smap, const CUtensorMap& bmap, BatchArgs a, const uint8_t* blob0, int64_t M, int grid,
-                           int smem_optin, cudaStream_t s) {
+                           int smem_optin, int device, cudaStream_t s) {
   constexpr int MT = 8 * NT;
   constexpr int bytes = bt_smem_bytes(MT);
   if (bytes > smem_optin) return TB_ERR_UNSUPPORTED;
-  cudaError_t e = cudaFuncSetAttribute(w2_gemv_batch_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e != cudaSuccess) {
-    record_cuda_error(e);
-    return TB_ERR_CUDA;
-  }
+  const int rc = ensure_dynamic_smem(reinterpret_cast<const void*>(w2_gemv_batch_kernel<NT>), device, bytes);
+  if (rc != TB_OK) return rc;
+  cudaError_t e;
   __half* y0 = a.y;
   for (int64_t m0 = 0; m0 < M; m0 += MT) {
     a.y = y0 + m0 * a.N;
@@ -525,10 +523,10 @@ int launch_batch_gemv(int64_t M, int64_t K, const uint32_t* w, const __half* sca
   const int64_t S = tiles * C;
   const int grid = (int)(S < f.sms ? S : f.sms);
   switch (NT) {
-    case 1: return launch_batch_nt<1>(map, smap, bmap, a, blob0, M, grid, f.smem_optin, s);
-    case 2: return launch_batch_nt<2>(map, smap, bmap, a, blob0, M, grid, f.smem_optin, s);
-    case 4: return launch_batch_nt<4>(map, smap, bmap, a, blob0, M, grid, f.smem_optin, s);
-    default: return launch_batch_nt<8>(map, smap, bmap, a, blob0, M, grid, f.smem_optin, s);
+    case 1: return launch_batch_nt<1>(map, smap, bmap, a, blob0, M, grid, f.smem_optin, f.device, s);
+    case 2: return launch_batch_nt<2>(map, smap, bmap, a, blob0, M, grid, f.smem_optin, f.device, s);
+    case 4: return launch_batch_nt<4>(map, smap, bmap, a, blob0, M, grid, f.smem_optin, f.device, s);
+    default: return launch_batch_nt<8>(map, smap, bmap, a, blob0, M, grid, f.smem_optin, f.device, s);
   }
 }
 

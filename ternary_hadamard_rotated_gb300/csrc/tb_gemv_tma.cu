@@ -593,11 +593,9 @@ static int launch_tma_mt(GemvTmaArgs a, const CodeMaps& maps, int64_t M, int64_t
   if (dw < 1) return TB_ERR_SHAPE;
   a.dw = dw;
   const int bytes = gemv_tma_layout<MT>(a.G, dw, kGvSlot).total;
-  cudaError_t e = cudaFuncSetAttribute(w2_gemv_tma_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e != cudaSuccess) {
-    record_cuda_error(e);
-    return TB_ERR_CUDA;
-  }
+  int rc = ensure_dynamic_smem(reinterpret_cast<const void*>(w2_gemv_tma_kernel<MT>), f.device, bytes);
+  if (rc != TB_OK) return rc;
+  cudaError_t e;
   const int64_t S = (int64_t)a.n_tiles * a.C;
   int grid = f.sms;
   if (!a.split && a.n_tiles < grid) grid = a.n_tiles;

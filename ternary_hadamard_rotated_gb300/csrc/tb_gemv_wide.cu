@@ -431,14 +431,12 @@ __global__ void __launch_bounds__(kWdThreads, 1)
 
 template <int MT>
 static int launch_wide_mt(const CUtensorMap& cmap, const CUtensorMap& xmap, const WideArgs& a, int grid,
-                          int smem_optin, cudaStream_t s) {
+                          int smem_optin, int device, cudaStream_t s) {
   constexpr int bytes = wide_layout<MT>().total;
   if (bytes > smem_optin) return TB_ERR_UNSUPPORTED;
-  cudaError_t e = cudaFuncSetAttribute(w2_gemv_wide_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e != cudaSuccess) {
-    record_cuda_error(e);
-    return TB_ERR_CUDA;
-  }
+  const int rc = ensure_dynamic_smem(reinterpret_cast<const void*>(w2_gemv_wide_kernel<MT>), device, bytes);
+  if (rc != TB_OK) return rc;
+  cudaError_t e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kWdThreads);
@@ -508,10 +506,10 @@ int launch_gemv_wide(const __half* xp, int64_t M, int64_t K, const uint32_t* w, 
   const int64_t S = tiles * C;
   const int grid = (int)(S < f.sms ? S : f.sms);
   switch (MT) {
-    case 16: return launch_wide_mt<16>(cmap, xmap, a, grid, f.smem_optin, s);
-    case 32: return launch_wide_mt<32>(cmap, xmap, a, grid, f.smem_optin, s);
-    case 48: return launch_wide_mt<48>(cmap, xmap, a, grid, f.smem_optin, s);
-    default: return launch_wide_mt<64>(cmap, xmap, a, grid, f.smem_optin, s);
+    case 16: return launch_wide_mt<16>(cmap, xmap, a, grid, f.smem_optin, f.device, s);
+    case 32: return launch_wide_mt<32>(cmap, xmap, a, grid, f.smem_optin, f.device, s);
+    case 48: return launch_wide_mt<48>(cmap, xmap, a, grid, f.smem_optin, f.device, s);
+    default: return launch_wide_mt<64>(cmap, xmap, a, grid, f.smem_optin, f.device, s);
   }
 }
 

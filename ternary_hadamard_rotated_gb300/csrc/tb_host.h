@@ -45,4 +45,9 @@ struct DeviceFacts {
 };
 int device_facts(DeviceFacts* f);
 
+// cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes), made only when
+// bytes exceeds what was set before for this kernel on this device (a driver call per launch
+// costs host time that a stream of small launches does not hide)
+int ensure_dynamic_smem(const void* func, int device, int bytes);
+
 }  // namespace tb
