@@ -16,8 +16,9 @@
 //    packed codes (TMA, 128-byte swizzle), the 128 rows' scales and biases of two chunks (TMA
 //    boxes of 8 groups: the smallest the copy engine takes) and the chunk's blob (one bulk
 //    copy) into one ring slot, so the consumers issue no global loads (a fence on their path
-//    would wait for any still in flight); eight consumer warps of 16 rows each decode their codes once per group (LOP3 into
-//    fp16 1024 + sigma*q) and run them against the NT token tiles of the blob:
+//    would wait for any still in flight); eight consumer warps of 16 rows each decode their
+//    codes once per group (LOP3 into fp16 1024 + sigma*q) and run them against the NT token
+//    tiles of the blob:
 //      y[row, tok] += s * (D - C) + b * S   per group of 128,
 //    D the group's mma sum starting from zero.  A tile that lies wholly in the CTA's range is
 //    written from registers; a tile cut by a range boundary goes through the workspace (each
@@ -54,7 +55,8 @@ __host__ __device__ constexpr int bt_blob_bytes(int MT) { return 1024 * MT + 32 
 __host__ __device__ constexpr int bt_slot_bytes(int MT) {
   return (kBtBlobOff + bt_blob_bytes(MT) + 1023) / 1024 * 1024;  // codes stay 1024-aligned
 }
-// ring slots per token count: four while they leave room for the L1, fewer for wide blobs
+// ring slots per token count: four up to 16 tokens (five or six measured the same), fewer as
+// the blobs widen
 __host__ __device__ constexpr int bt_slots(int MT) { return MT <= 16 ? 4 : MT <= 32 ? 3 : 2; }
 __host__ __device__ constexpr int bt_smem_bytes(int MT) {
   return bt_slots(MT) * bt_slot_bytes(MT) + 2 * 4 * 8 + 1024;
