@@ -81,7 +81,7 @@ def test_linear_other_blocks(tb, block, M, K, N, algo, scale_only):
     assert_linear_close(y.cpu().numpy(), ref, bound, f"block {block} {M}x{K}x{N} algo={algo}")
 
 
-@pytest.mark.parametrize("M", [1, 64])
+@pytest.mark.parametrize("M", [1, 16, 64])  # the decode GEMV, the batched GEMV, the tensor-memory one
 def test_multi_other_block(tb, M):
     K, Ns, block = 4096, (300, 1000), 2048
     x = ti.activations(620 + M, M, K)
