@@ -106,6 +106,9 @@ def test_workspace_size_query(lib):
     assert ws(3, 17408, 5120, 1024) == fix + batch(3, 17408)
     assert ws(32, 5120, 6144, 1024) == fix + batch(32, 5120)
     assert lib.tb_packed_linear_algo_workspace_size(100, 2048, 64, 1024, 6) == fix + batch(100, 2048)
+    # a block that is not fused: x' in natural order (fp16 [M, K], 1 KB rounded) after the region
+    assert ws(16, 4096, 1000, 2048) == fix + batch(16, 4096) + (16 * 4096 * 2 + 1023) // 1024 * 1024
+    assert ws(16, 1000, 1000, 2048) == 0            # K not a multiple of the block
     # tensor-core path: x' (fp16 [M, K]), two int32 counters per 128 x 128 output tile (claims
     # of a split tile, parts written), then two fp32 256 x 256 parts per SM for the stream-K
     # schedule's split tiles (with no GPU visible the bound is 256 SMs), each region rounded up
